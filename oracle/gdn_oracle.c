@@ -197,6 +197,7 @@ void oracle_conv_update(int CH, int K, const uint16_t *x, const float *w, uint16
         if (slot < 0) continue;
         int t0 = qsl[n], L = qsl[n + 1] - qsl[n];
         int init = has_init ? has_init[n] : 1;
+        if (L <= 0) continue; /* no tokens: the slot is left untouched */
         for (int c = 0; c < CH; ++c) {
             uint16_t *h = hist_pool + ((int64_t)slot * CH + c) * (K - 1);
             uint16_t hn[16];

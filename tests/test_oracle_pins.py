@@ -378,3 +378,17 @@ def test_forward_write_through_needs_unit_q_and_k():
     r = _fwd(w2, np.array([0, T], np.int32), np.array([0], np.int32), want_y=True)
     v = r["y"][:, 2 * Hk * dk :].reshape(T, TINY.num_v_heads, TINY.head_v_dim)
     np.testing.assert_allclose(r["o"] * np.sqrt(dk), v, rtol=1e-11, atol=1e-12)
+
+
+def test_empty_request_leaves_its_slot_untouched():
+    """A request with no tokens reads and writes nothing, with or without an initial state."""
+    w = _tiny_inputs(26, T=3)
+    qsl = np.array([0, 0, 3], np.int32)
+    slots = np.array([1, 2], np.int32)
+    for init in (0, 1):
+        r = _fwd(w, qsl, slots, has_init=np.array([init, 1], np.uint8))
+        np.testing.assert_array_equal(r["state"][1], w["state"][1])
+        np.testing.assert_array_equal(r["conv_hist"][1], w["conv_hist"][1])
+        _, h = oracle.conv_update(TINY, w["qkv0"], w["conv_w"], w["conv_hist"], qsl, slots,
+                                  np.array([init, 1], np.uint8))
+        np.testing.assert_array_equal(h[1], w["conv_hist"][1])
