@@ -1,0 +1,226 @@
+// api.cu - the extern "C" entry points of libgdn: argument validation on the
+// host, then one launch on the caller's stream. Declarations and the full
+// contract of every entry point are in include/gdn.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <unordered_map>
+
+#include "device.cuh"
+#include "gdn.h"
+#include "launch.h"
+
+namespace gdn {
+
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, uint64_t> done;  // function -> bitmask of devices
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(fn);
+    if (bit && it != done.end() && (it->second & bit)) return cudaSuccess;
+  }
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  done[fn] |= bit;
+  return cudaSuccess;
+}
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Geometry check shared by every call that takes gdn_dims.
+gdn_status check_dims(const gdn_dims* d) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->num_k_heads <= 0 || d->num_v_heads <= 0 || d->head_k_dim <= 0 || d->head_v_dim <= 0 ||
+      d->conv_kernel <= 0 || d->num_slots <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (d->head_k_dim != kHeadDim || d->head_v_dim != kHeadDim || d->conv_kernel != kTaps)
+    return GDN_ERR_UNSUPPORTED;
+  if (d->num_v_heads % d->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+  if (d->num_v_heads / d->num_k_heads > kMaxGroup) return GDN_ERR_UNSUPPORTED;
+  if (d->num_v_heads > 65535) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+int channels(const gdn_dims* d) {
+  return 2 * d->num_k_heads * d->head_k_dim + d->num_v_heads * d->head_v_dim;
+}
+
+bool eps_ok(float eps) { return std::isfinite(eps) && eps >= 0.f; }
+
+gdn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+size_t gdn_state_bytes(const gdn_dims* d) {
+  if (!d || d->num_v_heads <= 0 || d->head_v_dim <= 0 || d->head_k_dim <= 0) return 0;
+  return (size_t)d->num_v_heads * d->head_v_dim * d->head_k_dim * sizeof(float);
+}
+
+size_t gdn_conv_hist_bytes(const gdn_dims* d) {
+  if (!d || d->num_k_heads <= 0 || d->num_v_heads <= 0 || d->head_k_dim <= 0 || d->head_v_dim <= 0 ||
+      d->conv_kernel <= 1)
+    return 0;
+  return (size_t)channels(d) * (d->conv_kernel - 1) * sizeof(uint16_t);
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_dims* d, int32_t num_seqs, int32_t num_tokens) {
+  (void)d;
+  (void)num_seqs;
+  (void)num_tokens;
+  return 0;
+}
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported geometry";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime or launch failure";
+    case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK: the device flagged an invalid index";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait ran out";
+  }
+  return "unknown gdn_status";
+}
+
+gdn_status gdn_read_device_error(int32_t* dev_err, int32_t* host_err, int32_t reset, void* stream) {
+  if (!dev_err || !host_err) return GDN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_err, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (reset && v != 0) {
+    if (cudaMemsetAsync(dev_err, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  *host_err = v;
+  if (v == 0) return GDN_OK;
+  return (v & GDN_DEVERR_TIMEOUT) ? GDN_ERR_TIMEOUT : GDN_ERR_DEVICE_CHECK;
+}
+
+gdn_status gdn_conv_update(const gdn_dims* d, const uint16_t* x, const float* conv_w, uint16_t* conv_hist,
+                           const int32_t* qsl, const int32_t* slot_idx, const uint8_t* has_init,
+                           int32_t num_seqs, int32_t num_tokens, uint16_t* y, int32_t* dev_err,
+                           void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (!conv_w || !conv_hist || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!x || !y)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  ConvArgs a{x, conv_w, conv_hist, qsl, slot_idx, has_init, y, dev_err, channels(d), d->num_slots, num_seqs,
+             num_tokens};
+  return from_cuda(launch_conv(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_decode_step(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w, uint16_t* conv_hist,
+                           float* state, const int32_t* slot_idx, const float* alpha, const float* beta,
+                           const uint16_t* z, const float* gamma, float eps, uint16_t* o, uint16_t* ogate,
+                           int32_t num_seqs, int32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return GDN_OK;
+  if (!qkv0 || !conv_w || !conv_hist || !state || !slot_idx || !alpha || !beta) return GDN_ERR_INVALID_ARG;
+  if (!o && !ogate) return GDN_ERR_INVALID_ARG;
+  if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  StepArgs a{qkv0, conv_w, conv_hist, state, slot_idx, nullptr, alpha, beta, z, gamma, eps, o, ogate, dev_err,
+             d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d), d->num_slots,
+             num_seqs, 1};
+  return from_cuda(launch_step(a, /*spec=*/false, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_spec_verify(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w, uint16_t* conv_hist,
+                           float* state, const int32_t* slot_idx, const int32_t* spec_slot_idx,
+                           const float* alpha, const float* beta, const uint16_t* z, const float* gamma,
+                           float eps, uint16_t* o, uint16_t* ogate, int32_t num_seqs, int32_t num_pos,
+                           int32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || num_pos < 1 || num_pos > 8) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return GDN_OK;
+  if (!qkv0 || !conv_w || !conv_hist || !state || !slot_idx || !spec_slot_idx || !alpha || !beta)
+    return GDN_ERR_INVALID_ARG;
+  if (!o && !ogate) return GDN_ERR_INVALID_ARG;
+  if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  StepArgs a{qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma, eps, o, ogate,
+             dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
+             d->num_slots, num_seqs, num_pos};
+  return from_cuda(launch_step(a, /*spec=*/true, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_spec_commit(const gdn_dims* d, const int32_t* accepted, const int32_t* spec_slot_idx,
+                           int32_t* slot_idx, float* state, uint16_t* conv_hist, int32_t num_seqs,
+                           int32_t num_pos, int32_t mode, int32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || num_pos < 1 || num_pos > 8) return GDN_ERR_INVALID_ARG;
+  if (mode != GDN_COMMIT_COPY && mode != GDN_COMMIT_REPOINT) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return GDN_OK;
+  if (!accepted || !spec_slot_idx || !slot_idx) return GDN_ERR_INVALID_ARG;
+  if (mode == GDN_COMMIT_COPY && (!state || !conv_hist || !aligned(state, 16))) return GDN_ERR_INVALID_ARG;
+  CommitArgs a{accepted, spec_slot_idx, slot_idx, state, conv_hist, dev_err, d->num_v_heads, channels(d),
+               d->num_slots, num_seqs, num_pos, mode};
+  return from_cuda(launch_commit(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w, uint16_t* conv_hist,
+                             float* state, const int32_t* qsl, const int32_t* slot_idx, const uint8_t* has_init,
+                             const float* alpha, const float* beta, const uint16_t* z, const float* gamma,
+                             float eps, uint16_t* o, uint16_t* ogate, int32_t num_seqs, int32_t num_tokens,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!qkv0 || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+  if (!o && !ogate) return GDN_ERR_INVALID_ARG;
+  if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  if ((o && !aligned(o, 8)) || (ogate && (!aligned(ogate, 8) || !aligned(z, 8) || !aligned(gamma, 16))))
+    return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_workspace_bytes(d, num_seqs, num_tokens);
+  if (workspace_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 256))))
+    return GDN_ERR_INVALID_ARG;
+  PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
+                dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
+                d->num_slots, num_seqs, num_tokens};
+  return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_gated_rmsnorm(const uint16_t* o, const uint16_t* z, const float* gamma, float eps, uint16_t* out,
+                             int32_t num_tokens, int32_t num_heads, int32_t head_dim, void* stream) {
+  if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0) return GDN_ERR_INVALID_ARG;
+  if (head_dim % 4 != 0 || head_dim > 1024) return GDN_ERR_UNSUPPORTED;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  const long long rows = (long long)num_tokens * num_heads;
+  if (rows == 0) return GDN_OK;
+  if (rows > (1ll << 31) - 1) return GDN_ERR_INVALID_ARG;
+  if (!o || !z || !gamma || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned(o, 8) || !aligned(z, 8) || !aligned(out, 8) || !aligned(gamma, 16)) return GDN_ERR_INVALID_ARG;
+  NormArgs a{o, z, gamma, out, eps, (int)rows, head_dim};
+  return from_cuda(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

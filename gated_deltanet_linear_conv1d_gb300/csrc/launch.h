@@ -1,0 +1,90 @@
+// launch.h - argument blocks and launchers shared between the C-ABI layer
+// (api.cu) and the kernel files. Internal to libgdn.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct StepArgs {
+  const uint16_t* qkv0;       // [N*P][CH]
+  const float* conv_w;        // [CH][4]
+  uint16_t* conv_hist;        // [Rs][CH][3]
+  float* state;               // [Rs][Hv][128][128]
+  const int32_t* slot_idx;    // [N]
+  const int32_t* spec_slot;   // [N][P] (verify) or nullptr (decode)
+  const float* alpha;         // [N*P][Hv]
+  const float* beta;          // [N*P][Hv]
+  const uint16_t* z;          // [N*P][Hv][128]
+  const float* gamma;         // [128]
+  float eps;
+  uint16_t* o;                // [N*P][Hv][128] or nullptr
+  uint16_t* ogate;            // [N*P][Hv*128] or nullptr
+  int32_t* dev_err;
+  int Hk, Hv, G, CH, Rs, N, P;
+};
+
+struct CommitArgs {
+  const int32_t* accepted;    // [N]
+  const int32_t* spec_slot;   // [N][P]
+  int32_t* slot_idx;          // [N]
+  float* state;
+  uint16_t* conv_hist;
+  int32_t* dev_err;
+  int Hv, CH, Rs, N, P, mode;
+};
+
+struct ConvArgs {
+  const uint16_t* x;          // [T][CH]
+  const float* conv_w;        // [CH][4]
+  uint16_t* conv_hist;        // [Rs][CH][3]
+  const int32_t* qsl;         // [N+1]
+  const int32_t* slot_idx;    // [N]
+  const uint8_t* has_init;    // [N] or nullptr
+  uint16_t* y;                // [T][CH]
+  int32_t* dev_err;
+  int CH, Rs, N, T;
+};
+
+struct PrefillArgs {
+  const uint16_t* qkv0;       // [T][CH]
+  const float* conv_w;
+  uint16_t* conv_hist;
+  float* state;
+  const int32_t* qsl;         // [N+1]
+  const int32_t* slot_idx;    // [N]
+  const uint8_t* has_init;    // [N] or nullptr
+  const float* alpha;         // [T][Hv]
+  const float* beta;
+  const uint16_t* z;          // [T][Hv][128] or nullptr
+  const float* gamma;
+  float eps;
+  uint16_t* o;                // or nullptr
+  uint16_t* ogate;            // or nullptr
+  int32_t* dev_err;
+  int Hk, Hv, G, CH, Rs, N, T;
+};
+
+struct NormArgs {
+  const uint16_t* o;
+  const uint16_t* z;
+  const float* gamma;
+  uint16_t* out;
+  float eps;
+  int rows;  // T * H
+  int D;
+};
+
+// Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (function, device).
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
+
+size_t step_smem_bytes(int P);
+cudaError_t launch_step(const StepArgs& a, bool spec, cudaStream_t stream);
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream);
+
+}  // namespace gdn

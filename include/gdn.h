@@ -1,0 +1,244 @@
+/*
+ * gdn.h - C ABI of libgdn, the Gated DeltaNet (GDN) mixer core for one GB300
+ * (sm_103a).
+ *
+ * The mixer core is the chain of the GDN operator table on the page
+ * "Qwen3.8-27B: from model structure to vLLM inference data flow"
+ * (ai-learning.gods8.com), section 01 LAYER-BY-LAYER, GDN layer L00:
+ *
+ *   c_t  = SiLU( sum_{i=0..3} w_i (.) QKV0_{t-i} )      causal depthwise conv, 4 taps
+ *   q    = normalize(q),  k = normalize(k)              per key head (dk = 128)
+ *   Sbar = alpha S_prev;  e = v - Sbar k;  S = Sbar + beta e k^T;  o = S q / sqrt(dk)
+ *   Ogate = RMSNorm(o) (.) SiLU(Z)                      per value head (dv = 128)
+ *
+ * with the shapes of that section's L00 data-structure table: packed QKV0
+ * [T, 10240] = [Q 16x128 | K 16x128 | V 48x128], Z [T, 48, 128], the recurrent
+ * state S [R, 48, 128, 128] fp32 (3 MiB per sequence per layer) and the conv
+ * history [R, 10240, 3] (3 past inputs; 4 taps with the current one). Value
+ * head h reads key head floor(h / (Hv / Hk)) (section 06, TP4 head split).
+ * Requests are packed along the token axis and split by query_start_loc
+ * (section 01, "vLLM can pack several requests into [T, 5120];
+ * query_start_loc / seq_lens separate them"), and each request owns one slot
+ * of the state and conv-history caches.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is DEVICE memory owned by the caller, unless its
+ *   comment says otherwise. libgdn allocates nothing and keeps no state
+ *   besides per-device function attributes set on first use.
+ * - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
+ * - Layouts are dense and row-major in the order of the bracketed shapes:
+ *     qkv0 / x   [T][CH]          CH = 2*Hk*dk + Hv*dv, channels [Q | K | V],
+ *                                 head-major inside each part
+ *     conv_w     [CH][K]          conv_w[c][i] multiplies the input i steps back
+ *     conv_hist  [Rs][CH][K-1]    time-ascending: entry K-2 is the newest input
+ *     state      [Rs][Hv][dv][dk] fp32; row i (over dv) gives (S k)_i = sum_j S[i][j] k_j
+ *     alpha,beta [T][Hv]          fp32 (the per-token gates, given directly)
+ *     z, o       [T][Hv][dv]      bf16
+ *     ogate      [T][Hv*dv]       bf16
+ *     gamma      [dv]             fp32, shared by all heads
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream), performs no host synchronisation and no allocation, and
+ *   may be captured in a CUDA graph.
+ * - Host-side argument errors return GDN_ERR_INVALID_ARG or GDN_ERR_UNSUPPORTED
+ *   before anything is launched. Launch failures return GDN_ERR_CUDA.
+ * - Errors that only the device can see (a slot index outside [0, num_slots),
+ *   non-monotone query_start_loc, an accepted length outside [0, num_pos), a
+ *   bounded wait that ran out) set bits of *dev_err (GDN_DEVERR_*), when
+ *   dev_err is non-NULL, and the affected request writes nothing. Nothing
+ *   traps. Read the word with gdn_read_device_error().
+ * - A negative slot index marks a padding request: it is skipped and its
+ *   output rows are left untouched. A request with no tokens leaves its slot
+ *   untouched, whatever its has_init flag.
+ * - Two requests of one call must not name the same slot (undefined result).
+ * - Supported geometry: dk = dv = 128, K = 4, Hv a multiple of Hk with
+ *   Hv / Hk <= 8. Anything else returns GDN_ERR_UNSUPPORTED.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Geometry of one GDN layer and its cache pools (the linear_* config fields
+ * that size the recurrent state, "How Qwen3.8-27B's 64 layers are dispatched
+ * in vLLM", step 5: key heads, value heads, key/value head dims, conv kernel). */
+typedef struct gdn_dims {
+    int32_t num_k_heads; /* Hk: q and k heads (16, or 4 per TP4 rank)          */
+    int32_t num_v_heads; /* Hv: v and z heads (48, or 12 per TP4 rank)         */
+    int32_t head_k_dim;  /* dk = 128                                           */
+    int32_t head_v_dim;  /* dv = 128                                           */
+    int32_t conv_kernel; /* K = 4 conv taps (the current input + 3 history)    */
+    int32_t num_slots;   /* Rs: slots in the state and conv-history pools      */
+} gdn_dims;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad mode, misaligned buffer */
+    GDN_ERR_UNSUPPORTED = 2,  /* geometry outside the supported set                      */
+    GDN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed                    */
+    GDN_ERR_DEVICE_CHECK = 4, /* returned by gdn_read_device_error when *dev_err != 0    */
+    GDN_ERR_TIMEOUT = 5       /* returned by gdn_read_device_error for a timed-out wait  */
+} gdn_status;
+
+/* Bits of the device error word. */
+#define GDN_DEVERR_SLOT 1      /* slot index >= num_slots                       */
+#define GDN_DEVERR_OFFSETS 2   /* query_start_loc not monotone or out of range  */
+#define GDN_DEVERR_TIMEOUT 4   /* a bounded wait on an async copy ran out       */
+#define GDN_DEVERR_ACCEPTED 8  /* accepted length outside [0, num_pos)          */
+
+/* Commit modes of gdn_spec_commit. */
+#define GDN_COMMIT_COPY 0    /* copy the accepted checkpoint into the live slot */
+#define GDN_COMMIT_REPOINT 1 /* make the checkpoint's slot the live slot        */
+
+/*
+ * gdn_conv_update - varlen causal depthwise conv + SiLU with history update.
+ * Page: section 01, conv row c_t = SiLU(sum_i w_i QKV0_{t-i}); L00 table,
+ * conv history row (3 past inputs, 4 taps with the current one).
+ *
+ *   x               [T][CH] bf16 packed tokens (T = num_tokens)
+ *   conv_w          [CH][K] fp32
+ *   conv_hist       [Rs][CH][K-1] bf16, in/out: after the call, the slot of
+ *                   request n holds the last K-1 inputs of [history, its tokens]
+ *   query_start_loc [num_seqs+1] int32, 0 = q[0] <= q[1] <= ... <= q[N] = T
+ *   slot_idx        [num_seqs] int32
+ *   has_init        [num_seqs] uint8 or NULL (= all 1); 0 starts from a zero
+ *                   history without reading the slot
+ *   y               [T][CH] bf16 out: SiLU(conv)
+ */
+gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *x, const float *conv_w,
+                           uint16_t *conv_hist, const int32_t *query_start_loc,
+                           const int32_t *slot_idx, const uint8_t *has_init, int32_t num_seqs,
+                           int32_t num_tokens, uint16_t *y, int32_t *dev_err, void *stream);
+
+/*
+ * gdn_decode_step - one token per request through the whole mixer core:
+ * slot gather, conv + SiLU with in-place history update, q/k L2 norm, one
+ * gated-delta-rule step on the fp32 state (in place), gated RMSNorm.
+ * Page: section 01 GDN operator table (conv, recurrence and gate rows);
+ * section 08, decay first, then predict from the decayed state.
+ *
+ *   qkv0      [N][CH] bf16 (N = num_seqs, one token each)
+ *   conv_w    [CH][K] fp32;  conv_hist [Rs][CH][K-1] bf16 in/out
+ *   state     [Rs][Hv][dv][dk] fp32 in/out, 16-byte aligned
+ *   slot_idx  [N] int32
+ *   alpha, beta [N][Hv] fp32;  z [N][Hv][dv] bf16;  gamma [dv] fp32;  eps >= 0
+ *   o         [N][Hv][dv] bf16 out, or NULL
+ *   ogate     [N][Hv*dv] bf16 out, or NULL (at least one of o, ogate)
+ */
+gdn_status gdn_decode_step(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
+                           uint16_t *conv_hist, float *state, const int32_t *slot_idx,
+                           const float *alpha, const float *beta, const uint16_t *z,
+                           const float *gamma, float eps, uint16_t *o, uint16_t *ogate,
+                           int32_t num_seqs, int32_t *dev_err, void *stream);
+
+/*
+ * gdn_chunk_prefill - varlen prefill of packed requests through the whole
+ * mixer core, the conv fused in, the state carried from chunk to chunk of 64
+ * tokens (a chunk never crosses a request boundary). Page: section 01 GDN
+ * operator table, and "GDN's block recurrence uses the associative structure
+ * to run in parallel" (prefill paragraph after the 64-layer list).
+ *
+ *   qkv0      [T][CH] bf16 packed tokens (T = num_tokens)
+ *   conv_w, conv_hist, state: as gdn_decode_step (in/out)
+ *   query_start_loc [N+1] int32 (as gdn_conv_update); slot_idx [N]
+ *   has_init  [N] uint8 or NULL (= all 1); 0 starts from S = 0 and a zero
+ *             history without reading the slot
+ *   alpha, beta [T][Hv] fp32;  z [T][Hv][dv] bf16 or NULL (then ogate must be
+ *             NULL);  gamma [dv];  eps
+ *   o [T][Hv][dv] bf16 or NULL;  ogate [T][Hv*dv] bf16 or NULL (not both NULL)
+ *   workspace, workspace_bytes: device scratch of at least
+ *             gdn_prefill_workspace_bytes(dims, N, T) bytes, 256-byte aligned
+ *             (may be NULL when that size is 0). Contents need not be zeroed
+ *             and are clobbered.
+ */
+gdn_status gdn_chunk_prefill(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
+                             uint16_t *conv_hist, float *state, const int32_t *query_start_loc,
+                             const int32_t *slot_idx, const uint8_t *has_init, const float *alpha,
+                             const float *beta, const uint16_t *z, const float *gamma, float eps,
+                             uint16_t *o, uint16_t *ogate, int32_t num_seqs, int32_t num_tokens,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                             void *stream);
+
+/*
+ * gdn_spec_verify - speculative verify: P = num_pos positions per request (the
+ * last sampled token and P-1 drafts, verified in one forward) through the
+ * whole mixer core, keeping the state and conv history after EVERY position p
+ * in checkpoint slot spec_slot_idx[n][p] of the same pools. The live slot
+ * slot_idx[n] is only read. Pages: "Qwen3.8 MTP" (huashanblogllm.xyz),
+ * section 4 (verify: context + drafts in one pass) and section 5 (accept /
+ * reject); the DeepSeek-V3 pipeline page, section 7.3 (the input
+ * [..., t_{T+1}, d1 .. dk] is verified in parallel); first page, L00 table
+ * ("extra speculative slots counted separately").
+ *
+ *   qkv0 [N*P][CH] bf16, request-major (row n*P + p);  alpha, beta [N*P][Hv];
+ *   z [N*P][Hv][dv];  o [N*P][Hv][dv] or NULL;  ogate [N*P][Hv*dv] or NULL
+ *   conv_hist, state: the pools (live slots read, checkpoint slots written)
+ *   slot_idx [N];  spec_slot_idx [N][P] int32, distinct from every live slot
+ *   num_pos: 1 <= P <= 8
+ */
+gdn_status gdn_spec_verify(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
+                           uint16_t *conv_hist, float *state, const int32_t *slot_idx,
+                           const int32_t *spec_slot_idx, const float *alpha, const float *beta,
+                           const uint16_t *z, const float *gamma, float eps, uint16_t *o,
+                           uint16_t *ogate, int32_t num_seqs, int32_t num_pos, int32_t *dev_err,
+                           void *stream);
+
+/*
+ * gdn_spec_commit - make the state after the accepted position a = accepted[n]
+ * (0 <= a < num_pos; position 0 is the last sampled token) the request's
+ * state ("Qwen3.8 MTP" page, section 5: the longest matching prefix is kept).
+ *
+ *   mode GDN_COMMIT_COPY:    state and conv history of slot spec_slot_idx[n][a]
+ *                            are copied into slot slot_idx[n] (slot_idx read)
+ *   mode GDN_COMMIT_REPOINT: slot_idx[n] = spec_slot_idx[n][a] (nothing copied)
+ *   accepted [N] int32; spec_slot_idx [N][P]; slot_idx [N] (in/out for REPOINT)
+ */
+gdn_status gdn_spec_commit(const gdn_dims *dims, const int32_t *accepted,
+                           const int32_t *spec_slot_idx, int32_t *slot_idx, float *state,
+                           uint16_t *conv_hist, int32_t num_seqs, int32_t num_pos, int32_t mode,
+                           int32_t *dev_err, void *stream);
+
+/*
+ * gdn_gated_rmsnorm - Ogate = RMSNorm(o) (.) SiLU(z) per head row of D values:
+ * out = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z). Page: section 01, gate row
+ * ([T,48,128] -> [T,6144]); section 08 (the GDN output gate is SiLU after
+ * RMSNorm).
+ *
+ *   o, z [T][H][D] bf16;  gamma [D] fp32;  out [T][H*D] bf16
+ *   D a multiple of 4, 4 <= D <= 1024
+ */
+gdn_status gdn_gated_rmsnorm(const uint16_t *o, const uint16_t *z, const float *gamma, float eps,
+                             uint16_t *out, int32_t num_tokens, int32_t num_heads,
+                             int32_t head_dim, void *stream);
+
+/* Bytes of one slot of the fp32 state pool: Hv*dv*dk*4 (3 MiB at 48x128x128,
+ * the L00 table's "3 MiB per sequence per layer"). 0 for invalid dims. */
+size_t gdn_state_bytes(const gdn_dims *dims);
+
+/* Bytes of one slot of the bf16 conv-history pool: CH*(K-1)*2. 0 for invalid dims. */
+size_t gdn_conv_hist_bytes(const gdn_dims *dims);
+
+/* Device scratch gdn_chunk_prefill needs for N requests and T packed tokens. */
+size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t num_seqs, int32_t num_tokens);
+
+/* Static, human-readable name of a status code. */
+const char *gdn_status_string(gdn_status status);
+
+/*
+ * Synchronises `stream`, copies the device error word to *host_err (host
+ * memory) and, if reset != 0, zeroes it. Returns GDN_OK when the word is 0,
+ * GDN_ERR_TIMEOUT when the timeout bit is set, else GDN_ERR_DEVICE_CHECK.
+ * This is the only entry point that synchronises.
+ */
+gdn_status gdn_read_device_error(int32_t *dev_err, int32_t *host_err, int32_t reset, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,79 @@
+"""libgdn builds, loads and exports every entry point include/gdn.h declares (CPU only).
+
+Only host-side paths run here: size queries, status strings and argument
+validation that returns before any CUDA call. No kernel is launched.
+"""
+import ctypes
+
+import pytest
+
+from gated_deltanet_linear_conv1d_gb300 import build as gdn_build
+from gated_deltanet_linear_conv1d_gb300 import synth
+
+
+@pytest.fixture(scope="module")
+def b():
+    gdn_build.build()
+    from gated_deltanet_linear_conv1d_gb300 import binding
+    return binding
+
+
+def test_every_declared_symbol_is_exported(b):
+    names = b.header_symbols()
+    assert {"gdn_conv_update", "gdn_decode_step", "gdn_chunk_prefill", "gdn_spec_verify",
+            "gdn_gated_rmsnorm", "gdn_spec_commit"} <= set(names)
+    lib = ctypes.CDLL(b.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_size_queries_match_the_page(b):
+    d = b.make_dims(synth.FULL_HEADS, 512)
+    assert b.gdn_state_bytes(d) == 48 * 128 * 128 * 4 == 3 * 2**20  # "3 MiB per sequence per layer"
+    assert b.gdn_conv_hist_bytes(d) == 10240 * 3 * 2
+    r = b.make_dims(synth.RANK_HEADS, 8)
+    assert b.gdn_state_bytes(r) == 12 * 128 * 128 * 4
+    assert b.gdn_conv_hist_bytes(r) == 2560 * 3 * 2
+    assert b.gdn_state_bytes(b.GdnDims(0, 0, 0, 0, 0, 0)) == 0
+
+
+def test_status_strings(b):
+    for s in range(6):
+        assert b._lib.gdn_status_string(s).decode().startswith("GDN_")
+
+
+def _decode_call(b, dims, eps=1e-6, num_seqs=1, ptr=1):
+    # Non-NULL dummy pointers: validation must reject before touching them.
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return b._lib.gdn_decode_step(ctypes.byref(dims), p, p, p, p, p, p, p, p, p, eps, p, p, num_seqs, None, None)
+
+
+@pytest.mark.parametrize("geom,expect", [
+    (synth.Dims(16, 48, 64, 128, 4), 2),   # dk != 128
+    (synth.Dims(16, 48, 128, 128, 3), 2),  # 3 taps
+    (synth.Dims(16, 40, 128, 128, 4), 2),  # Hv not a multiple of Hk
+    (synth.Dims(2, 48, 128, 128, 4), 2),   # group 24 > 8
+    (synth.Dims(0, 48, 128, 128, 4), 1),
+])
+def test_geometry_is_rejected_before_launch(b, geom, expect):
+    assert _decode_call(b, b.make_dims(geom, 4)) == expect
+
+
+def test_arguments_are_rejected_before_launch(b):
+    d = b.make_dims(synth.FULL_HEADS, 4)
+    assert _decode_call(b, d, ptr=0) == b.GDN_ERR_INVALID_ARG  # NULL pointers
+    assert _decode_call(b, d, eps=float("nan")) == b.GDN_ERR_INVALID_ARG
+    assert _decode_call(b, d, eps=-1.0) == b.GDN_ERR_INVALID_ARG
+    assert _decode_call(b, d, num_seqs=-1) == b.GDN_ERR_INVALID_ARG
+    assert _decode_call(b, d, ptr=2) == b.GDN_ERR_INVALID_ARG  # state not 16-byte aligned
+    assert _decode_call(b, d, num_seqs=0) == b.GDN_OK  # empty batch: nothing to launch
+    p = ctypes.c_void_p(16)
+    lib = b._lib
+    assert lib.gdn_spec_verify(ctypes.byref(d), *([p] * 10), 1e-6, p, p, 4, 9, None, None) == 1  # 9 positions
+    assert lib.gdn_spec_commit(ctypes.byref(d), p, p, p, p, p, 4, 4, 7, None, None) == 1  # bad mode
+    assert lib.gdn_gated_rmsnorm(p, p, p, 1e-6, p, 4, 4, 6, None) == 2  # D not a multiple of 4
+    assert lib.gdn_gated_rmsnorm(p, p, p, 1e-6, p, 0, 4, 128, None) == 0  # no rows
+    assert lib.gdn_chunk_prefill(ctypes.byref(d), *([p] * 11), 1e-6, p, p, 0, 5, None, 0, None, None) == 1
+    assert lib.gdn_conv_update(ctypes.byref(d), p, p, p, p, p, None, 0, 0, p, None, None) == 0
+    host = ctypes.c_int32(0)
+    assert lib.gdn_read_device_error(None, ctypes.byref(host), 0, None) == 1

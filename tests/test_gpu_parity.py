@@ -1,0 +1,303 @@
+"""GPU parity: every libgdn entry point, called through the C ABI, against the fp64 oracle
+on the same seeded inputs (small shapes spanning several tiles and ragged tails, the
+workload sizes, and the edge cases)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from gated_deltanet_linear_conv1d_gb300 import synth  # noqa: E402
+from oracle import oracle  # noqa: E402
+from tests import gdnutil as U  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def b():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_linear_conv1d_gb300 import build
+    build.build()
+    from gated_deltanet_linear_conv1d_gb300 import binding
+    return binding
+
+
+def _dev_err():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ---------------------------------------------------------------- standalone pieces
+
+@pytest.mark.parametrize("lengths", [[64], [1, 2, 3, 70, 0, 129]])
+def test_conv_update_matches_oracle(b, lengths):
+    dims = synth.FULL_HEADS
+    w = synth.prefill_workload(dims, lengths, seed=31)
+    d = U.to_device(w)
+    T = int(sum(lengths))
+    y = torch.zeros((T, dims.channels), dtype=torch.bfloat16, device="cuda")
+    D = b.make_dims(dims, w["num_slots"])
+    err = _dev_err()
+    b.gdn_conv_update(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["query_start_loc"], d["slot_idx"], y,
+                      has_init=d["has_init"], dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    y_ref, hist_ref = oracle.conv_update(dims, w["qkv0"], w["conv_w"], w["conv_hist"], w["query_start_loc"],
+                                         w["slot_idx"], w["has_init"])
+    U.check_out(U.host_f64_from_bf16(y), y_ref, "y")
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"]), hist_ref)  # bit-exact, untouched slots too
+
+
+def test_gated_rmsnorm_matches_oracle(b):
+    rng = np.random.default_rng(32)
+    T, H, D = 37, 48, 128
+    o = synth.bf16_bits(rng.standard_normal((T, H, D)).astype(np.float32) * 0.3)
+    z = synth.bf16_bits(rng.standard_normal((T, H, D)).astype(np.float32))
+    gamma = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    b.gdn_gated_rmsnorm(U.dev_bf16(o), U.dev_bf16(z), U.dev(gamma), 1e-6, out)
+    ref = oracle.gated_rmsnorm(o, z, gamma, 1e-6)
+    U.check_out(U.host_f64_from_bf16(out), ref, "ogate")
+
+
+# ---------------------------------------------------------------- decode
+
+def _run_decode(b, w, want_o=True):
+    dims = w["dims"]
+    N = len(w["slot_idx"])
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    o = torch.zeros((N, dims.num_v_heads, dims.head_v_dim), dtype=torch.bfloat16, device="cuda") if want_o else None
+    og = torch.zeros((N, dims.num_v_heads * dims.head_v_dim), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_decode_step(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"], d["alpha"], d["beta"],
+                      d["z"], d["gamma"], w["eps"], o=o, ogate=og, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    return d, o, og
+
+
+def _check_decode(w, d, o, og, requests=None, pool_exact=True):
+    N = len(w["slot_idx"])
+    requests = np.arange(N) if requests is None else np.asarray(requests)
+    r, toks = U.oracle_compact(w, requests)
+    if o is not None:
+        U.check_out(U.host_f64_from_bf16(o)[toks], r["o"], "o")
+    U.check_out(U.host_f64_from_bf16(og)[toks], r["ogate"], "ogate")
+    slots = w["slot_idx"][requests]
+    st = d["state"][torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy()
+    U.check_state(st, r["state"], U.STATE_REL_L2_DECODE, "state")
+    hist = U.host_bits(d["conv_hist"][torch.from_numpy(slots.astype(np.int64)).cuda()])
+    np.testing.assert_array_equal(hist, r["conv_hist"])
+    if pool_exact:  # slots no request names are left bit-for-bit as they were
+        untouched = np.setdiff1d(np.arange(w["num_slots"]), w["slot_idx"])
+        idx = torch.from_numpy(untouched.astype(np.int64)).cuda()
+        np.testing.assert_array_equal(d["state"][idx].cpu().numpy(), w["state"][untouched])
+        np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), w["conv_hist"][untouched])
+
+
+@pytest.mark.parametrize("geom", [synth.FULL_HEADS, synth.RANK_HEADS], ids=["16x48", "4x12"])
+@pytest.mark.parametrize("R", [1, 8, 64])
+def test_decode_small_batches(b, geom, R):
+    w = synth.decode_workload(geom, R, seed=40 + R)
+    d, o, og = _run_decode(b, w)
+    _check_decode(w, d, o, og)
+
+
+def test_decode_headline_256_of_512(b):
+    """The headline decode step: 256 requests over a 512-slot pool, random permutation."""
+    w = synth.decode_workload(synth.FULL_HEADS, 256, 512, seed=1)
+    d, o, og = _run_decode(b, w)
+    _check_decode(w, d, o, og)
+
+
+@pytest.mark.parametrize("geom", [synth.FULL_HEADS, synth.RANK_HEADS], ids=["16x48", "4x12"])
+def test_decode_1024(b, geom):
+    w = synth.decode_workload(geom, 1024, seed=44)
+    d, o, og = _run_decode(b, w, want_o=False)
+    rng = np.random.default_rng(0)
+    _check_decode(w, d, None, og, requests=np.sort(rng.choice(1024, 96, replace=False)), pool_exact=False)
+
+
+def test_decode_padding_and_bad_slot(b):
+    dims = synth.RANK_HEADS
+    w = synth.decode_workload(dims, 6, 12, seed=45)
+    w["slot_idx"][1] = -1  # padding: skipped
+    bad = w["slot_idx"].copy()
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    og = torch.zeros((6, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_decode_step(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"], d["alpha"],
+                      d["beta"], d["z"], d["gamma"], w["eps"], ogate=og, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    assert not og[1].any()
+    live = np.array([0, 2, 3, 4, 5])
+    r, _ = U.oracle_compact(w, live)
+    U.check_out(U.host_f64_from_bf16(og)[live], r["ogate"], "ogate")
+    # an out-of-range slot is flagged on the device and writes nothing
+    bad[3] = 12
+    d2 = U.to_device(dict(w, slot_idx=bad))
+    og2 = torch.zeros_like(og)
+    b.gdn_decode_step(D, d2["qkv0"], d2["conv_w"], d2["conv_hist"], d2["state"], d2["slot_idx"], d2["alpha"],
+                      d2["beta"], d2["z"], d2["gamma"], w["eps"], ogate=og2, dev_err=err)
+    assert b.gdn_read_device_error(err) == b.GDN_DEVERR_SLOT
+    assert not og2[3].any()
+    torch.cuda.synchronize()
+
+
+def test_decode_is_deterministic(b):
+    w = synth.decode_workload(synth.FULL_HEADS, 16, seed=46)
+    d1, _, og1 = _run_decode(b, w, want_o=False)
+    d2, _, og2 = _run_decode(b, w, want_o=False)
+    assert torch.equal(og1, og2) and torch.equal(d1["state"], d2["state"])
+
+
+# ---------------------------------------------------------------- speculative verify + commit
+
+@pytest.mark.parametrize("N", [5, 256])
+def test_spec_verify_and_commit(b, N):
+    dims = synth.FULL_HEADS if N == 5 else synth.RANK_HEADS
+    w = synth.spec_workload(dims, N, num_pos=4, seed=47 + N)
+    P = w["num_pos"]
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    o = torch.zeros((N * P, dims.num_v_heads, 128), dtype=torch.bfloat16, device="cuda")
+    og = torch.zeros((N * P, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_spec_verify(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"], d["spec_slot_idx"],
+                      d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], o=o, ogate=og, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    sample = np.arange(N) if N <= 8 else np.sort(np.random.default_rng(1).choice(N, 24, replace=False))
+    ref = oracle.spec_verify(dims, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], w["slot_idx"],
+                             w["spec_slot_idx"], w["alpha"], w["beta"], w["z"], w["gamma"], w["eps"])
+    toks = (sample[:, None] * P + np.arange(P)[None, :]).reshape(-1)
+    U.check_out(U.host_f64_from_bf16(o)[toks], ref["o"][toks], "o")
+    U.check_out(U.host_f64_from_bf16(og)[toks], ref["ogate"][toks], "ogate")
+    ck = w["spec_slot_idx"][sample].reshape(-1)
+    idx = torch.from_numpy(ck.astype(np.int64)).cuda()
+    U.check_state(d["state"][idx].cpu().numpy(), ref["state"][ck], U.STATE_REL_L2_DECODE, "checkpoints")
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), ref["conv_hist"][ck])
+    live = torch.from_numpy(w["slot_idx"].astype(np.int64)).cuda()
+    np.testing.assert_array_equal(d["state"][live].cpu().numpy(), w["state"][w["slot_idx"]])  # live untouched
+
+    # commit by copy: the live slot becomes the accepted checkpoint, bit for bit
+    state_before = d["state"].clone()
+    hist_before = d["conv_hist"].clone()
+    b.gdn_spec_commit(D, d["accepted"], d["spec_slot_idx"], d["slot_idx"], d["state"], d["conv_hist"],
+                      mode=b.GDN_COMMIT_COPY, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    src = torch.from_numpy(w["spec_slot_idx"][np.arange(N), w["accepted"]].astype(np.int64)).cuda()
+    assert torch.equal(d["state"][live], state_before[src])
+    assert torch.equal(d["conv_hist"][live], hist_before[src])
+    # commit by repoint: only the slot index changes
+    slots = d["slot_idx"].clone()
+    b.gdn_spec_commit(D, d["accepted"], d["spec_slot_idx"], slots, mode=b.GDN_COMMIT_REPOINT, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    assert torch.equal(slots.long(), src)
+
+
+def test_spec_commit_rejects_bad_accepted_length(b):
+    dims = synth.RANK_HEADS
+    w = synth.spec_workload(dims, 4, num_pos=4, seed=49)
+    w["accepted"][2] = 4
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    err = _dev_err()
+    slots = d["slot_idx"].clone()
+    b.gdn_spec_commit(D, d["accepted"], d["spec_slot_idx"], slots, mode=b.GDN_COMMIT_REPOINT, dev_err=err)
+    assert b.gdn_read_device_error(err) == b.GDN_DEVERR_ACCEPTED
+    assert int(slots[2]) == int(w["slot_idx"][2])
+
+
+# ---------------------------------------------------------------- prefill
+
+def _run_prefill(b, w, want_o=True):
+    dims = w["dims"]
+    T = int(w["query_start_loc"][-1])
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    o = torch.zeros((T, dims.num_v_heads, 128), dtype=torch.bfloat16, device="cuda") if want_o else None
+    og = torch.zeros((T, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_chunk_prefill(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["query_start_loc"],
+                        d["slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], o=o, ogate=og,
+                        has_init=d["has_init"], dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    return d, o, og
+
+
+def _check_prefill(w, d, o, og, requests):
+    r, toks = U.oracle_compact(w, requests)
+    if o is not None:
+        U.check_out(U.host_f64_from_bf16(o)[toks], r["o"], "o")
+    U.check_out(U.host_f64_from_bf16(og)[toks], r["ogate"], "ogate")
+    slots = torch.from_numpy(w["slot_idx"][requests].astype(np.int64)).cuda()
+    U.check_state(d["state"][slots].cpu().numpy(), r["state"], U.STATE_REL_L2_PREFILL, "state")
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][slots]), r["conv_hist"])
+
+
+def test_prefill_single_request_from_zero(b):
+    """One request of 64 tokens from a zero state (the reference prefill case)."""
+    w = synth.prefill_workload(synth.FULL_HEADS, [64], seed=0, zero_first_half=False)
+    w["has_init"][:] = 0
+    d, o, og = _run_prefill(b, w)
+    _check_prefill(w, d, o, og, [0])
+
+
+@pytest.mark.parametrize("geom", [synth.FULL_HEADS, synth.RANK_HEADS], ids=["16x48", "4x12"])
+def test_prefill_ragged_batch(b, geom):
+    """Lengths across chunk edges (1, 2, 63, 64, 65, 130), an empty request, half from zero."""
+    lengths = [1, 65, 0, 130, 2, 63, 64, 17]
+    w = synth.prefill_workload(geom, lengths, seed=50)
+    d, o, og = _run_prefill(b, w)
+    _check_prefill(w, d, o, og, np.arange(len(lengths)))
+
+
+def test_prefill_varlen_64_requests_sampled(b):
+    """64 requests, log-uniform lengths in [16, 8192], half from zero; sampled requests checked."""
+    lengths = synth.loguniform_lengths(np.random.default_rng(3), 64, 16, 8192)
+    w = synth.prefill_workload(synth.FULL_HEADS, lengths, seed=3)
+    d, o, og = _run_prefill(b, w, want_o=False)
+    order = np.argsort(lengths)
+    sample = np.unique(np.concatenate([order[:2], order[-1:], order[30:32]]))
+    _check_prefill(w, d, None, og, sample)
+
+
+def test_prefill_then_decode_continues_the_request(b):
+    """Prefill of T1 tokens, then decode steps, equals one oracle pass over all tokens."""
+    geom = synth.RANK_HEADS
+    T1, T2 = 70, 3
+    w = synth.prefill_workload(geom, [T1 + T2], seed=51, zero_first_half=False)
+    full, _ = U.oracle_compact(w, [0])
+    d = U.to_device(w)
+    D = b.make_dims(geom, w["num_slots"])
+    og = torch.zeros((T1 + T2, geom.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    qsl = torch.tensor([0, T1], dtype=torch.int32, device="cuda")
+    b.gdn_chunk_prefill(D, d["qkv0"][:T1].contiguous(), d["conv_w"], d["conv_hist"], d["state"], qsl,
+                        d["slot_idx"], d["alpha"][:T1].contiguous(), d["beta"][:T1].contiguous(),
+                        d["z"][:T1].contiguous(), d["gamma"], w["eps"], ogate=og[:T1], dev_err=err)
+    for t in range(T1, T1 + T2):
+        sl = slice(t, t + 1)
+        b.gdn_decode_step(D, d["qkv0"][sl].contiguous(), d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"],
+                          d["alpha"][sl].contiguous(), d["beta"][sl].contiguous(), d["z"][sl].contiguous(),
+                          d["gamma"], w["eps"], ogate=og[sl], dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    U.check_out(U.host_f64_from_bf16(og), full["ogate"], "ogate")
+    slot = int(w["slot_idx"][0])
+    U.check_state(d["state"][slot].cpu().numpy(), full["state"][0], U.STATE_REL_L2_PREFILL, "state")
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][slot]), full["conv_hist"][0])
+
+
+def test_prefill_bad_offsets_are_flagged(b):
+    geom = synth.RANK_HEADS
+    w = synth.prefill_workload(geom, [5, 7], seed=52)
+    w["query_start_loc"] = np.array([0, 5, 13], np.int32)  # the last request ends past T = 12
+    d = U.to_device(w)
+    D = b.make_dims(geom, w["num_slots"])
+    og = torch.zeros((12, geom.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_chunk_prefill(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["query_start_loc"],
+                        d["slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og, dev_err=err)
+    assert b.gdn_read_device_error(err) & b.GDN_DEVERR_OFFSETS
+    assert og[:5].any() and not og[5:].any()  # the valid request ran, the flagged one wrote nothing
+    s1 = int(w["slot_idx"][1])
+    np.testing.assert_array_equal(d["state"][s1].cpu().numpy(), w["state"][s1])
