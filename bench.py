@@ -104,7 +104,7 @@ def load_traffic(kernel: str):
     """dram read+write bytes per launch from a committed ncu summary, if its source hash still matches."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}.md")
-    src = os.path.join(ROOT, "gated_deltanet_linear_conv1d_gb300", "csrc", "step.cu")
+    src = os.path.join(ROOT, "gated_deltanet_linear_conv1d_gb300", "csrc", "decode.cu")
     try:
         text = open(path).read()
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -364,7 +364,7 @@ def run_gpu(args):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "kernel": "step_kernel<false> (gdn_decode_step)",
+                "kernel": "decode_kernel (gdn_decode_step)",
                 "algorithmic_bytes_per_launch": bytes_launch, "mean_launch_ms": mean_kernel_ms}
     cpu = oracle_decode_rate(w, NUM_REQ, min_seconds=10.0, max_seconds=30.0)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

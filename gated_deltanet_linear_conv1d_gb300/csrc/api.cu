@@ -140,11 +140,13 @@ gdn_status gdn_decode_step(const gdn_dims* d, const uint16_t* qkv0, const float*
   if (!o && !ogate) return GDN_ERR_INVALID_ARG;
   if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
   if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
-  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16) || !aligned(qkv0, 16) || !aligned(conv_hist, 16) ||
+      (ogate && !aligned(z, 16)))
+    return GDN_ERR_INVALID_ARG;
   StepArgs a{qkv0, conv_w, conv_hist, state, slot_idx, nullptr, alpha, beta, z, gamma, eps, o, ogate, dev_err,
              d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d), d->num_slots,
              num_seqs, 1};
-  return from_cuda(launch_step(a, /*spec=*/false, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_spec_verify(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w, uint16_t* conv_hist,

@@ -82,6 +82,7 @@ cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
 size_t step_smem_bytes(int P);
 cudaError_t launch_step(const StepArgs& a, bool spec, cudaStream_t stream);
+cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
