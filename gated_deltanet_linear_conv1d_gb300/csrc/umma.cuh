@@ -1,0 +1,156 @@
+// umma.cuh - inline-PTX wrappers for the 5th-generation tensor cores
+// (tcgen05.mma with accumulators in tensor memory) used by libgdn's
+// tensor-core kernels, plus the shared-memory operand layout they share.
+//
+// Operand layout in shared memory ("canonical, no swizzle"): a tile of R rows
+// by C columns is stored as 8-row x 16-byte core matrices. Core matrix
+// (row octet ro, 16-byte column chunk cc) starts at ro * SBO + cc * 128 bytes,
+// and inside it row r % 8 sits at (r % 8) * 16 bytes. So each core matrix is
+// 128 contiguous bytes, LBO = 128 bytes separates neighbouring column chunks
+// and SBO = 128 * (C * esize / 16) separates row octets.
+//  - As a K-major operand, rows are M (or N) and columns are K.
+//  - As an MN-major operand, rows are K and columns are M (or N).
+// A K-major MMA step advances the start address along the columns, an
+// MN-major step advances it by whole row octets.
+#pragma once
+
+#include <stdint.h>
+
+#include "device.cuh"
+
+namespace gdn {
+namespace umma {
+
+// ---- shared-memory operand layout ------------------------------------------
+
+// Byte offset of element (r, c) in a tile whose rows hold `row_bytes` bytes.
+__host__ __device__ __forceinline__ uint32_t tile_off(int r, int c_bytes, int row_bytes) {
+  return (uint32_t)((r >> 3) * (row_bytes * 8) + (c_bytes >> 4) * 128 + (r & 7) * 16 + (c_bytes & 15));
+}
+
+// Shared-memory matrix descriptor (no swizzle) for a tile with the layout above.
+// In the no-swizzle canonical layouts the two byte offsets play opposite roles
+// for the two majors: K-major takes LBO = the stride between K chunks (128 B
+// here) and SBO = the stride between 8-row MN groups; MN-major takes LBO = the
+// stride between 8-row K groups and SBO = the stride between 16-byte MN chunks.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t row_bytes, bool mn_major = false) {
+  const uint64_t octet = (uint64_t)row_bytes * 8, chunk = 128;
+  const uint64_t lbo = mn_major ? octet : chunk, sbo = mn_major ? chunk : octet;
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) | (1ull << 46);
+}
+
+// ---- instruction descriptors -------------------------------------------------
+
+enum : uint32_t { kBF16 = 1, kTF32 = 2 };
+
+// kind::f16 (bf16 operands) or kind::tf32, fp32 accumulator, dense.
+__host__ __device__ constexpr uint32_t idesc(uint32_t ab_type, bool a_mn_major, bool b_mn_major, int M, int N) {
+  return (1u << 4) | (ab_type << 7) | (ab_type << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- tensor-memory allocation (one full warp executes these) -----------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the tensor
+// core (async proxy); call before the barrier that precedes the MMA issue.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- MMA issue and completion (one thread) -----------------------------------
+
+template <uint32_t kKind>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc_v,
+                                    uint32_t accumulate) {
+  if constexpr (kKind == kTF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc_v), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc_v), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Arrives once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// ---- tensor-memory loads and stores (one warp; lanes = its 32-lane quarter) --
+
+// 32 consecutive columns of this thread's lane.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Tensor-memory address of (lane, column).
+__device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
+  return base + (lane << 16) + col;
+}
+
+// fp32 -> tf32 (round to nearest, ties away), kept in an fp32 container.
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+}  // namespace umma
+}  // namespace gdn

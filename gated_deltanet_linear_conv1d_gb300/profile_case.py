@@ -106,11 +106,23 @@ def main(argv=None):
         def run():
             b.gdn_gated_rmsnorm(o, z, gamma, 1e-6, out)
 
-    for _ in range(args.warmup + args.launches):
+    times = []
+    for it in range(args.warmup + args.launches):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
         run()
+        e1.record()
         torch.cuda.synchronize()
+        if it >= args.warmup:
+            times.append(e0.elapsed_time(e1))
     flag = b.gdn_read_device_error(err)
-    print(f"profile_case {args.case}: {args.launches} launches after {args.warmup} warm-up, device error word {flag}")
+    tokens = {"decode": args.requests, "spec": args.requests * 4}.get(args.case)
+    if args.case in ("prefill", "conv"):
+        tokens = T
+    ms = sum(times) / max(1, len(times))
+    rate = f", {tokens / (ms / 1e3):.4g} tokens/s" if tokens else ""
+    print(f"profile_case {args.case}: {args.launches} launches after {args.warmup} warm-up, "
+          f"mean {ms:.4f} ms{rate}, device error word {flag}")
     if flag:
         raise SystemExit(1)
 

@@ -1,0 +1,56 @@
+"""Tensor-core (tcgen05) operand layouts and descriptors of umma.cuh, checked on the GPU
+against numpy: one 128 x N x K GEMM per case. bf16 operands K-major or MN-major (B also as a
+sub-block of a wider tile); tf32 operands K-major (the form the tensor cores take tf32 in)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tests.csrc import build_selftest
+    lib = ctypes.CDLL(build_selftest.build())
+    lib.umma_selftest.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 7 + [ctypes.c_void_p]
+    lib.umma_selftest.restype = ctypes.c_int
+    return lib
+
+
+def _round(x, kind):
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    if kind == 1:  # bf16, nearest even
+        u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16 << 16
+    else:  # tf32, nearest, ties away from zero
+        u = (u + 0x1000) >> 13 << 13
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+CASES = [(kind, N, K, a_mn, b_mn, b_cols)
+         for kind in (1, 2) for N in (64, 128) for K in (64, 128) for a_mn in (0, 1) for b_mn in (0, 1)
+         for b_cols in {N if b_mn else K, 128}
+         if not (kind == 2 and (a_mn or b_mn))  # tf32 operands are K-major only
+         and (b_cols == (N if b_mn else K) or (kind == 1 and b_mn and N == 64))]
+
+
+@pytest.mark.parametrize("kind,N,K,a_mn,b_mn,b_cols", CASES)
+def test_tcgen05_gemm(lib, kind, N, K, a_mn, b_mn, b_cols):
+    rng = np.random.default_rng(N * 1000 + K * 10 + kind + 7 * b_mn + 3 * a_mn)
+    M = 128
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dD = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.umma_selftest(dA.data_ptr(), dB.data_ptr(), dD.data_ptr(), err.data_ptr(), M, N, K, kind, a_mn, b_mn,
+                           b_cols, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = _round(A, kind) @ _round(B, kind).T
+    got = dD.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(got, ref, rtol=1e-4, atol=1e-4 * np.abs(ref).max())
