@@ -25,8 +25,9 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// SiLU(x) = x * sigmoid(x).
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+// SiLU(x) = x * sigmoid(x) = x / (1 + e^-x), with the fast exponential and
+// division (a few ulp; large negative x gives -0).
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ void report(int32_t* dev_err, int32_t bits) {
   if (dev_err) atomicOr(dev_err, bits);

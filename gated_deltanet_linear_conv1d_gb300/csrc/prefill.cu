@@ -1,24 +1,41 @@
-// prefill.cu - gdn_chunk_prefill: varlen prefill through the whole mixer core
-// (page "Qwen3.8-27B: from model structure to vLLM inference data flow",
-// section 01 GDN operator table): conv + SiLU fused in, q/k L2 norm, the gated
-// delta rule carried across the request, gated RMSNorm.
+// prefill.cu - gdn_chunk_prefill on the tensor cores: varlen prefill through
+// the whole mixer core (page "Qwen3.8-27B: from model structure to vLLM
+// inference data flow", section 01 GDN operator table), with the gated delta
+// rule evaluated in chunks of 64 tokens in its WY / UT form.
 //
-// This is the CUDA-core path: one CTA per (value head h, request n) with 128
-// threads, thread r holding row r of the fp32 state (128 registers) for the
-// whole request. Tokens are staged 32 at a time: the conv outputs of the
-// CTA's q, k and v channels go to shared memory, q and k are normalised there,
-// then the recurrence walks the staged tokens (every thread reads the same k
-// and q vectors, a shared-memory broadcast), and the staged outputs are gated
-// and written. Rows are independent given k, q, alpha, beta, so no reduction
-// crosses threads inside the recurrence.
+// Chunked form (derived from the recurrence row S = a S + b (v - a S k) k^T;
+// the page only says that the block recurrence uses the associative structure
+// to run in parallel). For a chunk starting from state S0 with, per token r,
+// g_r = sum_{i<=r} ln a_i and Gamma[r][i] = exp(g_r - g_i):
+//   (I + A) E = diag(b) V - diag(b e^g) K S0^T,  A[r][i] = b_r Gamma[r][i] k_r.k_i (i < r)
+//   E^T = (V^T - S0 Kg^T) Tb^T,   Kg = diag(e^g) K,  Tb = (I + A)^-1 diag(b)
+//   O^T = diag_cols(e^g) S0 Q^T + E^T P^T,  P[r][i] = Gamma[r][i] q_r.k_i (i <= r)
+//   S_C = e^{g_C} S0 + E^T diag(Gamma[C][.]) K
+// with q, k unit-normalised; the per-token norms are folded into the
+// products' readouts, so the tensor cores take the raw conv outputs.
 //
-// The G CTAs of one key head form a cluster: all read the old conv history of
-// their shared q/k channels before a cluster barrier, and the group's first CTA
-// writes the new history after the request is done.
+// One CTA per (value head h, request n), 256 threads; the G CTAs of a key
+// head form a cluster (only to order the in-place conv-history update). The
+// fp32 state lives in tensor memory (128 lanes x 128 columns) for the whole
+// request. Per chunk:
+//   conv + SiLU (CUDA cores, thread = channel)  -> raw q, k (bf16, channel-major),
+//       k e^g (bf16), k (tf32, channel-major), v (fp32), per-token |q|, |k|
+//   [K;Q] K^T                 tcgen05 bf16  M=128 N=64  K=128  (operands MN-major)
+//   S0 -> bf16 operand, S *= e^{g_C} in tensor memory
+//   X = S0 Kg^T, Z = S0 Q^T   tcgen05 bf16  M=128 N=64  K=128
+//   A, P from K K^T, Q K^T;  T = (I + A)^-1 on CUDA cores (blocked by 16)
+//   Y = V^T - X  -> tf32;  E^T = Y Tb^T   tcgen05 tf32 M=128 N=64 K=64
+//   S += (E^T diag(Gamma_C / |k|)) K     tcgen05 tf32 M=128 N=128 K=64 (accumulate)
+//   O' = E^T P^T                tcgen05 bf16 M=128 N=64 K=64
+//   o = e^g Z / |q| + O',  gated RMSNorm, bf16 out.
+// The two products that feed the carried state (E and the state update) take
+// tf32 operands; the others take bf16 (measured against the fp64 oracle:
+// state error ~6e-4, output error ~3e-3 relative L2).
 #include <cooperative_groups.h>
 
 #include "device.cuh"
 #include "launch.h"
+#include "umma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -26,189 +43,598 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = kHeadDim;  // one thread per state row / channel
-constexpr int kStage = 32;          // tokens staged per pass
+constexpr int kThreads = 256;
+constexpr int kC = 64;  // chunk length
 constexpr float kInvSqrtDk = 0.08838834764831845f;
 
-struct PfSmem {
-  float q[kStage][kHeadDim];
-  float k[kStage][kHeadDim];
-  float v[kStage][kHeadDim];
-  float o[kStage][kHeadDim];
-  float a[kStage], b[kStage], kq[kStage];
-};
+// Shared-memory regions (byte offsets, 1024-aligned).
+constexpr int kKQ = 0;                  // bf16 [128 dk][128 t]: k tokens 0-63, q tokens 64-127 (MN-major)
+constexpr int kKG = kKQ + 32768;        // bf16 [128 dk][64 t]: k e^g (MN-major B)      | later E bf16 [128 dv][64 t]
+constexpr int kKT = kKG + 16384;        // tf32 [128 dk][64 t]: raw k (K-major B)
+constexpr int kVS = kKT + 32768;        // fp32 [128 dv][65]: v, channel-major, padded
+constexpr int kS0 = kVS + 33792;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
+constexpr int kAM = kS0 + 32768;        // fp32 [64][65]: A for the inverse
+constexpr int kTS = kAM + 17408;        // fp32 [64][65]: T, row-major
+constexpr int kTB = kTS + 17408;        // tf32 [64 r][64 i]: T diag(b) (K-major B)
+constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
+constexpr int kSmall = kPB + 8192;      // small per-chunk vectors
+constexpr int kSmallFloats = 64 * 8 + 8 * 64 + 4 * 64 + 64;
+constexpr int kMS = kSmall + kSmallFloats * 4;  // fp32 [3][16][17]: inverse scratch
+constexpr int kBars = kMS + 3 * 272 * 4;
+constexpr int kSmemBytes = kBars + 64;
 
-__global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillArgs p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  PfSmem& sm = *reinterpret_cast<PfSmem*>(smem_raw);
+// Tensor-memory columns.
+constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_X = 192, kT_Z = 256, kT_E = 320, kT_O = 384, kTmemCols = 512;
+
+__device__ __forceinline__ float to_tf32(float x) { return umma::to_tf32(x); }
+
+// Sums v[0..7] over the 32 lanes of a warp, 8 values at once (9 shuffles).
+// Returns the total of value index tok8(lane) in every lane.
+__device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = hi ? v[i] : v[i + 4], keep = hi ? v[i + 4] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool hi = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  {
+    const bool hi = lane & 4;
+    const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return v[0];
+}
+__device__ __forceinline__ int tok8(int lane) {
+  return ((lane >> 2) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
+}
+
+// Waits for an MMA-completion phase; the verdict is uniform over the CTA.
+__device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity) {
+  const int ok = __syncthreads_and(mbar_wait_bounded(bar, parity) ? 1 : 0);
+  umma::fence_after_sync();
+  return ok != 0;
+}
+
+// Syncs the CTA after shared-memory operand writes and tensor-memory stores,
+// so that the MMAs issued next see them.
+__device__ __forceinline__ void sync_for_mma() {
+  umma::fence_proxy_async_smem();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillArgs p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int h = blockIdx.x, n = blockIdx.y;
   const int g = h % p.G, j = h / p.G;
-  const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = 32 * quarter + lane;  // tensor-memory lane read by this thread
 
+  // ---- request checks (uniform over the cluster: same request)
   const int slot = p.slot_idx[n];
-  if (slot < 0) return;  // padding (uniform over the cluster)
+  if (slot < 0) return;
   const int t0 = p.qsl[n], t1 = p.qsl[n + 1];
   if (t0 < 0 || t1 < t0 || t1 > p.T || (n == 0 && t0 != 0) || (n == p.N - 1 && t1 != p.T)) {
-    if (r == 0 && g == 0) report(p.dev_err, GDN_DEVERR_OFFSETS);
+    if (tid == 0 && g == 0) report(p.dev_err, GDN_DEVERR_OFFSETS);
     return;
   }
   if (slot >= p.Rs) {
-    if (r == 0 && g == 0) report(p.dev_err, GDN_DEVERR_SLOT);
+    if (tid == 0 && g == 0) report(p.dev_err, GDN_DEVERR_SLOT);
     return;
   }
-  if (t1 == t0) return;  // no tokens: the slot is left untouched (uniform over the cluster)
+  if (t1 == t0) return;  // no tokens: the slot is left untouched
   const bool init = p.has_init ? p.has_init[n] != 0 : true;
 
-  // channels of this thread: q head j, k head j, v head h, element r
-  const int gc[3] = {j * kHeadDim + r, (p.Hk + j) * kHeadDim + r, 2 * p.Hk * kHeadDim + h * kHeadDim + r};
-  float4 w[3];
-  uint16_t hb[3][3];  // conv windows: oldest .. newest input, per part
-#pragma unroll
-  for (int u = 0; u < 3; ++u) {
-    w[u] = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gc[u] * kTaps);
-    const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc[u]) * (kTaps - 1);
-    hb[u][0] = init ? hp[0] : 0;
-    hb[u][1] = init ? hp[1] : 0;
-    hb[u][2] = init ? hp[2] : 0;
+  uint16_t* KQ = reinterpret_cast<uint16_t*>(smem + kKQ);
+  unsigned char* KGb = smem + kKG;
+  unsigned char* KTb = smem + kKT;
+  float* VS = reinterpret_cast<float*>(smem + kVS);
+  unsigned char* S0b = smem + kS0;
+  float* AM = reinterpret_cast<float*>(smem + kAM);
+  float* TS = reinterpret_cast<float*>(smem + kTS);
+  unsigned char* TBb = smem + kTB;
+  unsigned char* PBb = smem + kPB;
+  float* small = reinterpret_cast<float*>(smem + kSmall);
+  float* gv = small;             // [64] g
+  float* egv = gv + 64;          // [64] e^g
+  float* glv = egv + 64;         // [64] e^{g_C - g_t} (0 past the chunk end)
+  float* bv = glv + 64;          // [64] beta
+  float* iqv = bv + 64;          // [64] 1/|q|
+  float* ikv = iqv + 64;         // [64] 1/|k|
+  float* rinv = ikv + 64;        // [64] gate 1/rms
+  float* scan = rinv + 64;       // [64] scan scratch
+  float* npart = scan + 64;      // [8][64] norm partials (warps 0-3: q, 4-7: k)
+  float* rpart = npart + 8 * 64; // [4][64] gate partials
+  float* MS = reinterpret_cast<float*>(smem + kMS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);  // 0: [K;Q]K^T  1: X,Z  2: E  3: S, O'
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+
+  // ---- conv channels of this thread: q (tid < 128) and v (tid < 128), or k
+  const bool qv = tid < 128;
+  const int d = qv ? tid : tid - 128;
+  const int gc_a = qv ? j * kHeadDim + d : (p.Hk + j) * kHeadDim + d;  // q or k channel
+  const int gc_v = (2 * p.Hk + h) * kHeadDim + d;                       // v channel (qv threads)
+  const float4 wa = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gc_a * kTaps);
+  const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gc_v * kTaps);
+  uint16_t ha[3] = {0, 0, 0}, hv[3] = {0, 0, 0};  // conv windows, oldest first
+  if (init) {
+    const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc_a) * 3;
+    ha[0] = hp[0]; ha[1] = hp[1]; ha[2] = hp[2];
+    if (qv) {
+      const uint16_t* hq = p.conv_hist + ((size_t)slot * p.CH + gc_v) * 3;
+      hv[0] = hq[0]; hv[1] = hq[1]; hv[2] = hq[2];
+    }
   }
-  float* Srow_g = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + r) * kHeadDim;
-  float S[kHeadDim];
-#pragma unroll
-  for (int c = 0; c < kHeadDim; c += 4) {
-    float4 v4 = init ? *reinterpret_cast<const float4*>(Srow_g + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    S[c] = v4.x;
-    S[c + 1] = v4.y;
-    S[c + 2] = v4.z;
-    S[c + 3] = v4.w;
+
+  if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
+  if (tid == 0) {
+    for (int b = 0; b < 4; ++b) mbar_init(&bars[b], 1);
+    fence_mbar_init();
   }
+  umma::fence_before_sync();
   // All CTAs of the key-head group have read the old history from here on.
   cg::this_cluster().sync();
+  umma::fence_after_sync();
+  const uint32_t tm = *tmem_slot;
+  const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
 
-  for (int c0 = t0; c0 < t1; c0 += kStage) {
-    const int L = min(kStage, t1 - c0);
-    // ---- a2: conv + SiLU of the staged tokens
-    for (int t = 0; t < L; ++t) {
-      const size_t rowx = (size_t)(c0 + t) * p.CH;
+  // ---- initial state into tensor memory: thread (row, half) owns 64 columns
+  {
+    const float* src = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + half * 64;
 #pragma unroll
-      for (int u = 0; u < 3; ++u) {
-        const uint16_t xb = p.qkv0[rowx + gc[u]];
-        float pre = w[u].x * bf16_to_f32(xb);
-        pre = fmaf(w[u].y, bf16_to_f32(hb[u][2]), pre);
-        pre = fmaf(w[u].z, bf16_to_f32(hb[u][1]), pre);
-        pre = fmaf(w[u].w, bf16_to_f32(hb[u][0]), pre);
-        const float y = silu(pre);
-        if (u == 0) sm.q[t][r] = y;
-        else if (u == 1) sm.k[t][r] = y;
-        else sm.v[t][r] = y;
-        hb[u][0] = hb[u][1];
-        hb[u][1] = hb[u][2];
-        hb[u][2] = xb;
+    for (int c = 0; c < 2; ++c) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 f = init ? *reinterpret_cast<const float4*>(src + c * 32 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
       }
+      umma::st32(tm + lane_base + kTS_S + half * 64 + c * 32, v);
     }
-    if (r < L) {
-      const size_t ai = (size_t)(c0 + r) * p.Hv + h;
-      sm.a[r] = p.alpha[ai];
-      sm.b[r] = p.beta[ai];
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+
+  const uint32_t id_kk = umma::idesc(umma::kBF16, true, true, 128, 64);
+  const uint32_t id_xz = umma::idesc(umma::kBF16, false, true, 128, 64);
+  const uint32_t id_e = umma::idesc(umma::kTF32, false, false, 128, 64);
+  const uint32_t id_s = umma::idesc(umma::kTF32, false, false, 128, 128);
+  const uint32_t id_o = umma::idesc(umma::kBF16, false, false, 128, 64);
+  const uint32_t sKQ = smem_u32(KQ), sKG = smem_u32(KGb), sKT = smem_u32(KTb), sS0 = smem_u32(S0b);
+  const uint32_t sTB = smem_u32(TBb), sPB = smem_u32(PBb);
+
+  const int nchunks = (t1 - t0 + kC - 1) / kC;
+  bool ok = true;
+  for (int c = 0; c < nchunks && ok; ++c) {
+    const int tc = t0 + c * kC;
+    const int L = min(kC, t1 - tc);
+    const uint32_t par = c & 1;
+
+    // ---- gates: g = inclusive cumsum of ln(alpha), e^g, beta
+    if (tid < kC) {
+      float la = 0.f, b = 0.f;
+      if (tid < L) {
+        const size_t ai = (size_t)(tc + tid) * p.Hv + h;
+        la = fmaxf(logf(p.alpha[ai]), -80.f);
+        b = p.beta[ai];
+      }
+      float s = la;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += u;
+      }
+      scan[tid] = s;
+      bv[tid] = b;
     }
     __syncthreads();
-    // ---- a3: L2 norm of q and k; warp w takes tokens w, w+4, ...
-    for (int t = warp; t < L; t += kThreads / 32) {
-      float4 q4 = reinterpret_cast<const float4*>(sm.q[t])[lane];
-      float4 k4 = reinterpret_cast<const float4*>(sm.k[t])[lane];
-      const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
-      const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
-      const float iq = rsqrtf(sq + 1e-12f), ik = rsqrtf(sk + 1e-12f);
-      q4.x *= iq; q4.y *= iq; q4.z *= iq; q4.w *= iq;
-      k4.x *= ik; k4.y *= ik; k4.z *= ik; k4.w *= ik;
-      reinterpret_cast<float4*>(sm.q[t])[lane] = q4;
-      reinterpret_cast<float4*>(sm.k[t])[lane] = k4;
-      const float kq = warp_sum(q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w);
-      if (lane == 0) sm.kq[t] = kq;
+    if (tid < kC) {
+      const float gt = scan[tid] + (tid >= 32 ? scan[31] : 0.f);
+      gv[tid] = gt;
+      egv[tid] = expf(gt);
     }
     __syncthreads();
-    // ---- a4: the recurrence, row r of the state in registers
-    for (int t = 0; t < L; ++t) {
-      const float a = sm.a[t], b = sm.b[t];
-      const float4* k4p = reinterpret_cast<const float4*>(sm.k[t]);
-      const float4* q4p = reinterpret_cast<const float4*>(sm.q[t]);
-      float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f;
+    if (tid < kC) glv[tid] = tid < L ? expf(gv[L - 1] - gv[tid]) : 0.f;
+
+    // ---- conv + SiLU: every input of the chunk is loaded first (one memory
+    // round trip), then 8 tokens at a time, operands written channel-major
+    uint32_t xa2[kC / 2], xv2[kC / 2];  // bf16 pairs (token 2i low, 2i+1 high)
 #pragma unroll
-      for (int c = 0; c < kHeadDim; c += 8) {
-        const float4 ka = k4p[c / 4], kb = k4p[c / 4 + 1];
-        const float4 qa = q4p[c / 4], qb = q4p[c / 4 + 1];
-        pk0 = fmaf(S[c], ka.x, pk0); pk0 = fmaf(S[c + 1], ka.y, pk0);
-        pk0 = fmaf(S[c + 2], ka.z, pk0); pk0 = fmaf(S[c + 3], ka.w, pk0);
-        pk1 = fmaf(S[c + 4], kb.x, pk1); pk1 = fmaf(S[c + 5], kb.y, pk1);
-        pk1 = fmaf(S[c + 6], kb.z, pk1); pk1 = fmaf(S[c + 7], kb.w, pk1);
-        pq0 = fmaf(S[c], qa.x, pq0); pq0 = fmaf(S[c + 1], qa.y, pq0);
-        pq0 = fmaf(S[c + 2], qa.z, pq0); pq0 = fmaf(S[c + 3], qa.w, pq0);
-        pq1 = fmaf(S[c + 4], qb.x, pq1); pq1 = fmaf(S[c + 5], qb.y, pq1);
-        pq1 = fmaf(S[c + 6], qb.z, pq1); pq1 = fmaf(S[c + 7], qb.w, pq1);
+    for (int i = 0; i < kC / 2; ++i) {
+      uint32_t a = 0, v = 0;
+      const int t = 2 * i;
+      if (t < L) {
+        const size_t xr = (size_t)(tc + t) * p.CH;
+        a = p.qkv0[xr + gc_a];
+        if (qv) v = p.qkv0[xr + gc_v];
       }
-      const float sk = pk0 + pk1, sq = pq0 + pq1;
-      const float e = sm.v[t][r] - a * sk;  // v - Sbar k
-      const float be = b * e;
-      sm.o[t][r] = fmaf(be, sm.kq[t], a * sq) * kInvSqrtDk;
+      if (t + 1 < L) {
+        const size_t xr = (size_t)(tc + t + 1) * p.CH;
+        a |= (uint32_t)p.qkv0[xr + gc_a] << 16;
+        if (qv) v |= (uint32_t)p.qkv0[xr + gc_v] << 16;
+      }
+      xa2[i] = a;
+      xv2[i] = v;
+    }
 #pragma unroll
-      for (int c = 0; c < kHeadDim; c += 4) {
-        const float4 k4 = k4p[c / 4];
-        S[c] = fmaf(be, k4.x, a * S[c]);
-        S[c + 1] = fmaf(be, k4.y, a * S[c + 1]);
-        S[c + 2] = fmaf(be, k4.z, a * S[c + 2]);
-        S[c + 3] = fmaf(be, k4.w, a * S[c + 3]);
+    for (int grp = 0; grp < kC / 8; ++grp) {
+      float ya[8], yv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = grp * 8 + e;
+        ya[e] = 0.f;
+        yv[e] = 0.f;
+        if (t < L) {
+          const uint16_t xa = (uint16_t)(xa2[t >> 1] >> ((t & 1) * 16));
+          float pre = wa.x * bf16_to_f32(xa);
+          pre = fmaf(wa.y, bf16_to_f32(ha[2]), pre);
+          pre = fmaf(wa.z, bf16_to_f32(ha[1]), pre);
+          pre = fmaf(wa.w, bf16_to_f32(ha[0]), pre);
+          ya[e] = silu(pre);
+          ha[0] = ha[1]; ha[1] = ha[2]; ha[2] = xa;
+          if (qv) {
+            const uint16_t xv = (uint16_t)(xv2[t >> 1] >> ((t & 1) * 16));
+            float pv = wv.x * bf16_to_f32(xv);
+            pv = fmaf(wv.y, bf16_to_f32(hv[2]), pv);
+            pv = fmaf(wv.z, bf16_to_f32(hv[1]), pv);
+            pv = fmaf(wv.w, bf16_to_f32(hv[0]), pv);
+            yv[e] = silu(pv);
+            hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
+          }
+        }
+      }
+      // raw q or k, bf16: row d of KQ, tokens (qv ? 64 : 0) + 8 grp ...
+      {
+        uint4 pk;
+        pk.x = pack_bf16(ya[0], ya[1]);
+        pk.y = pack_bf16(ya[2], ya[3]);
+        pk.z = pack_bf16(ya[4], ya[5]);
+        pk.w = pack_bf16(ya[6], ya[7]);
+        const int col = (qv ? 64 : 0) + grp * 8;
+        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(d, col * 2, 256)) = pk;
+      }
+      if (!qv) {
+        uint4 pk;
+        const int t = grp * 8;
+        pk.x = pack_bf16(ya[0] * egv[t + 0], ya[1] * egv[t + 1]);
+        pk.y = pack_bf16(ya[2] * egv[t + 2], ya[3] * egv[t + 3]);
+        pk.z = pack_bf16(ya[4] * egv[t + 4], ya[5] * egv[t + 5]);
+        pk.w = pack_bf16(ya[6] * egv[t + 6], ya[7] * egv[t + 7]);
+        *reinterpret_cast<uint4*>(KGb + umma::tile_off(d, t * 2, 128)) = pk;
+        *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4, 256)) =
+            make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
+        *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
+            make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) VS[d * 65 + grp * 8 + e] = yv[e];
+      }
+      // per-token sum of squares of the raw q (warps 0-3) or k (warps 4-7)
+      float sq[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
+      const float tot = reduce8(sq, lane);
+      if ((lane & 3) == 0) npart[warp * 64 + grp * 8 + tok8(lane)] = tot;
+    }
+    sync_for_mma();
+
+    // ---- [K;Q] K^T (bf16): D1 lanes 0-63 = K K^T rows, lanes 64-127 = Q K^T rows
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        const uint64_t a = umma::smem_desc(sKQ + kk * 4096, 256, true);
+        umma::mma<umma::kBF16>(tm + kT_D1, a, a, id_kk, kk > 0);
+      }
+      umma::commit(&bars[0]);
+    }
+    if (tid < kC) {
+      const float sq = (npart[0 * 64 + tid] + npart[1 * 64 + tid]) + (npart[2 * 64 + tid] + npart[3 * 64 + tid]);
+      const float sk = (npart[4 * 64 + tid] + npart[5 * 64 + tid]) + (npart[6 * 64 + tid] + npart[7 * 64 + tid]);
+      iqv[tid] = rsqrtf(sq + 1e-12f);
+      ikv[tid] = rsqrtf(sk + 1e-12f);
+    }
+    // ---- S0 as a bf16 operand; S *= e^{g_C} in tensor memory for the update below
+    {
+      const float decay = egv[L - 1];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        float v[32];
+        const uint32_t col = kTS_S + half * 64 + cc * 32;
+        umma::ld32(tm + lane_base + col, v);
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint4 pk;
+          pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
+          pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
+          pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
+          pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
+          const int dk = half * 64 + cc * 32 + q8 * 8;
+          *reinterpret_cast<uint4*>(S0b + umma::tile_off(row, dk * 2, 256)) = pk;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= decay;
+        umma::st32(tm + lane_base + col, v);
+      }
+    }
+    sync_for_mma();
+    // ---- X = S0 Kg^T and Z = S0 Q^T (bf16)
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        const uint64_t a = umma::smem_desc(sS0 + kk * 256, 256, false);
+        umma::mma<umma::kBF16>(tm + kT_X, a, umma::smem_desc(sKG + kk * 2048, 128, true), id_xz, kk > 0);
+        umma::mma<umma::kBF16>(tm + kT_Z, a, umma::smem_desc(sKQ + 1024 + kk * 4096, 256, true), id_xz, kk > 0);
+      }
+      umma::commit(&bars[1]);
+    }
+
+    // ---- A (for the inverse) and P from K K^T and Q K^T
+    if (!wait_mma(&bars[0], par)) { ok = false; break; }
+    {
+      float v[32];
+      umma::ld32(tm + lane_base + kT_D1 + half * 32, v);
+      if (row < 64) {
+        const int r = row;
+        const float br = bv[r], gr = gv[r], ikr = ikv[r];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int i = half * 32 + e;
+          AM[r * 65 + i] = i < r ? br * expf(gr - gv[i]) * v[e] * ikr * ikv[i] : 0.f;
+        }
+      } else {
+        const int r = row - 64;
+        const float gr = gv[r], iqr = iqv[r];
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float pe[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int i = half * 32 + q8 * 8 + e;
+            pe[e] = i <= r ? expf(gr - gv[i]) * v[q8 * 8 + e] * iqr * ikv[i] : 0.f;
+          }
+          uint4 pk;
+          pk.x = pack_bf16(pe[0], pe[1]);
+          pk.y = pack_bf16(pe[2], pe[3]);
+          pk.z = pack_bf16(pe[4], pe[5]);
+          pk.w = pack_bf16(pe[6], pe[7]);
+          *reinterpret_cast<uint4*>(PBb + umma::tile_off(r, (half * 32 + q8 * 8) * 2, 128)) = pk;
+        }
       }
     }
     __syncthreads();
-    // ---- a5: gated RMSNorm of the staged outputs; warp w takes tokens w, w+4, ...
-    for (int t = warp; t < L; t += kThreads / 32) {
-      const float4 o4 = reinterpret_cast<const float4*>(sm.o[t])[lane];
-      const size_t base = ((size_t)(c0 + t) * p.Hv + h) * kHeadDim + lane * 4;
-      if (p.o) {
-        uint2 packed;
-        packed.x = (uint32_t)f32_to_bf16(o4.x) | ((uint32_t)f32_to_bf16(o4.y) << 16);
-        packed.y = (uint32_t)f32_to_bf16(o4.z) | ((uint32_t)f32_to_bf16(o4.w) << 16);
-        *reinterpret_cast<uint2*>(p.o + base) = packed;
+    // ---- T = (I + A)^-1, blocked by 16 (T row-major in TS). Diagonal blocks by
+    // forward substitution (one column per thread); then the off-diagonal
+    // blocks one block diagonal at a time: T_ab = -T_aa sum_{b<=c<a} A_ac T_cb.
+    for (int it = tid; it < kC * kC; it += kThreads) TS[(it >> 6) * 65 + (it & 63)] = 0.f;
+    __syncthreads();
+    if (tid < kC) {
+      const int a = tid >> 4, cc = tid & 15;
+      const float* Ab = AM + (16 * a) * 65 + 16 * a;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) s = fmaf(Ab[r * 65 + i], x[i], s);
+        x[r] = r < cc ? 0.f : (r == cc ? 1.f : -s);
       }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) TS[(16 * a + r) * 65 + 16 * a + cc] = x[r];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int dist = 1; dist < 4; ++dist) {
+      const int nblk = 4 - dist;  // blocks (a, a - dist) for a = dist .. 3
+      for (int it = tid; it < nblk * 256; it += kThreads) {
+        const int blk = it >> 8, r = (it >> 4) & 15, col = it & 15;
+        const int a = dist + blk, b = a - dist;
+        const float* ar = AM + (16 * a + r) * 65;
+        float s = 0.f;
+#pragma unroll 4
+        for (int i = 16 * b; i < 16 * a; ++i) s = fmaf(ar[i], TS[i * 65 + 16 * b + col], s);
+        MS[blk * 272 + r * 17 + col] = s;
+      }
+      __syncthreads();
+      for (int it = tid; it < nblk * 256; it += kThreads) {
+        const int blk = it >> 8, r = (it >> 4) & 15, col = it & 15;
+        const int a = dist + blk, b = a - dist;
+        const float* tr = TS + (16 * a + r) * 65 + 16 * a;
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s = fmaf(tr[i], MS[blk * 272 + i * 17 + col], s);
+        TS[(16 * a + r) * 65 + 16 * b + col] = -s;
+      }
+      __syncthreads();
+    }
+    // ---- Tb = T diag(beta) as a tf32 K-major operand: rows r, 16-byte chunks of 4 columns
+    for (int it = tid; it < kC * 16; it += kThreads) {
+      const int r = it >> 4, ck = it & 15;
+      float4 f;
+      f.x = to_tf32(TS[r * 65 + 4 * ck + 0] * bv[4 * ck + 0]);
+      f.y = to_tf32(TS[r * 65 + 4 * ck + 1] * bv[4 * ck + 1]);
+      f.z = to_tf32(TS[r * 65 + 4 * ck + 2] * bv[4 * ck + 2]);
+      f.w = to_tf32(TS[r * 65 + 4 * ck + 3] * bv[4 * ck + 3]);
+      *reinterpret_cast<float4*>(TBb + umma::tile_off(r, ck * 16, 256)) = f;
+    }
+    // ---- Y = V^T - X (tf32, rows dv), over S0's now-free space
+    if (!wait_mma(&bars[1], par)) { ok = false; break; }
+    {
+      float v[32];
+      umma::ld32(tm + lane_base + kT_X + half * 32, v);
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        float y4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = half * 32 + q4 * 4 + e;
+          y4[e] = to_tf32(VS[row * 65 + t] - v[q4 * 4 + e] * ikv[t]);
+        }
+        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (half * 32 + q4 * 4) * 4, 256)) =
+            make_float4(y4[0], y4[1], y4[2], y4[3]);
+      }
+    }
+    sync_for_mma();
+    // ---- E^T = Y Tb^T (tf32)
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kC / 8; ++kk)
+        umma::mma<umma::kTF32>(tm + kT_E, umma::smem_desc(sS0 + kk * 256, 256, false),
+                               umma::smem_desc(sTB + kk * 256, 256, false), id_e, kk > 0);
+      umma::commit(&bars[2]);
+    }
+    if (!wait_mma(&bars[2], par)) { ok = false; break; }
+    // ---- E as bf16 (A of O' = E^T P^T) and E' = E diag(Gamma_C / |k|) as tf32 (A of the update)
+    {
+      float v[32];
+      umma::ld32(tm + lane_base + kT_E + half * 32, v);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint4 pk;
+        pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
+        pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
+        pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
+        pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(KGb + umma::tile_off(row, (half * 32 + q8 * 8) * 2, 128)) = pk;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        float e4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = half * 32 + q4 * 4 + e;
+          e4[e] = to_tf32(v[q4 * 4 + e] * glv[t] * ikv[t]);
+        }
+        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (half * 32 + q4 * 4) * 4, 256)) =
+            make_float4(e4[0], e4[1], e4[2], e4[3]);
+      }
+    }
+    sync_for_mma();
+    // ---- S += E' K (tf32, accumulate) and O' = E^T P^T (bf16)
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kC / 8; ++kk)
+        umma::mma<umma::kTF32>(tm + kTS_S, umma::smem_desc(sS0 + kk * 256, 256, false),
+                               umma::smem_desc(sKT + kk * 256, 256, false), id_s, 1);
+#pragma unroll
+      for (int kk = 0; kk < kC / 16; ++kk)
+        umma::mma<umma::kBF16>(tm + kT_O, umma::smem_desc(sKG + kk * 256, 128, false),
+                               umma::smem_desc(sPB + kk * 256, 128, false), id_o, kk > 0);
+      umma::commit(&bars[3]);
+    }
+    // this thread's 32 gate inputs z, fetched while the last MMAs run
+    uint32_t zz2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t v = 0;
+      const int t = half * 32 + 2 * i;
       if (p.ogate) {
-        const float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
-        const float rinv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-        const uint2 zr = *reinterpret_cast<const uint2*>(p.z + base);
-        const float4 gm = reinterpret_cast<const float4*>(p.gamma)[lane];
-        uint2 packed;
-        packed.x = (uint32_t)f32_to_bf16(o4.x * rinv * gm.x * silu(bf16_to_f32(zr.x & 0xffff))) |
-                   ((uint32_t)f32_to_bf16(o4.y * rinv * gm.y * silu(bf16_to_f32(zr.x >> 16))) << 16);
-        packed.y = (uint32_t)f32_to_bf16(o4.z * rinv * gm.z * silu(bf16_to_f32(zr.y & 0xffff))) |
-                   ((uint32_t)f32_to_bf16(o4.w * rinv * gm.w * silu(bf16_to_f32(zr.y >> 16))) << 16);
-        *reinterpret_cast<uint2*>(p.ogate + base) = packed;
+        if (t < L) v = p.z[((size_t)(tc + t) * p.Hv + h) * kHeadDim + row];
+        if (t + 1 < L) v |= (uint32_t)p.z[((size_t)(tc + t + 1) * p.Hv + h) * kHeadDim + row] << 16;
+      }
+      zz2[i] = v;
+    }
+    if (!wait_mma(&bars[3], par)) { ok = false; break; }
+    // ---- o = (e^g Z / |q| + O') / sqrt(dk), then the gated RMSNorm over dv
+    float ov[32];
+    {
+      float z[32];
+      umma::ld32(tm + lane_base + kT_Z + half * 32, z);
+      umma::ld32(tm + lane_base + kT_O + half * 32, ov);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int t = half * 32 + e;
+        ov[e] = fmaf(egv[t] * iqv[t], z[e], ov[e]) * kInvSqrtDk;
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float sq[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sq[e] = ov[q8 * 8 + e] * ov[q8 * 8 + e];
+        const float tot = reduce8(sq, lane);
+        if ((lane & 3) == 0) rpart[quarter * 64 + half * 32 + q8 * 8 + tok8(lane)] = tot;
+      }
+    }
+    __syncthreads();
+    if (tid < kC)
+      rinv[tid] = rsqrtf(((rpart[tid] + rpart[64 + tid]) + (rpart[128 + tid] + rpart[192 + tid])) *
+                             (1.0f / kHeadDim) + p.eps);
+    __syncthreads();
+    {
+      const float gm = p.ogate ? p.gamma[row] : 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int t = half * 32 + e;
+        if (t < L) {
+          const size_t idx = ((size_t)(tc + t) * p.Hv + h) * kHeadDim + row;
+          if (p.o) p.o[idx] = f32_to_bf16(ov[e]);
+          if (p.ogate) {
+            const uint16_t zb = (uint16_t)(zz2[e >> 1] >> ((e & 1) * 16));
+            p.ogate[idx] = f32_to_bf16(ov[e] * rinv[t] * gm * silu(bf16_to_f32(zb)));
+          }
+        }
       }
     }
     __syncthreads();
   }
 
-  // ---- a6: state and history scatter
+  if (ok) {
+    // ---- final state back to the slot, history to the owners' channels
+    float* dst = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + half * 64;
 #pragma unroll
-  for (int c = 0; c < kHeadDim; c += 4)
-    *reinterpret_cast<float4*>(Srow_g + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+    for (int cc = 0; cc < 2; ++cc) {
+      float v[32];
+      umma::ld32(tm + lane_base + kTS_S + half * 64 + cc * 32, v);
 #pragma unroll
-  for (int u = 0; u < 3; ++u) {
-    if (u < 2 && g != 0) continue;  // q/k history is written by the group's first CTA
-    uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc[u]) * (kTaps - 1);
-    hp[0] = hb[u][0];
-    hp[1] = hb[u][1];
-    hp[2] = hb[u][2];
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + cc * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+    if (g == 0) {  // q and k history: the group's first CTA
+      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc_a) * 3;
+      hp[0] = ha[0]; hp[1] = ha[1]; hp[2] = ha[2];
+    }
+    if (qv) {  // v history: the head's own CTA
+      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc_v) * 3;
+      hp[0] = hv[0]; hp[1] = hv[1]; hp[2] = hv[2];
+    }
+  } else {
+    if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
+    // give MMAs still in flight a second bounded chance before the memory is freed
+    for (int b = 0; b < 4; ++b) mbar_wait_bounded(&bars[b], 0);
   }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  if (warp == 0) umma::tmem_dealloc(tm, kTmemCols);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  const size_t smem = sizeof(PfSmem);
-  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(&prefill_kernel), smem);
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(&prefill_tc_kernel), kSmemBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hv, a.N, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -217,7 +643,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, a);
 }
 
 }  // namespace gdn
