@@ -100,6 +100,48 @@ def load_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def load_bf16_peak() -> tuple[float, float, str]:
+    """(burst, sustained) dense bf16 TFLOP/s of the GB300s, and where they came from."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+# tf32 tensor rate relative to bf16 (nominal dense figures: 1.1 vs 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def prefill_flops(geom, lengths) -> tuple[float, float]:
+    """Tensor-core FLOPs (bf16, tf32) of the chunked prefill for these request lengths.
+
+    Per 64-token chunk and value head: S0 Kg^T and S0 Q^T (bf16, 2 x 2*128*64*128),
+    E^T P^T (bf16, 2*128*64*64), E^T = Y Tb^T (tf32, 2*128*64*64), the state update
+    (tf32, 2*128*128*64); per key head [K;Q] K^T (bf16, 2*128*64*128). A partial last
+    chunk is computed as a full one.
+    """
+    chunks = sum((int(L) + 63) // 64 for L in lengths)
+    hv, hk = geom.num_v_heads, geom.num_k_heads
+    bf16 = chunks * (hv * (2 * 2 * 128 * 64 * 128 + 2 * 128 * 64 * 64) + hk * 2 * 128 * 64 * 128)
+    tf32 = chunks * hv * (2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
+    return float(bf16), float(tf32)
+
+
+def prefill_bytes(geom, lengths, has_init) -> float:
+    """HBM bytes a prefill must move: per token QKV0, z, alpha, beta and Ogate; per request the
+    state and conv history (read only when continuing a slot) and their write-back."""
+    state = geom.num_v_heads * geom.head_v_dim * geom.head_k_dim * 4
+    hist = geom.channels * (geom.conv_kernel - 1) * 2
+    per_tok = geom.channels * 2 + 2 * geom.num_v_heads * geom.head_v_dim * 2 + geom.num_v_heads * 8
+    total = sum(int(L) for L in lengths) * per_tok
+    for L, init in zip(lengths, has_init):
+        if int(L) > 0:
+            total += (state + hist) * (2 if init else 1)
+    return float(total + geom.channels * geom.conv_kernel * 4 + geom.head_v_dim * 4)
+
+
 def load_traffic(kernel: str):
     """dram read+write bytes per launch from a committed ncu summary, if its source hash still matches."""
     import hashlib
@@ -263,6 +305,138 @@ def to_device(w: dict, dev) -> dict:
     return out
 
 
+def device_workload(geom, num_slots, tokens, seed, dev) -> dict:
+    """Benchmark-only inputs drawn on the device with the distributions of synth (QKV0, z ~ N(0,1)
+    bf16; conv taps ~ N(0, 0.25); alpha = exp(-U(0.001, 0.1)); beta ~ U(0, 1); gamma = 1; state
+    ~ N(0, 0.02); history ~ N(0, 1) bf16). Never compared with the oracle."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    H, D, CH = geom.num_v_heads, geom.head_v_dim, geom.channels
+
+    def randn(*shape, std=1.0, dtype=torch.float32):
+        return (torch.randn(shape, generator=gen, device=dev) * std).to(dtype)
+
+    u = torch.rand((tokens, H), generator=gen, device=dev) * (0.1 - 0.001) + 0.001
+    return {
+        "qkv0": randn(tokens, CH, dtype=torch.bfloat16),
+        "z": randn(tokens, H, D, dtype=torch.bfloat16),
+        "alpha": torch.exp(-u),
+        "beta": torch.rand((tokens, H), generator=gen, device=dev),
+        "conv_w": randn(CH, geom.conv_kernel, std=0.25),
+        "gamma": torch.ones(D, device=dev),
+        "state": randn(num_slots, H, D, geom.head_k_dim, std=0.02),
+        "conv_hist": randn(num_slots, CH, geom.conv_kernel - 1, dtype=torch.bfloat16),
+    }
+
+
+def timed(fn, steps: int, warmup: int, stream) -> float:
+    """Mean milliseconds of fn() over `steps` launches after `warmup`, CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_prefill(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
+    """Varlen chunked prefill: 64 requests, log-uniform lengths in [16, 8192], half from zero."""
+    import torch
+    geom = synth.FULL_HEADS
+    lengths = synth.loguniform_lengths(np.random.default_rng(3), 64, 16, 8192)
+    N, T = len(lengths), int(lengths.sum())
+    Rs = 2 * N
+    w = device_workload(geom, Rs, T, seed=3, dev=dev)
+    slots = torch.from_numpy(synth.slot_permutation(np.random.default_rng(3), N, Rs)).to(dev)
+    qsl = torch.from_numpy(synth.pack_offsets(lengths)).to(dev)
+    has_init = np.ones(N, np.uint8)
+    has_init[: N // 2] = 0
+    hi = torch.from_numpy(has_init).to(dev)
+    og = torch.empty((T, geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    D = b.make_dims(geom, Rs)
+
+    def run():
+        b.gdn_chunk_prefill(D, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], qsl, slots, w["alpha"],
+                            w["beta"], w["z"], w["gamma"], 1e-6, ogate=og, has_init=hi, dev_err=err, stream=stream)
+
+    ms = timed(run, steps, warmup, stream)
+    if b.gdn_read_device_error(err) != 0:
+        raise RuntimeError("device error flagged during the prefill measurement")
+    f_bf16, f_tf32 = prefill_flops(geom, lengths)
+    p_bf16, _, kind = load_bf16_peak()
+    p_tf32 = p_bf16 * TF32_PER_BF16
+    t_peak = f_bf16 / (p_bf16 * 1e12) + f_tf32 / (p_tf32 * 1e12)
+    hbm_peak, hbm_kind = load_peaks()
+    nbytes = prefill_bytes(geom, lengths, has_init)
+    return {"workload": f"{N} requests, log-uniform lengths in [16, 8192] (seed 3), {T} tokens packed, "
+                        f"half from a zero state; 16/48 heads; chunk 64",
+            "value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps, "warmup": warmup,
+            "kernel": "prefill_tc_kernel (gdn_chunk_prefill)",
+            "tensor": {"achieved_tflops": (f_bf16 + f_tf32) / (ms / 1e3) / 1e12, "bf16_flops": f_bf16,
+                       "tf32_flops": f_tf32, "peak_bf16_tflops": p_bf16, "peak_tf32_tflops": p_tf32,
+                       "frac": t_peak / (ms / 1e3),
+                       "peak_kind": f"{kind} bf16 burst; tf32 = bf16 x 1.1/2.25 (nominal ratio)"},
+            "hbm": {"achieved_gbs": nbytes / (ms / 1e3) / 1e9, "algorithmic_bytes": nbytes, "peak": hbm_peak,
+                    "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "peak_kind": hbm_kind}}
+
+
+def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
+    """One mixed step: speculative verify of 256 requests x 4 positions with per-position
+    checkpoints, commit (copy) at accepted lengths U{0..3}, and a prefill of 8 x 2048 tokens."""
+    import torch
+    geom = synth.FULL_HEADS
+    N, P = 256, 4
+    Rs = N * (P + 1)
+    w = device_workload(geom, Rs, N * P, seed=4, dev=dev)
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(Rs).astype(np.int32)
+    slots = torch.from_numpy(perm[:N].copy()).to(dev)
+    spec = torch.from_numpy(perm[N:].reshape(N, P).copy()).to(dev)
+    acc = torch.from_numpy(rng.integers(0, P, size=N).astype(np.int32)).to(dev)
+    og = torch.empty((N * P, geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
+    lengths = np.full(8, 2048, np.int32)
+    wp = device_workload(geom, 16, int(lengths.sum()), seed=5, dev=dev)
+    pslots = torch.arange(8, dtype=torch.int32, device=dev)
+    pqsl = torch.from_numpy(synth.pack_offsets(lengths)).to(dev)
+    pog = torch.empty((int(lengths.sum()), geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    D, Dp = b.make_dims(geom, Rs), b.make_dims(geom, 16)
+
+    def spec_only():
+        b.gdn_spec_verify(D, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], slots, spec, w["alpha"],
+                          w["beta"], w["z"], w["gamma"], 1e-6, ogate=og, dev_err=err, stream=stream)
+        b.gdn_spec_commit(D, acc, spec, slots, w["state"], w["conv_hist"], mode=b.GDN_COMMIT_COPY, dev_err=err,
+                          stream=stream)
+
+    def mixed():
+        spec_only()
+        b.gdn_chunk_prefill(Dp, wp["qkv0"], wp["conv_w"], wp["conv_hist"], wp["state"], pqsl, pslots,
+                            wp["alpha"], wp["beta"], wp["z"], wp["gamma"], 1e-6, ogate=pog, dev_err=err,
+                            stream=stream)
+
+    ms_spec = timed(spec_only, steps, warmup, stream)
+    ms_mixed = timed(mixed, steps, warmup, stream)
+    if b.gdn_read_device_error(err) != 0:
+        raise RuntimeError("device error flagged during the speculative-verify measurement")
+    state = geom.num_v_heads * geom.head_v_dim * geom.head_k_dim * 4
+    hist = geom.channels * (geom.conv_kernel - 1) * 2
+    act = geom.channels * 2 + 2 * geom.num_v_heads * geom.head_v_dim * 2 + geom.num_v_heads * 8
+    spec_bytes = N * ((state + hist) * (1 + P) + P * act + 2 * (state + hist))  # verify + commit copy
+    hbm_peak, _ = load_peaks()
+    return {"workload": "A: 256 requests x 4 positions (last sampled token + 3 drafts), a state and history "
+                        "checkpoint per position, commit by copy at accepted U{0..3}; B: prefill 8 x 2048 tokens",
+            "spec_value": N * P / (ms_spec / 1e3), "unit": "verified tokens/s", "spec_ms": ms_spec,
+            "spec_hbm_gbs": spec_bytes / (ms_spec / 1e3) / 1e9, "spec_hbm_frac": spec_bytes / (ms_spec / 1e3) / 1e9 / hbm_peak,
+            "mixed_ms": ms_mixed, "mixed_tokens_per_s": (N * P + int(lengths.sum())) / (ms_mixed / 1e3)}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -367,6 +541,13 @@ def run_gpu(args):
                 "kernel": "decode_kernel (gdn_decode_step)",
                 "algorithmic_bytes_per_launch": bytes_launch, "mean_launch_ms": mean_kernel_ms}
     cpu = oracle_decode_rate(w, NUM_REQ, min_seconds=10.0, max_seconds=30.0)
+    del d
+    torch.cuda.empty_cache()
+    extra = {}
+    if not args.decode_only:
+        extra["prefill"] = measure_prefill(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["spec_mixed"] = measure_spec_mixed(b, dev, stream)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -376,6 +557,7 @@ def run_gpu(args):
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps, "clocks": clocks}
+    line.update(extra)
     print(json.dumps(line), flush=True)
 
 
@@ -385,6 +567,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="skip the prefill and speculative-verify lines (decode headline only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
