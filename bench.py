@@ -538,7 +538,7 @@ def run_gpu(args):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "kernel": "decode_kernel (gdn_decode_step)",
+                "kernel": "stream_kernel (gdn_decode_step)",
                 "algorithmic_bytes_per_launch": bytes_launch, "mean_launch_ms": mean_kernel_ms}
     cpu = oracle_decode_rate(w, NUM_REQ, min_seconds=10.0, max_seconds=30.0)
     del d

@@ -15,21 +15,18 @@
 namespace gdn {
 
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
+  // (function, device) -> the largest dynamic shared-memory size set so far
   static std::mutex mu;
-  static std::unordered_map<const void*, uint64_t> done;  // function -> bitmask of devices
+  static std::unordered_map<const void*, std::unordered_map<int, size_t>> set_to;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = done.find(fn);
-    if (bit && it != done.end() && (it->second & bit)) return cudaSuccess;
-  }
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = set_to[fn][dev];
+  if (bytes <= cur) return cudaSuccess;
   err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (err != cudaSuccess) return err;
-  std::lock_guard<std::mutex> lock(mu);
-  done[fn] |= bit;
+  cur = bytes;
   return cudaSuccess;
 }
 
@@ -146,7 +143,7 @@ gdn_status gdn_decode_step(const gdn_dims* d, const uint16_t* qkv0, const float*
   StepArgs a{qkv0, conv_w, conv_hist, state, slot_idx, nullptr, alpha, beta, z, gamma, eps, o, ogate, dev_err,
              d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d), d->num_slots,
              num_seqs, 1};
-  return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_stream(a, static_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_spec_verify(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w, uint16_t* conv_hist,
@@ -167,6 +164,9 @@ gdn_status gdn_spec_verify(const gdn_dims* d, const uint16_t* qkv0, const float*
   StepArgs a{qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma, eps, o, ogate,
              dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
              d->num_slots, num_seqs, num_pos};
+  // the streaming kernel when its shared-memory ring fits, else one CTA per (head, request)
+  if (stream_supported(a.G, a.P) && aligned(qkv0, 16) && aligned(conv_hist, 16) && (!ogate || aligned(z, 16)))
+    return from_cuda(launch_stream(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_step(a, /*spec=*/true, static_cast<cudaStream_t>(stream)));
 }
 

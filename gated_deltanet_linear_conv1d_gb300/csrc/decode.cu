@@ -1,31 +1,33 @@
-// decode.cu - the persistent, warp-specialised decode kernel behind
-// gdn_decode_step (one token per request through the whole mixer core, state
-// updated in place).
+// decode.cu - the persistent, warp-specialised state-streaming kernel behind
+// gdn_decode_step (one token per request, the state updated in place) and
+// gdn_spec_verify (P positions per request, the state after every position kept
+// in its checkpoint slot).
 //
 // Math (page "Qwen3.8-27B: from model structure to vLLM inference data flow",
 // section 01 GDN operator table; section 08: decay first, then predict from the
-// decayed state), per value head h with key head j = h / G:
+// decayed state), per value head h with key head j = h / G and position p:
 //   y = SiLU(sum_i w_i x_{t-i});  q = y_q/|y_q|,  k = y_k/|y_k|,  v = y_v
 //   e = v - a (S k);  S' = a S + b e k^T;  o = (a (S q) + b e (k . q)) / sqrt(dk)
 //   Ogate = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z)
-// so each state element is read once and written once.
+// so each state element is read once and written once per position.
 //
-// Design. Decode is bound by HBM bandwidth: 97% of its bytes are the fp32
-// state read and written back. The kernel keeps the state stream continuous:
+// Design. The path is bound by HBM bandwidth: nearly all of its bytes are the
+// fp32 state read and written back. The kernel keeps the state stream
+// continuous:
 //  - one CTA per SM, each owning a contiguous range of work units; a unit is
 //    (request n, key head j) with its G = Hv/Hk value heads, so the unit owns
 //    the conv channels of q_j, k_j and its value heads outright (the in-place
 //    history update needs no cross-CTA ordering);
 //  - a producer warp streams the unit's 2G half-tiles of state (64 rows x 128
-//    fp32 = 32 KiB each) through a ring of kStages shared-memory stages with
-//    bulk (TMA) copies completing on mbarriers, running up to kStages
-//    half-tiles ahead of the consumers; it also stages the unit's QKV0, conv
-//    history and z segments (double-buffered per unit);
-//  - sixteen consumer warps compute the conv + L2 norm of the unit, then each
-//    warp takes 4 rows of a half-tile (8 lanes per row): four 16-byte shared
-//    loads per lane, the two dot products (S k, S q) reduced over the 8 lanes,
-//    the update, and four coalesced 16-byte stores per lane straight back to
-//    HBM; then the gated RMSNorm of each head.
+//    fp32 = 32 KiB each) through a ring of shared-memory stages with bulk (TMA)
+//    copies completing on mbarriers, running ahead of the consumers; it also
+//    stages the unit's QKV0, conv history and z segments (double-buffered);
+//  - sixteen consumer warps compute the conv + L2 norm of the unit for all P
+//    positions, then each warp takes 4 rows of a half-tile (8 lanes per row):
+//    four 16-byte shared loads per lane, then per position the two dot
+//    products (S k, S q) reduced over the 8 lanes, the update kept in
+//    registers, and four coalesced 16-byte stores per lane straight to HBM;
+//    then the gated RMSNorm of each head and position.
 // Every wait is bounded: a stalled copy sets GDN_DEVERR_TIMEOUT and the CTA
 // leaves instead of hanging.
 #include "device.cuh"
@@ -38,30 +40,38 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStages = 6;
+constexpr int kMaxStages = 6;
+constexpr int kMaxPos = 8;
 constexpr int kHalfRows = 64;
 constexpr int kHalfFloats = kHalfRows * kHeadDim;
-constexpr uint32_t kHalfBytes = kHalfFloats * 4;  // 32 KiB
-constexpr int kRowsPerWarp = kHalfRows / kConsumerWarps;  // 4: lanes 8r..8r+7 share row r
-constexpr float kInvSqrtDk = 0.08838834764831845f;  // 1/sqrt(128)
+constexpr uint32_t kHalfBytes = kHalfFloats * 4;           // 32 KiB
+constexpr int kRowsPerWarp = kHalfRows / kConsumerWarps;   // 4: lanes 8r..8r+7 share row r
+constexpr float kInvSqrtDk = 0.08838834764831845f;         // 1/sqrt(128)
+constexpr int kSmemLimit = 227 * 1024;
 
-// Dynamic shared-memory layout for group size G (byte offsets, 16-byte aligned).
+// Dynamic shared-memory layout for group size G and P positions (byte offsets,
+// 16-byte aligned). The stage ring takes what the rest leaves, up to 6 stages.
 struct Layout {
-  int stage, x, hist, z, q, k, v, o, red, ab, bars, total;
-  __host__ __device__ explicit Layout(int G) {
-    const int nseg = 2 + G;                         // q, k, G value heads
-    stage = 0;                                      // [kStages][kHalfFloats] fp32
-    x = stage + kStages * kHalfBytes;               // [2][nseg*128] bf16
-    hist = x + 2 * nseg * kHeadDim * 2;             // [2][nseg*128*3] bf16
-    z = hist + 2 * nseg * kHeadDim * 3 * 2;         // [2][G*128] bf16
-    q = z + 2 * G * kHeadDim * 2;                   // [128] fp32
-    k = q + kHeadDim * 4;                           // [128] fp32
-    v = k + kHeadDim * 4;                           // [G][128] fp32
-    o = v + G * kHeadDim * 4;                       // [128] fp32
-    red = o + kHeadDim * 4;                         // [32] fp32
-    ab = red + 32 * 4;                              // [G][4] fp32: alpha, beta
-    bars = ab + kMaxGroup * 4 * 4;                  // mbarriers
-    total = bars + (2 * kStages + 4) * 8 + 16;
+  int stages, stage, x, hist, z, q, k, v, o, red, ab, bars, total;
+  __host__ __device__ Layout(int G, int P) {
+    const int nseg = 2 + G;  // q, k, G value heads
+    int rest = 0;
+    x = rest;        rest += 2 * P * nseg * kHeadDim * 2;   // [2][P][nseg*128] bf16
+    hist = rest;     rest += 2 * nseg * kHeadDim * 3 * 2;   // [2][nseg*128*3] bf16
+    z = rest;        rest += 2 * P * G * kHeadDim * 2;      // [2][P][G*128] bf16
+    q = rest;        rest += P * kHeadDim * 4;              // [P][128] fp32
+    k = rest;        rest += P * kHeadDim * 4;              // [P][128] fp32
+    v = rest;        rest += G * P * kHeadDim * 4;          // [G][P][128] fp32
+    o = rest;        rest += P * kHeadDim * 4;              // [P][128] fp32
+    red = rest;      rest += P * 32 * 4;                    // [P][32] fp32 partial sums
+    ab = rest;       rest += kMaxGroup * kMaxPos * 4 * 4;   // [G][P][4] alpha, beta
+    bars = rest;     rest += (2 * kMaxStages + 4) * 8 + 16; // mbarriers + abort flag
+    stages = (kSmemLimit - rest) / (int)kHalfBytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    const int off = stages * (int)kHalfBytes;
+    stage = 0;
+    x += off; hist += off; z += off; q += off; k += off; v += off; o += off; red += off; ab += off; bars += off;
+    total = off + rest;
   }
 };
 
@@ -81,11 +91,27 @@ __device__ __forceinline__ void bulk_g2s_nohint(void* smem_dst, const void* gsrc
       : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const StepArgs p, const int units_per_cta,
+// Slot that receives the state after position p: the live slot (decode) or the
+// position's checkpoint slot (speculative verify). -1 when out of range.
+__device__ __forceinline__ bool unit_slots_ok(const StepArgs& p, int n) {
+  const int slot = p.slot_idx[n];
+  if (slot < 0 || slot >= p.Rs) return false;
+  if (p.spec_slot)
+    for (int q = 0; q < p.P; ++q) {
+      const int s = p.spec_slot[n * p.P + q];
+      if (s < 0 || s >= p.Rs) return false;
+    }
+  return true;
+}
+
+// kOne: exactly one position (decode), so the per-position vectors are loaded once per unit.
+template <bool kOne>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, const int units_per_cta,
                                                              const int extra) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int G = p.G;
-  const Layout L(G);
+  const int G = p.G, P = kOne ? 1 : p.P;
+  const Layout L(G, P);
+  const int S_N = L.stages;
   float* stage = reinterpret_cast<float*>(smem + L.stage);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.x);
   uint16_t* hs = reinterpret_cast<uint16_t*>(smem + L.hist);
@@ -97,20 +123,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const StepArgs p, c
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* ab = reinterpret_cast<float*>(smem + L.ab);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + kStages;
-  uint64_t* in_full = empty + kStages;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* in_full = empty + kMaxStages;
   uint64_t* in_empty = in_full + 2;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(in_empty + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nseg = 2 + G;
+  const int xrow_len = nseg * kHeadDim;  // bf16 per position in the x buffer
   // contiguous range of units: the first `extra` CTAs take one more
   const int c = blockIdx.x;
   const int u0 = c * units_per_cta + min(c, extra);
   const int nunits = units_per_cta + (c < extra ? 1 : 0);
+  const bool want_z = p.ogate != nullptr;  // z may be NULL when only o is written
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S_N; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -130,32 +158,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const StepArgs p, c
     int t = 0, kin = 0;
     for (int i = 0; i < nunits && !*abort_flag; ++i) {
       const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
+      if (!unit_slots_ok(p, n)) continue;  // the consumers skip the same unit
       const int slot = p.slot_idx[n];
-      if (slot < 0 || slot >= p.Rs) continue;  // the consumers skip the same unit
       const int b = kin & 1;
       if (!mbar_wait_bounded(&in_empty[b], ((kin >> 1) & 1) ^ 1)) { *abort_flag = 1; break; }
-      const bool want_z = p.ogate != nullptr;  // z may be NULL when only o is written
-      const uint32_t in_bytes = nseg * kHeadDim * 2 + nseg * kHeadDim * 6 + (want_z ? G * kHeadDim * 2 : 0);
+      const uint32_t in_bytes = P * (nseg * kHeadDim * 2 + (want_z ? G * kHeadDim * 2 : 0)) + nseg * kHeadDim * 6;
       mbar_arrive_expect_tx(&in_full[b], in_bytes);
-      const uint16_t* xrow = p.qkv0 + (size_t)n * p.CH;
-      uint16_t* xb = xs + b * nseg * kHeadDim;
-      bulk_g2s_nohint(xb, xrow + j * kHeadDim, kHeadDim * 2, &in_full[b]);
-      bulk_g2s_nohint(xb + kHeadDim, xrow + (p.Hk + j) * kHeadDim, kHeadDim * 2, &in_full[b]);
-      bulk_g2s_nohint(xb + 2 * kHeadDim, xrow + (2 * p.Hk + G * j) * kHeadDim, G * kHeadDim * 2, &in_full[b]);
+      for (int q = 0; q < P; ++q) {
+        const uint16_t* xrow = p.qkv0 + (size_t)(n * P + q) * p.CH;
+        uint16_t* xb = xs + (b * P + q) * xrow_len;
+        bulk_g2s_nohint(xb, xrow + j * kHeadDim, kHeadDim * 2, &in_full[b]);
+        bulk_g2s_nohint(xb + kHeadDim, xrow + (p.Hk + j) * kHeadDim, kHeadDim * 2, &in_full[b]);
+        bulk_g2s_nohint(xb + 2 * kHeadDim, xrow + (2 * p.Hk + G * j) * kHeadDim, G * kHeadDim * 2, &in_full[b]);
+        if (want_z)
+          bulk_g2s_nohint(zs + (b * P + q) * G * kHeadDim, p.z + ((size_t)(n * P + q) * p.Hv + G * j) * kHeadDim,
+                          G * kHeadDim * 2, &in_full[b]);
+      }
       const uint16_t* hrow = p.conv_hist + (size_t)slot * p.CH * 3;
       uint16_t* hb = hs + b * nseg * kHeadDim * 3;
       bulk_g2s(hb, hrow + (size_t)j * kHeadDim * 3, kHeadDim * 6, &in_full[b], pol);
       bulk_g2s(hb + kHeadDim * 3, hrow + (size_t)(p.Hk + j) * kHeadDim * 3, kHeadDim * 6, &in_full[b], pol);
       bulk_g2s(hb + 2 * kHeadDim * 3, hrow + (size_t)(2 * p.Hk + G * j) * kHeadDim * 3, G * kHeadDim * 6,
                &in_full[b], pol);
-      if (want_z)
-        bulk_g2s_nohint(zs + b * G * kHeadDim, p.z + ((size_t)n * p.Hv + G * j) * kHeadDim, G * kHeadDim * 2,
-                        &in_full[b]);
       ++kin;
       const float* sbase = p.state + ((size_t)slot * p.Hv + G * j) * (kHeadDim * kHeadDim);
       for (int h2 = 0; h2 < 2 * G; ++h2, ++t) {
-        const int s = t % kStages;
-        if (!mbar_wait_bounded(&empty[s], ((t / kStages) & 1) ^ 1)) { *abort_flag = 1; break; }
+        const int s = t % S_N;
+        if (!mbar_wait_bounded(&empty[s], ((t / S_N) & 1) ^ 1)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&full[s], kHalfBytes);
         const float* src = sbase + (size_t)h2 * kHalfFloats;
         float* dst = stage + s * kHalfFloats;
@@ -166,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const StepArgs p, c
     if (*abort_flag) {
       report(p.dev_err, GDN_DEVERR_TIMEOUT);
       // let copies already in flight land before the CTA may exit (bounded)
-      for (int back = 1; back <= kStages && t - back >= 0; ++back) {
+      for (int back = 1; back <= S_N && t - back >= 0; ++back) {
         const int tt = t - back;
-        mbar_wait_bounded(&full[tt % kStages], (tt / kStages) & 1);
+        mbar_wait_bounded(&full[tt % S_N], (tt / S_N) & 1);
       }
     }
     return;
@@ -183,15 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const StepArgs p, c
   int t = 0, kin = 0;
   for (int i = 0; i < nunits; ++i) {
     const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
-    const int slot = p.slot_idx[n];
-    if (slot < 0) continue;
-    if (slot >= p.Rs) {
-      if (ctid == 0) report(p.dev_err, GDN_DEVERR_SLOT);
+    if (!unit_slots_ok(p, n)) {
+      if (ctid == 0 && p.slot_idx[n] >= 0) report(p.dev_err, GDN_DEVERR_SLOT);
       continue;
     }
+    const int slot = p.slot_idx[n];
     const int b = kin & 1;
-    if (ctid < G) {
-      const size_t ai = (size_t)n * p.Hv + G * j + ctid;
+    if (ctid < G * P) {
+      const int g = ctid / P, q = ctid % P;
+      const size_t ai = (size_t)(n * P + q) * p.Hv + G * j + g;
       ab[ctid * 4 + 0] = p.alpha[ai];
       ab[ctid * 4 + 1] = p.beta[ai];
     }
@@ -201,141 +230,178 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const StepArgs p, c
       *abort_flag = 1;
       report(p.dev_err, GDN_DEVERR_TIMEOUT);
     }
-    // ---- conv + SiLU of the unit's channels; new history straight to HBM
-    const uint16_t* xb = xs + b * nseg * kHeadDim;
+    // ---- conv + SiLU of the unit's channels for every position; the history
+    // after each position goes to its checkpoint slot (verify), or the final
+    // one back to the live slot (decode)
     const uint16_t* hb = hs + b * nseg * kHeadDim * 3;
-    uint16_t* hrow = p.conv_hist + (size_t)slot * p.CH * 3;
     for (int cc = ctid; cc < nseg * kHeadDim && !dead; cc += kConsumers) {
       const int seg = cc >> 7, d = cc & 127;
       const int gc = seg == 0 ? j * kHeadDim + d
                    : seg == 1 ? (p.Hk + j) * kHeadDim + d
                               : (2 * p.Hk + G * j + (seg - 2)) * kHeadDim + d;
       const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w) + gc);
-      const uint16_t x0 = xb[cc], h0 = hb[cc * 3], h1 = hb[cc * 3 + 1], h2 = hb[cc * 3 + 2];
-      float pre = w.x * bf16_to_f32(x0);
-      pre = fmaf(w.y, bf16_to_f32(h2), pre);
-      pre = fmaf(w.z, bf16_to_f32(h1), pre);
-      pre = fmaf(w.w, bf16_to_f32(h0), pre);
-      const float y = silu(pre);
-      if (seg == 0) qs[d] = y;
-      else if (seg == 1) ks[d] = y;
-      else vs[(seg - 2) * kHeadDim + d] = y;
-      uint16_t* hp = hrow + (size_t)gc * 3;
-      hp[0] = h1;
-      hp[1] = h2;
-      hp[2] = x0;
+      uint16_t h0 = hb[cc * 3], h1 = hb[cc * 3 + 1], h2 = hb[cc * 3 + 2];
+      for (int q = 0; q < P; ++q) {
+        const uint16_t x0 = xs[(b * P + q) * xrow_len + cc];
+        float pre = w.x * bf16_to_f32(x0);
+        pre = fmaf(w.y, bf16_to_f32(h2), pre);
+        pre = fmaf(w.z, bf16_to_f32(h1), pre);
+        pre = fmaf(w.w, bf16_to_f32(h0), pre);
+        const float y = silu(pre);
+        if (seg == 0) qs[q * kHeadDim + d] = y;
+        else if (seg == 1) ks[q * kHeadDim + d] = y;
+        else vs[((seg - 2) * P + q) * kHeadDim + d] = y;
+        h0 = h1;
+        h1 = h2;
+        h2 = x0;
+        if (p.spec_slot) {
+          uint16_t* hp = p.conv_hist + ((size_t)p.spec_slot[n * P + q] * p.CH + gc) * 3;
+          hp[0] = h0;
+          hp[1] = h1;
+          hp[2] = h2;
+        }
+      }
+      if (!p.spec_slot) {
+        uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc) * 3;
+        hp[0] = h0;
+        hp[1] = h1;
+        hp[2] = h2;
+      }
     }
     consumer_sync();
-    // ---- L2 norm of q (warps 0-3) and k (warps 4-7), then k . q
-    {
-      float* vec = warp < 4 ? qs : ks;
-      float x = 0.f;
+    // ---- L2 norm of q (warps 0-3) and k (warps 4-7) per position, then k . q
+    for (int q = 0; q < P; ++q)
       if (warp < 8) {
-        x = vec[(warp & 3) * 32 + lane];
+        const float x = (warp < 4 ? qs : ks)[q * kHeadDim + (warp & 3) * 32 + lane];
         const float ss = warp_sum(x * x);
-        if (lane == 0) red[warp] = ss;
+        if (lane == 0) red[q * 32 + warp] = ss;
       }
-      consumer_sync();
+    consumer_sync();
+    for (int q = 0; q < P; ++q)
       if (warp < 8) {
-        const float* r = red + (warp < 4 ? 0 : 4);
-        vec[(warp & 3) * 32 + lane] = x * rsqrtf(((r[0] + r[1]) + (r[2] + r[3])) + 1e-12f);
+        const float* r = red + q * 32 + (warp < 4 ? 0 : 4);
+        (warp < 4 ? qs : ks)[q * kHeadDim + (warp & 3) * 32 + lane] *=
+            rsqrtf(((r[0] + r[1]) + (r[2] + r[3])) + 1e-12f);
       }
-      consumer_sync();
+    consumer_sync();
+    for (int q = 0; q < P; ++q)
       if (warp < 4) {
-        const float kqp = warp_sum(ks[warp * 32 + lane] * qs[warp * 32 + lane]);
-        if (lane == 0) red[8 + warp] = kqp;
+        const float kqp = warp_sum(ks[q * kHeadDim + warp * 32 + lane] * qs[q * kHeadDim + warp * 32 + lane]);
+        if (lane == 0) red[q * 32 + 8 + warp] = kqp;
       }
-      consumer_sync();
-    }
-    const float kq = (red[8] + red[9]) + (red[10] + red[11]);
+    consumer_sync();
+
     // Row layout: the 8 lanes 8r..8r+7 of a warp share one state row; lane
     // c = lane & 7 holds columns 4c + 32m .. 4c + 32m + 3 for m = 0..3, so each
     // 16-byte access of a quarter-warp covers 128 contiguous bytes of one row
     // (conflict-free in shared memory, full sectors in HBM) and the row's dot
     // products need three shuffle levels.
     const int sub = lane >> 3, cl = lane & 7;
-    float4 kk[4], qq[4];
+    float4 kk1[4], qq1[4];
+    float kq1 = 0.f;
+    if constexpr (kOne) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      kk[m] = reinterpret_cast<const float4*>(ks)[cl + 8 * m];
-      qq[m] = reinterpret_cast<const float4*>(qs)[cl + 8 * m];
+      for (int m = 0; m < 4; ++m) {
+        kk1[m] = reinterpret_cast<const float4*>(ks)[cl + 8 * m];
+        qq1[m] = reinterpret_cast<const float4*>(qs)[cl + 8 * m];
+      }
+      kq1 = (red[8] + red[9]) + (red[10] + red[11]);
     }
-
     for (int g = 0; g < G; ++g) {
       const int h = G * j + g;
-      const float a = ab[g * 4 + 0], bb = ab[g * 4 + 1];
-      const float* vg = vs + g * kHeadDim;
-      float* Sg = p.state + ((size_t)slot * p.Hv + h) * (kHeadDim * kHeadDim);
       for (int hh = 0; hh < 2; ++hh, ++t) {
-        const int s = t % kStages;
+        const int s = t % S_N;
         dead = dead || *abort_flag;
-        if (!dead && !mbar_wait_bounded(&full[s], (t / kStages) & 1)) {
+        if (!dead && !mbar_wait_bounded(&full[s], (t / S_N) & 1)) {
           dead = true;
           *abort_flag = 1;
           report(p.dev_err, GDN_DEVERR_TIMEOUT);
         }
-        const float* st = stage + s * kHalfFloats;
         if (!dead) {
           const int lr = warp * kRowsPerWarp + sub;
-          const int i = hh * kHalfRows + lr;
-          const float* srow = st + lr * kHeadDim;
+          const int ri = hh * kHalfRows + lr;  // row of the head's state
+          const float* srow = stage + s * kHalfFloats + lr * kHeadDim;
           float4 sv[4];
 #pragma unroll
           for (int m = 0; m < 4; ++m) sv[m] = reinterpret_cast<const float4*>(srow)[cl + 8 * m];
-          float pk = 0.f, pq = 0.f;
+          for (int q = 0; q < P; ++q) {
+            const float a = ab[(g * P + q) * 4 + 0], bb = ab[(g * P + q) * 4 + 1];
+            float kq;
+            float4 kk[4], qq[4];
+            if constexpr (kOne) {
+              kq = kq1;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            pk = fmaf(sv[m].x, kk[m].x, pk);
-            pk = fmaf(sv[m].y, kk[m].y, pk);
-            pk = fmaf(sv[m].z, kk[m].z, pk);
-            pk = fmaf(sv[m].w, kk[m].w, pk);
-            pq = fmaf(sv[m].x, qq[m].x, pq);
-            pq = fmaf(sv[m].y, qq[m].y, pq);
-            pq = fmaf(sv[m].z, qq[m].z, pq);
-            pq = fmaf(sv[m].w, qq[m].w, pq);
-          }
+              for (int m = 0; m < 4; ++m) {
+                kk[m] = kk1[m];
+                qq[m] = qq1[m];
+              }
+            } else {
+              kq = (red[q * 32 + 8] + red[q * 32 + 9]) + (red[q * 32 + 10] + red[q * 32 + 11]);
 #pragma unroll
-          for (int x = 1; x < 8; x <<= 1) {
-            pk += __shfl_xor_sync(0xffffffffu, pk, x);  // (S k)_i over the row's 8 lanes
-            pq += __shfl_xor_sync(0xffffffffu, pq, x);  // (S q)_i
-          }
-          const float e = vg[i] - a * pk;  // v - Sbar k
-          const float be = bb * e;
-          float* grow = Sg + i * kHeadDim;
+              for (int m = 0; m < 4; ++m) {
+                kk[m] = reinterpret_cast<const float4*>(ks + q * kHeadDim)[cl + 8 * m];
+                qq[m] = reinterpret_cast<const float4*>(qs + q * kHeadDim)[cl + 8 * m];
+              }
+            }
+            float pk = 0.f, pq = 0.f;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            float4 ns;
-            ns.x = fmaf(be, kk[m].x, a * sv[m].x);
-            ns.y = fmaf(be, kk[m].y, a * sv[m].y);
-            ns.z = fmaf(be, kk[m].z, a * sv[m].z);
-            ns.w = fmaf(be, kk[m].w, a * sv[m].w);
-            st_global_v4_hint(grow + 4 * (cl + 8 * m), ns, wpol);
+            for (int m = 0; m < 4; ++m) {
+              pk = fmaf(sv[m].x, kk[m].x, pk);
+              pk = fmaf(sv[m].y, kk[m].y, pk);
+              pk = fmaf(sv[m].z, kk[m].z, pk);
+              pk = fmaf(sv[m].w, kk[m].w, pk);
+              pq = fmaf(sv[m].x, qq[m].x, pq);
+              pq = fmaf(sv[m].y, qq[m].y, pq);
+              pq = fmaf(sv[m].z, qq[m].z, pq);
+              pq = fmaf(sv[m].w, qq[m].w, pq);
+            }
+#pragma unroll
+            for (int x = 1; x < 8; x <<= 1) {
+              pk += __shfl_xor_sync(0xffffffffu, pk, x);  // (S k)_i over the row's 8 lanes
+              pq += __shfl_xor_sync(0xffffffffu, pq, x);  // (S q)_i
+            }
+            const float e = vs[(g * P + q) * kHeadDim + ri] - a * pk;  // v - Sbar k
+            const float be = bb * e;
+            const int oslot = p.spec_slot ? p.spec_slot[n * P + q] : slot;
+            float* grow = p.state + (((size_t)oslot * p.Hv + h) * kHeadDim + ri) * kHeadDim;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              sv[m].x = fmaf(be, kk[m].x, a * sv[m].x);
+              sv[m].y = fmaf(be, kk[m].y, a * sv[m].y);
+              sv[m].z = fmaf(be, kk[m].z, a * sv[m].z);
+              sv[m].w = fmaf(be, kk[m].w, a * sv[m].w);
+              st_global_v4_hint(grow + 4 * (cl + 8 * m), sv[m], wpol);
+            }
+            if (cl == 0) os[q * kHeadDim + ri] = fmaf(be, kq, a * pq) * kInvSqrtDk;
           }
-          if (cl == 0) os[i] = fmaf(be, kq, a * pq) * kInvSqrtDk;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       consumer_sync();
-      // ---- gated RMSNorm of head h
-      float oi = 0.f;
-      if (ctid < kHeadDim) {
-        oi = os[ctid];
-        const float ss = warp_sum(oi * oi);
-        if (lane == 0) red[16 + warp] = ss;
-      }
-      consumer_sync();
-      if (ctid < kHeadDim && !dead) {
-        const float ms = ((red[16] + red[17]) + (red[18] + red[19])) * (1.0f / kHeadDim);
-        const float rinv = rsqrtf(ms + p.eps);
-        const size_t row = ((size_t)n * p.Hv + h) * kHeadDim + ctid;
-        if (p.o) p.o[row] = f32_to_bf16(oi);
-        if (p.ogate) {
-          const float zz = bf16_to_f32(zs[b * G * kHeadDim + g * kHeadDim + ctid]);
-          p.ogate[row] = f32_to_bf16(oi * rinv * p.gamma[ctid] * silu(zz));
+      // ---- gated RMSNorm of head h at every position; thread (q, i) for q < 4
+      for (int q0 = 0; q0 < P; q0 += 4) {
+        const int q = q0 + (ctid >> 7), i = ctid & 127;
+        float oi = 0.f;
+        if (q < P) {
+          oi = os[q * kHeadDim + i];
+          const float ss = warp_sum(oi * oi);
+          if (lane == 0) red[q * 32 + 16 + ((ctid >> 5) & 3)] = ss;
         }
+        consumer_sync();
+        if (q < P && !dead) {
+          const float* r = red + q * 32 + 16;
+          const float ms = ((r[0] + r[1]) + (r[2] + r[3])) * (1.0f / kHeadDim);
+          const float rinv = rsqrtf(ms + p.eps);
+          const size_t row = ((size_t)(n * P + q) * p.Hv + h) * kHeadDim + i;
+          if (p.o) p.o[row] = f32_to_bf16(oi);
+          if (p.ogate) {
+            const float zz = bf16_to_f32(zs[((b * P + q) * G + g) * kHeadDim + i]);
+            p.ogate[row] = f32_to_bf16(oi * rinv * p.gamma[i] * silu(zz));
+          }
+        }
+        consumer_sync();
       }
-      consumer_sync();
     }
     if (ctid == 0) mbar_arrive(&in_empty[b]);
     ++kin;
@@ -355,16 +421,23 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
-  const size_t smem = Layout(a.G).total;
-  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(&decode_kernel), smem);
+bool stream_supported(int G, int P) { return P >= 1 && P <= kMaxPos && Layout(G, P).stages >= 2; }
+
+cudaError_t launch_stream(const StepArgs& a, cudaStream_t stream) {
+  const Layout L(a.G, a.P);
+  if (L.stages < 2 || a.P > kMaxPos) return cudaErrorInvalidValue;
+  const bool one = a.P == 1 && a.spec_slot == nullptr;
+  const void* fn = one ? reinterpret_cast<const void*>(&stream_kernel<true>)
+                       : reinterpret_cast<const void*>(&stream_kernel<false>);
+  cudaError_t err = ensure_dynamic_smem(fn, L.total);
   if (err != cudaSuccess) return err;
   const int units = a.N * a.Hk;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = units < sms ? units : sms;
   const int per = units / grid, extra = units % grid;
-  decode_kernel<<<grid, kThreads, smem, stream>>>(a, per, extra);
+  if (one) stream_kernel<true><<<grid, kThreads, L.total, stream>>>(a, per, extra);
+  else stream_kernel<false><<<grid, kThreads, L.total, stream>>>(a, per, extra);
   return cudaGetLastError();
 }
 

@@ -82,7 +82,9 @@ cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
 size_t step_smem_bytes(int P);
 cudaError_t launch_step(const StepArgs& a, bool spec, cudaStream_t stream);
-cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
+// Persistent state-streaming kernel (decode: P = 1, spec_slot NULL; verify: P >= 1).
+bool stream_supported(int G, int P);
+cudaError_t launch_stream(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);

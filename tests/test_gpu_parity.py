@@ -301,3 +301,43 @@ def test_prefill_bad_offsets_are_flagged(b):
     assert og[:5].any() and not og[5:].any()  # the valid request ran, the flagged one wrote nothing
     s1 = int(w["slot_idx"][1])
     np.testing.assert_array_equal(d["state"][s1].cpu().numpy(), w["state"][s1])
+
+
+# ---------------------------------------------------------------- geometry and position variants
+
+GEOMS = [synth.Dims(4, 4, 128, 128, 4), synth.Dims(2, 16, 128, 128, 4)]  # G = 1 and G = 8
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=["G1", "G8"])
+def test_decode_group_sizes(b, geom):
+    w = synth.decode_workload(geom, 9, 20, seed=60)
+    d, o, og = _run_decode(b, w)
+    _check_decode(w, d, o, og)
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=["G1", "G8"])
+def test_prefill_group_sizes(b, geom):
+    w = synth.prefill_workload(geom, [3, 70, 129], seed=61)
+    d, o, og = _run_prefill(b, w)
+    _check_prefill(w, d, o, og, np.arange(3))
+
+
+@pytest.mark.parametrize("P", [1, 2, 8])
+def test_spec_verify_positions(b, P):
+    dims = synth.RANK_HEADS
+    N = 6
+    w = synth.spec_workload(dims, N, num_pos=P, seed=62 + P)
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    og = torch.zeros((N * P, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_spec_verify(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"], d["spec_slot_idx"],
+                      d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    ref = oracle.spec_verify(dims, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], w["slot_idx"],
+                             w["spec_slot_idx"], w["alpha"], w["beta"], w["z"], w["gamma"], w["eps"])
+    U.check_out(U.host_f64_from_bf16(og), ref["ogate"], "ogate")
+    ck = w["spec_slot_idx"].reshape(-1)
+    idx = torch.from_numpy(ck.astype(np.int64)).cuda()
+    U.check_state(d["state"][idx].cpu().numpy(), ref["state"][ck], U.STATE_REL_L2_DECODE, "checkpoints")
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), ref["conv_hist"][ck])
