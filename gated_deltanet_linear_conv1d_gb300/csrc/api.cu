@@ -200,7 +200,8 @@ gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const floa
   if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
   if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
   if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
-  if ((o && !aligned(o, 8)) || (ogate && (!aligned(ogate, 8) || !aligned(z, 8) || !aligned(gamma, 16))))
+  if (num_tokens > 0 && !aligned(qkv0, 16)) return GDN_ERR_INVALID_ARG;
+  if ((o && !aligned(o, 8)) || (ogate && (!aligned(ogate, 16) || !aligned(z, 16) || !aligned(gamma, 16))))
     return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_prefill_workspace_bytes(d, num_seqs, num_tokens);
   if (workspace_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 256))))

@@ -32,6 +32,10 @@
 // tf32 operands; the others take bf16 (measured against the fp64 oracle:
 // state error ~6e-4, output error ~3e-3 relative L2).
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "device.cuh"
 #include "launch.h"
@@ -51,20 +55,27 @@ constexpr float kInvSqrtDk = 0.08838834764831845f;
 constexpr int kKQ = 0;                  // bf16 [128 dk][128 t]: k tokens 0-63, q tokens 64-127 (MN-major)
 constexpr int kKG = kKQ + 32768;        // bf16 [128 dk][64 t]: k e^g (MN-major B)      | later E bf16 [128 dv][64 t]
 constexpr int kKT = kKG + 16384;        // tf32 [128 dk][64 t]: raw k (K-major B)
-constexpr int kVS = kKT + 32768;        // fp32 [128 dv][65]: v, channel-major, padded
-constexpr int kS0 = kVS + 33792;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
-constexpr int kAM = kS0 + 32768;        // fp32 [64][65]: A for the inverse
-constexpr int kTS = kAM + 17408;        // fp32 [64][65]: T, row-major
-constexpr int kTB = kTS + 17408;        // tf32 [64 r][64 i]: T diag(b) (K-major B)
+constexpr int kS0 = kKT + 32768;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
+// Scratch: raw QKV0 rows of a chunk [3 parts][64 t][128] bf16 (bulk-copied, read by
+// the conv), later the inverse's A [64][65], T [64][65] and block sums [3][16][17];
+// then the raw rows of the next chunk. Its tail holds the chunk's z rows [64][128]
+// bf16, overwritten in place by Ogate before they are bulk-stored.
+constexpr int kSCR = kS0 + 32768;
+constexpr int kXS = kSCR;               // raw QKV0 rows, 49152 B
+constexpr int kAM = kSCR;               // fp32 [64][65]
+constexpr int kTS = kAM + 16640;        // fp32 [64][65]
+constexpr int kMS = kTS + 16640;        // fp32 [3][16][17]
+constexpr int kZS = kSCR + 49152;       // bf16 [64][128]: z rows, then Ogate rows
+constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major B)
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
 constexpr int kSmall = kPB + 8192;      // small per-chunk vectors
 constexpr int kSmallFloats = 64 * 8 + 8 * 64 + 4 * 64 + 64;
-constexpr int kMS = kSmall + kSmallFloats * 4;  // fp32 [3][16][17]: inverse scratch
-constexpr int kBars = kMS + 3 * 272 * 4;
-constexpr int kSmemBytes = kBars + 64;
+constexpr int kBars = kSmall + kSmallFloats * 4;
+constexpr int kSmemBytes = kBars + 128;
 
-// Tensor-memory columns.
-constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_X = 192, kT_Z = 256, kT_E = 320, kT_O = 384, kTmemCols = 512;
+// Tensor-memory columns (v, fp32 channel-major, lives in the last 64).
+constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_X = 192, kT_Z = 256, kT_E = 320, kT_O = 384, kT_V = 448,
+                   kTmemCols = 512;
 
 __device__ __forceinline__ float to_tf32(float x) { return umma::to_tf32(x); }
 
@@ -100,6 +111,14 @@ __device__ __forceinline__ int tok8(int lane) {
   return ((lane >> 2) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
 }
 
+// 2^x via the hardware approximation (ex2.approx); its error is far below the
+// bf16 / tf32 rounding that every use of it is followed by.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
 }
@@ -120,7 +139,12 @@ __device__ __forceinline__ void sync_for_mma() {
   umma::fence_after_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillArgs p) {
+// Tensor maps: tmx over QKV0 [T][CH] (box 64 tokens x 128 channels); tmz, tmo over
+// z and Ogate [T][Hv][128] (box 64 tokens x 1 head x 128).
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillArgs p,
+                                                                  const __grid_constant__ CUtensorMap tmx,
+                                                                  const __grid_constant__ CUtensorMap tmz,
+                                                                  const __grid_constant__ CUtensorMap tmo) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int h = blockIdx.x, n = blockIdx.y;
   const int g = h % p.G, j = h / p.G;
@@ -146,14 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   uint16_t* KQ = reinterpret_cast<uint16_t*>(smem + kKQ);
   unsigned char* KGb = smem + kKG;
   unsigned char* KTb = smem + kKT;
-  float* VS = reinterpret_cast<float*>(smem + kVS);
+  const uint16_t* XS = reinterpret_cast<const uint16_t*>(smem + kXS);
+  uint16_t* ZS = reinterpret_cast<uint16_t*>(smem + kZS);
   unsigned char* S0b = smem + kS0;
   float* AM = reinterpret_cast<float*>(smem + kAM);
   float* TS = reinterpret_cast<float*>(smem + kTS);
   unsigned char* TBb = smem + kTB;
   unsigned char* PBb = smem + kPB;
   float* small = reinterpret_cast<float*>(smem + kSmall);
-  float* gv = small;             // [64] g
+  float* gv = small;             // [64] g / ln 2 (cumulative log2 of alpha)
   float* egv = gv + 64;          // [64] e^g
   float* glv = egv + 64;         // [64] e^{g_C - g_t} (0 past the chunk end)
   float* bv = glv + 64;          // [64] beta
@@ -164,8 +189,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* npart = scan + 64;      // [8][64] norm partials (warps 0-3: q, 4-7: k)
   float* rpart = npart + 8 * 64; // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);  // 0: [K;Q]K^T  1: X,Z  2: E  3: S, O'
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+  // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5: z rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+  const bool want_gate = p.ogate != nullptr;
+  // Thread 0: TMA the raw QKV0 rows (q_j, k_j, v_h segments, 64 tokens each, from
+  // token tcs) into the scratch area. Rows past the request are masked by the
+  // conv; rows past T arrive as zeros.
+  auto issue_x = [&](int tcs) {
+    mbar_arrive_expect_tx(&bars[4], (uint32_t)(3 * kC * kHeadDim * 2));
+    tma_load_2d(smem + kXS + 0 * kC * 256, &tmx, j * kHeadDim, tcs, &bars[4]);
+    tma_load_2d(smem + kXS + 1 * kC * 256, &tmx, (p.Hk + j) * kHeadDim, tcs, &bars[4]);
+    tma_load_2d(smem + kXS + 2 * kC * 256, &tmx, (2 * p.Hk + h) * kHeadDim, tcs, &bars[4]);
+  };
 
   // ---- conv channels of this thread: q (tid < 128) and v (tid < 128), or k
   const bool qv = tid < 128;
@@ -186,8 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 
   if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
-    for (int b = 0; b < 4; ++b) mbar_init(&bars[b], 1);
+    for (int b = 0; b < 6; ++b) mbar_init(&bars[b], 1);
     fence_mbar_init();
+    issue_x(t0);  // raw rows of the first chunk
   }
   umma::fence_before_sync();
   // All CTAs of the key-head group have read the old history from here on.
@@ -229,12 +266,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     const int L = min(kC, t1 - tc);
     const uint32_t par = c & 1;
 
+    // ---- z rows of the chunk (the previous chunk's Ogate store must have read ZS)
+    if (tid == 0 && want_gate) {
+      bulk_wait_read_all();
+      mbar_arrive_expect_tx(&bars[5], (uint32_t)(kC * kHeadDim * 2));
+      tma_load_3d(ZS, &tmz, 0, h, tc, &bars[5]);
+    }
+
     // ---- gates: g = inclusive cumsum of ln(alpha), e^g, beta
     if (tid < kC) {
       float la = 0.f, b = 0.f;
       if (tid < L) {
         const size_t ai = (size_t)(tc + tid) * p.Hv + h;
-        la = fmaxf(logf(p.alpha[ai]), -80.f);
+        la = fmaxf(log2f(p.alpha[ai]), -115.f);  // log2(alpha), alpha in (0, 1]
         b = p.beta[ai];
       }
       float s = la;
@@ -250,33 +294,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (tid < kC) {
       const float gt = scan[tid] + (tid >= 32 ? scan[31] : 0.f);
       gv[tid] = gt;
-      egv[tid] = expf(gt);
+      egv[tid] = ex2(gt);
     }
     __syncthreads();
-    if (tid < kC) glv[tid] = tid < L ? expf(gv[L - 1] - gv[tid]) : 0.f;
+    if (tid < kC) glv[tid] = tid < L ? ex2(gv[L - 1] - gv[tid]) : 0.f;
 
-    // ---- conv + SiLU: every input of the chunk is loaded first (one memory
-    // round trip), then 8 tokens at a time, operands written channel-major
-    uint32_t xa2[kC / 2], xv2[kC / 2];  // bf16 pairs (token 2i low, 2i+1 high)
+    // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time;
+    // q, k written channel-major to shared memory, v to tensor memory
+    if (!wait_mma(&bars[4], par)) { ok = false; break; }
+    const uint16_t* xa_s = XS + (qv ? 0 : kC) * kHeadDim + d;  // q or k part, channel d
+    const uint16_t* xv_s = XS + 2 * kC * kHeadDim + d;          // v part
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      float yv32[32];
 #pragma unroll
-    for (int i = 0; i < kC / 2; ++i) {
-      uint32_t a = 0, v = 0;
-      const int t = 2 * i;
-      if (t < L) {
-        const size_t xr = (size_t)(tc + t) * p.CH;
-        a = p.qkv0[xr + gc_a];
-        if (qv) v = p.qkv0[xr + gc_v];
-      }
-      if (t + 1 < L) {
-        const size_t xr = (size_t)(tc + t + 1) * p.CH;
-        a |= (uint32_t)p.qkv0[xr + gc_a] << 16;
-        if (qv) v |= (uint32_t)p.qkv0[xr + gc_v] << 16;
-      }
-      xa2[i] = a;
-      xv2[i] = v;
-    }
-#pragma unroll
-    for (int grp = 0; grp < kC / 8; ++grp) {
+      for (int gi = 0; gi < 4; ++gi) {
+      const int grp = hf * 4 + gi;
       float ya[8], yv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -284,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         ya[e] = 0.f;
         yv[e] = 0.f;
         if (t < L) {
-          const uint16_t xa = (uint16_t)(xa2[t >> 1] >> ((t & 1) * 16));
+          const uint16_t xa = xa_s[t * kHeadDim];
           float pre = wa.x * bf16_to_f32(xa);
           pre = fmaf(wa.y, bf16_to_f32(ha[2]), pre);
           pre = fmaf(wa.z, bf16_to_f32(ha[1]), pre);
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           ya[e] = silu(pre);
           ha[0] = ha[1]; ha[1] = ha[2]; ha[2] = xa;
           if (qv) {
-            const uint16_t xv = (uint16_t)(xv2[t >> 1] >> ((t & 1) * 16));
+            const uint16_t xv = xv_s[t * kHeadDim];
             float pv = wv.x * bf16_to_f32(xv);
             pv = fmaf(wv.y, bf16_to_f32(hv[2]), pv);
             pv = fmaf(wv.z, bf16_to_f32(hv[1]), pv);
@@ -326,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
             make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) VS[d * 65 + grp * 8 + e] = yv[e];
+        for (int e = 0; e < 8; ++e) yv32[gi * 8 + e] = yv[e];
       }
       // per-token sum of squares of the raw q (warps 0-3) or k (warps 4-7)
       float sq[8];
@@ -334,7 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
       const float tot = reduce8(sq, lane);
       if ((lane & 3) == 0) npart[warp * 64 + grp * 8 + tok8(lane)] = tot;
+      }
+      if (qv) umma::st32_nowait(tm + lane_base + kT_V + hf * 32, yv32);  // v rows d = this thread's lane
     }
+    if (qv) umma::wait_st();
     sync_for_mma();
 
     // ---- [K;Q] K^T (bf16): D1 lanes 0-63 = K K^T rows, lanes 64-127 = Q K^T rows
@@ -398,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int i = half * 32 + e;
-          AM[r * 65 + i] = i < r ? br * expf(gr - gv[i]) * v[e] * ikr * ikv[i] : 0.f;
+          AM[r * 65 + i] = i < r ? br * ex2(gr - gv[i]) * v[e] * ikr * ikv[i] : 0.f;
         }
       } else {
         const int r = row - 64;
@@ -409,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int i = half * 32 + q8 * 8 + e;
-            pe[e] = i <= r ? expf(gr - gv[i]) * v[q8 * 8 + e] * iqr * ikv[i] : 0.f;
+            pe[e] = i <= r ? ex2(gr - gv[i]) * v[q8 * 8 + e] * iqr * ikv[i] : 0.f;
           }
           uint4 pk;
           pk.x = pack_bf16(pe[0], pe[1]);
@@ -477,16 +513,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     }
     // ---- Y = V^T - X (tf32, rows dv), over S0's now-free space
     if (!wait_mma(&bars[1], par)) { ok = false; break; }
+    // the scratch area is free again (A and T consumed): raw rows of the next chunk
+    if (tid == 0 && c + 1 < nchunks) issue_x(tc + kC);
     {
-      float v[32];
+      float v[32], vv[32];
       umma::ld32(tm + lane_base + kT_X + half * 32, v);
+      umma::ld32(tm + lane_base + kT_V + half * 32, vv);
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
         float y4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int t = half * 32 + q4 * 4 + e;
-          y4[e] = to_tf32(VS[row * 65 + t] - v[q4 * 4 + e] * ikv[t]);
+          y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * ikv[t]);
         }
         *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (half * 32 + q4 * 4) * 4, 256)) =
             make_float4(y4[0], y4[1], y4[2], y4[3]);
@@ -540,18 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
                                umma::smem_desc(sPB + kk * 256, 128, false), id_o, kk > 0);
       umma::commit(&bars[3]);
     }
-    // this thread's 32 gate inputs z, fetched while the last MMAs run
-    uint32_t zz2[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      uint32_t v = 0;
-      const int t = half * 32 + 2 * i;
-      if (p.ogate) {
-        if (t < L) v = p.z[((size_t)(tc + t) * p.Hv + h) * kHeadDim + row];
-        if (t + 1 < L) v |= (uint32_t)p.z[((size_t)(tc + t + 1) * p.Hv + h) * kHeadDim + row] << 16;
-      }
-      zz2[i] = v;
-    }
     if (!wait_mma(&bars[3], par)) { ok = false; break; }
     // ---- o = (e^g Z / |q| + O') / sqrt(dk), then the gated RMSNorm over dv
     float ov[32];
@@ -577,23 +604,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (tid < kC)
       rinv[tid] = rsqrtf(((rpart[tid] + rpart[64 + tid]) + (rpart[128 + tid] + rpart[192 + tid])) *
                              (1.0f / kHeadDim) + p.eps);
-    __syncthreads();
+    if (want_gate && !wait_mma(&bars[5], par)) { ok = false; break; }  // z rows landed (also syncs)
+    if (!want_gate) __syncthreads();
     {
-      const float gm = p.ogate ? p.gamma[row] : 0.f;
+      if (p.o) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = half * 32 + e;
-        if (t < L) {
-          const size_t idx = ((size_t)(tc + t) * p.Hv + h) * kHeadDim + row;
-          if (p.o) p.o[idx] = f32_to_bf16(ov[e]);
-          if (p.ogate) {
-            const uint16_t zb = (uint16_t)(zz2[e >> 1] >> ((e & 1) * 16));
-            p.ogate[idx] = f32_to_bf16(ov[e] * rinv[t] * gm * silu(bf16_to_f32(zb)));
-          }
+        for (int e = 0; e < 32; ++e) {
+          const int t = half * 32 + e;
+          if (t < L) p.o[((size_t)(tc + t) * p.Hv + h) * kHeadDim + row] = f32_to_bf16(ov[e]);
+        }
+      }
+      if (want_gate) {
+        // Ogate over the z rows in place (thread: column `row` of 32 token rows) ...
+        const float gm = p.gamma[row];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int t = half * 32 + e;
+          uint16_t* zp = ZS + t * kHeadDim + row;
+          *zp = f32_to_bf16(ov[e] * rinv[t] * gm * silu(bf16_to_f32(*zp)));
         }
       }
     }
+    umma::fence_proxy_async_smem();
     __syncthreads();
+    // ... then stored with one tensor copy (a partial last chunk row by row, so
+    // that the next request's rows are not touched); the next chunk's z rows
+    // wait until these stores have read ZS
+    if (tid == 0 && want_gate) {
+      if (L == kC) {
+        tma_store_3d(&tmo, 0, h, tc, ZS);
+      } else {
+        for (int t = 0; t < L; ++t)
+          bulk_s2g(p.ogate + ((size_t)(tc + t) * p.Hv + h) * kHeadDim, ZS + t * kHeadDim, 256);
+      }
+      bulk_commit();
+    }
   }
 
   if (ok) {
@@ -618,17 +663,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   } else {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
     // give MMAs still in flight a second bounded chance before the memory is freed
-    for (int b = 0; b < 4; ++b) mbar_wait_bounded(&bars[b], 0);
+    for (int b = 0; b < 6; ++b) mbar_wait_bounded(&bars[b], 0);
   }
+  if (tid == 0) bulk_wait_all();  // Ogate rows stored
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 0) umma::tmem_dealloc(tm, kTmemCols);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// bf16 tensor map of `rank` dims (innermost first) with a box of `box` elements.
+bool encode_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                 const cuuint32_t* box) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  CUtensorMap tmx{}, tmz{}, tmo{};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.CH, (cuuint64_t)a.T};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.CH * 2};
+    const cuuint32_t box[2] = {kHeadDim, kC};
+    if (!encode_bf16(&tmx, a.qkv0, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  if (a.ogate) {
+    const cuuint64_t dims[3] = {kHeadDim, (cuuint64_t)a.Hv, (cuuint64_t)a.T};
+    const cuuint64_t strides[2] = {kHeadDim * 2, (cuuint64_t)a.Hv * kHeadDim * 2};
+    const cuuint32_t box[3] = {kHeadDim, 1, kC};
+    if (!encode_bf16(&tmz, a.z, 3, dims, strides, box) || !encode_bf16(&tmo, a.ogate, 3, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(&prefill_tc_kernel), kSmemBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -643,7 +728,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, a, tmx, tmz, tmo);
 }
 
 }  // namespace gdn
