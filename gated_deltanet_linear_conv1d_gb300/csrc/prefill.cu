@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "device.cuh"
 #include "launch.h"
@@ -300,77 +301,105 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (tid < kC) glv[tid] = tid < L ? ex2(gv[L - 1] - gv[tid]) : 0.f;
 
     // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time;
-    // q, k written channel-major to shared memory, v to tensor memory
+    // q, k written channel-major to shared memory, v to tensor memory. The v
+    // channel of lane d is split by tokens: warps 0-3 (which also carry q) take
+    // tokens 0-31, warps 4-7 (k) take 32-63. Every token row of the staging
+    // area is valid to read (rows past T arrive as zeros), so the loop runs
+    // branch-free over all 64 rows and masks outputs past the chunk end.
     if (!wait_mma(&bars[4], par)) { ok = false; break; }
     const uint16_t* xa_s = XS + (qv ? 0 : kC) * kHeadDim + d;  // q or k part, channel d
     const uint16_t* xv_s = XS + 2 * kC * kHeadDim + d;          // v part
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
+    auto conv_half = [&](auto qv_c, auto hf_c) {
+      constexpr bool kQV = decltype(qv_c)::value;
+      constexpr int kHF = decltype(hf_c)::value;
+      constexpr bool kV = kQV == (kHF == 0);  // v computed here for these 32 tokens
+      // windows (oldest first): a runs on from the previous half; v starts from
+      // the slot history (q/v warps, tokens 0..) or from rows 29-31 (k warps, 32..)
+      uint16_t wv3[3];
+      if constexpr (kQV) {
+        wv3[0] = hv[0]; wv3[1] = hv[1]; wv3[2] = hv[2];
+      } else {
+        wv3[0] = xv_s[29 * kHeadDim]; wv3[1] = xv_s[30 * kHeadDim]; wv3[2] = xv_s[31 * kHeadDim];
+      }
       float yv32[32];
 #pragma unroll
       for (int gi = 0; gi < 4; ++gi) {
-      const int grp = hf * 4 + gi;
-      float ya[8], yv[8];
+        const int grp = kHF * 4 + gi;
+        float ya[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int t = grp * 8 + e;
-        ya[e] = 0.f;
-        yv[e] = 0.f;
-        if (t < L) {
+        for (int e = 0; e < 8; ++e) {
+          const int t = grp * 8 + e;
           const uint16_t xa = xa_s[t * kHeadDim];
           float pre = wa.x * bf16_to_f32(xa);
           pre = fmaf(wa.y, bf16_to_f32(ha[2]), pre);
           pre = fmaf(wa.z, bf16_to_f32(ha[1]), pre);
           pre = fmaf(wa.w, bf16_to_f32(ha[0]), pre);
-          ya[e] = silu(pre);
+          ya[e] = t < L ? silu(pre) : 0.f;
           ha[0] = ha[1]; ha[1] = ha[2]; ha[2] = xa;
-          if (qv) {
+          if constexpr (kV) {
             const uint16_t xv = xv_s[t * kHeadDim];
             float pv = wv.x * bf16_to_f32(xv);
-            pv = fmaf(wv.y, bf16_to_f32(hv[2]), pv);
-            pv = fmaf(wv.z, bf16_to_f32(hv[1]), pv);
-            pv = fmaf(wv.w, bf16_to_f32(hv[0]), pv);
-            yv[e] = silu(pv);
-            hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
+            pv = fmaf(wv.y, bf16_to_f32(wv3[2]), pv);
+            pv = fmaf(wv.z, bf16_to_f32(wv3[1]), pv);
+            pv = fmaf(wv.w, bf16_to_f32(wv3[0]), pv);
+            yv32[gi * 8 + e] = t < L ? silu(pv) : 0.f;
+            wv3[0] = wv3[1]; wv3[1] = wv3[2]; wv3[2] = xv;
           }
         }
+        // raw q or k, bf16: row d of KQ, tokens (q ? 64 : 0) + 8 grp ...
+        {
+          uint4 pk;
+          pk.x = pack_bf16(ya[0], ya[1]);
+          pk.y = pack_bf16(ya[2], ya[3]);
+          pk.z = pack_bf16(ya[4], ya[5]);
+          pk.w = pack_bf16(ya[6], ya[7]);
+          const int col = (kQV ? 64 : 0) + grp * 8;
+          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(d, col * 2, 256)) = pk;
+        }
+        if constexpr (!kQV) {
+          uint4 pk;
+          const int t = grp * 8;
+          pk.x = pack_bf16(ya[0] * egv[t + 0], ya[1] * egv[t + 1]);
+          pk.y = pack_bf16(ya[2] * egv[t + 2], ya[3] * egv[t + 3]);
+          pk.z = pack_bf16(ya[4] * egv[t + 4], ya[5] * egv[t + 5]);
+          pk.w = pack_bf16(ya[6] * egv[t + 6], ya[7] * egv[t + 7]);
+          *reinterpret_cast<uint4*>(KGb + umma::tile_off(d, t * 2, 128)) = pk;
+          *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4, 256)) =
+              make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
+          *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
+              make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+        }
+        // per-token sum of squares of the raw q (warps 0-3) or k (warps 4-7)
+        float sq[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
+        const float tot = reduce8(sq, lane);
+        if ((lane & 3) == 0) npart[warp * 64 + grp * 8 + tok8(lane)] = tot;
       }
-      // raw q or k, bf16: row d of KQ, tokens (qv ? 64 : 0) + 8 grp ...
-      {
-        uint4 pk;
-        pk.x = pack_bf16(ya[0], ya[1]);
-        pk.y = pack_bf16(ya[2], ya[3]);
-        pk.z = pack_bf16(ya[4], ya[5]);
-        pk.w = pack_bf16(ya[6], ya[7]);
-        const int col = (qv ? 64 : 0) + grp * 8;
-        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(d, col * 2, 256)) = pk;
-      }
-      if (!qv) {
-        uint4 pk;
-        const int t = grp * 8;
-        pk.x = pack_bf16(ya[0] * egv[t + 0], ya[1] * egv[t + 1]);
-        pk.y = pack_bf16(ya[2] * egv[t + 2], ya[3] * egv[t + 3]);
-        pk.z = pack_bf16(ya[4] * egv[t + 4], ya[5] * egv[t + 5]);
-        pk.w = pack_bf16(ya[6] * egv[t + 6], ya[7] * egv[t + 7]);
-        *reinterpret_cast<uint4*>(KGb + umma::tile_off(d, t * 2, 128)) = pk;
-        *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4, 256)) =
-            make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
-        *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
-            make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+      // v rows d = this thread's lane, columns 32 hf ..
+      if constexpr (kV) umma::st32_nowait(tm + lane_base + kT_V + kHF * 32, yv32);
+    };
+    {
+      // the windows carried to the next chunk: raw rows L-3 .. L-1, reaching
+      // back into the previous window when the chunk is shorter than 3
+      const uint16_t na[3] = {L >= 3 ? xa_s[(L - 3) * kHeadDim] : (L == 2 ? ha[2] : ha[1]),
+                              L >= 2 ? xa_s[(L - 2) * kHeadDim] : ha[2], xa_s[(L - 1) * kHeadDim]};
+      const uint16_t nv[3] = {L >= 3 ? xv_s[(L - 3) * kHeadDim] : (L == 2 ? hv[2] : hv[1]),
+                              L >= 2 ? xv_s[(L - 2) * kHeadDim] : hv[2], xv_s[(L - 1) * kHeadDim]};
+      if (qv) {
+        conv_half(std::true_type{}, std::integral_constant<int, 0>{});
+        conv_half(std::true_type{}, std::integral_constant<int, 1>{});
       } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) yv32[gi * 8 + e] = yv[e];
+        conv_half(std::false_type{}, std::integral_constant<int, 0>{});
+        conv_half(std::false_type{}, std::integral_constant<int, 1>{});
       }
-      // per-token sum of squares of the raw q (warps 0-3) or k (warps 4-7)
-      float sq[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
-      const float tot = reduce8(sq, lane);
-      if ((lane & 3) == 0) npart[warp * 64 + grp * 8 + tok8(lane)] = tot;
+      for (int i = 0; i < 3; ++i) {
+        ha[i] = na[i];
+        hv[i] = nv[i];
       }
-      if (qv) umma::st32_nowait(tm + lane_base + kT_V + hf * 32, yv32);  // v rows d = this thread's lane
     }
-    if (qv) umma::wait_st();
+    umma::wait_st();
     sync_for_mma();
 
     // ---- [K;Q] K^T (bf16): D1 lanes 0-63 = K K^T rows, lanes 64-127 = Q K^T rows
