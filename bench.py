@@ -142,11 +142,12 @@ def prefill_bytes(geom, lengths, has_init) -> float:
     return float(total + geom.channels * geom.conv_kernel * 4 + geom.head_v_dim * 4)
 
 
-def load_traffic(kernel: str):
-    """dram read+write bytes per launch from a committed ncu summary, if its source hash still matches."""
+def load_traffic(summary: str, source: str):
+    """dram read+write bytes per launch from a committed ncu summary, if the kernel source it was
+    taken on (its sha256 prefix is recorded in the summary) is unchanged."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}.md")
-    src = os.path.join(ROOT, "gated_deltanet_linear_conv1d_gb300", "csrc", "decode.cu")
+    path = os.path.join(ROOT, "profiles", f"{summary}.md")
+    src = os.path.join(ROOT, "gated_deltanet_linear_conv1d_gb300", "csrc", source)
     try:
         text = open(path).read()
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -534,7 +535,7 @@ def run_gpu(args):
     bytes_launch = decode_bytes_per_launch(geom, N)
     mean_kernel_ms = sum(kernel_ms) / len(kernel_ms)
     achieved = bytes_launch / (mean_kernel_ms / 1e3) / 1e9
-    traffic = load_traffic("decode_step_256x48")
+    traffic = load_traffic("stream_kernel_decode_256x48", "decode.cu")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
