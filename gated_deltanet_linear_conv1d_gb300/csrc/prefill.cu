@@ -58,14 +58,17 @@ constexpr int kKG = kKQ + 32768;        // bf16 [128 dk][64 t]: k e^g (MN-major 
 constexpr int kKT = kKG + 16384;        // tf32 [128 dk][64 t]: raw k (K-major B)
 constexpr int kS0 = kKT + 32768;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
 // Scratch: raw QKV0 rows of a chunk [3 parts][64 t][128] bf16 (bulk-copied, read by
-// the conv), later the inverse's A [64][65], T [64][65] and block sums [3][16][17];
+// the conv), later the inverse's A [64][68], T [64][68] and block products [3][16][20];
 // then the raw rows of the next chunk. Its tail holds the chunk's z rows [64][128]
 // bf16, overwritten in place by Ogate before they are bulk-stored.
 constexpr int kSCR = kS0 + 32768;
 constexpr int kXS = kSCR;               // raw QKV0 rows, 49152 B
-constexpr int kAM = kSCR;               // fp32 [64][65]
-constexpr int kTS = kAM + 16640;        // fp32 [64][65]
-constexpr int kMS = kTS + 16640;        // fp32 [3][16][17]
+constexpr int kLd = 68;                 // row stride (floats) of A and T: 16-byte aligned rows
+constexpr int kMsLd = 20, kMsBlk = 16 * kMsLd;  // M blocks [3][16][20]
+constexpr int kAM = kSCR;               // fp32 [64][kLd]
+constexpr int kTS = kAM + 64 * kLd * 4;  // fp32 [64][kLd]
+constexpr int kMS = kTS + 64 * kLd * 4;  // fp32 [3][16][kMsLd]
+static_assert(kMS + 3 * kMsBlk * 4 <= kSCR + 49152, "inverse scratch overlaps the z rows");
 constexpr int kZS = kSCR + 49152;       // bf16 [64][128]: z rows, then Ogate rows
 constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major B)
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
@@ -120,8 +123,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Two floats to a bf16 pair (round to nearest even), a in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
+}
+
+// SiLU(x) = x / (1 + e^-x) with e^-x = 2^(-x log2 e), on the flush-to-zero
+// ex2 and reciprocal approximations. Large negative x gives -0.
+__device__ __forceinline__ float silu_ftz(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return x * r;
 }
 
 // Waits for an MMA-completion phase; the verdict is uniform over the CTA.
@@ -334,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           pre = fmaf(wa.y, bf16_to_f32(ha[2]), pre);
           pre = fmaf(wa.z, bf16_to_f32(ha[1]), pre);
           pre = fmaf(wa.w, bf16_to_f32(ha[0]), pre);
-          ya[e] = t < L ? silu(pre) : 0.f;
+          ya[e] = t < L ? silu_ftz(pre) : 0.f;
           ha[0] = ha[1]; ha[1] = ha[2]; ha[2] = xa;
           if constexpr (kV) {
             const uint16_t xv = xv_s[t * kHeadDim];
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
             pv = fmaf(wv.y, bf16_to_f32(wv3[2]), pv);
             pv = fmaf(wv.z, bf16_to_f32(wv3[1]), pv);
             pv = fmaf(wv.w, bf16_to_f32(wv3[0]), pv);
-            yv32[gi * 8 + e] = t < L ? silu(pv) : 0.f;
+            yv32[gi * 8 + e] = t < L ? silu_ftz(pv) : 0.f;
             wv3[0] = wv3[1]; wv3[1] = wv3[2]; wv3[2] = xv;
           }
         }
@@ -461,9 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         const int r = row;
         const float br = bv[r], gr = gv[r], ikr = ikv[r];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int i = half * 32 + e;
-          AM[r * 65 + i] = i < r ? br * ex2(gr - gv[i]) * v[e] * ikr * ikv[i] : 0.f;
+        for (int e4 = 0; e4 < 8; ++e4) {
+          float a4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = half * 32 + e4 * 4 + e;
+            a4[e] = i < r ? br * ex2(gr - gv[i]) * v[e4 * 4 + e] * ikr * ikv[i] : 0.f;
+          }
+          *reinterpret_cast<float4*>(AM + r * kLd + half * 32 + e4 * 4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
       } else {
         const int r = row - 64;
@@ -486,58 +506,86 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       }
     }
     __syncthreads();
-    // ---- T = (I + A)^-1, blocked by 16 (T row-major in TS). Diagonal blocks by
-    // forward substitution (one column per thread); then the off-diagonal
-    // blocks one block diagonal at a time: T_ab = -T_aa sum_{b<=c<a} A_ac T_cb.
-    for (int it = tid; it < kC * kC; it += kThreads) TS[(it >> 6) * 65 + (it & 63)] = 0.f;
-    __syncthreads();
+    // ---- T = (I + A)^-1, blocked by 16 (T row-major in TS, rows of kLd floats).
+    // Diagonal blocks by forward substitution (one column per thread); then the
+    // off-diagonal blocks one block diagonal at a time, T_ab = -T_aa M with
+    // M = sum_{b<=c<a} A_ac T_cb, each thread producing 4 adjacent columns from
+    // 16-byte shared-memory loads. The strictly upper blocks are never written:
+    // the Tb pass below masks them.
     if (tid < kC) {
       const int a = tid >> 4, cc = tid & 15;
-      const float* Ab = AM + (16 * a) * 65 + 16 * a;
+      const float* Ab = AM + (16 * a) * kLd + 16 * a;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
         float s = 0.f;
 #pragma unroll
-        for (int i = 0; i < r; ++i) s = fmaf(Ab[r * 65 + i], x[i], s);
+        for (int i = 0; i < r; ++i) s = fmaf(Ab[r * kLd + i], x[i], s);
         x[r] = r < cc ? 0.f : (r == cc ? 1.f : -s);
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) TS[(16 * a + r) * 65 + 16 * a + cc] = x[r];
+      for (int r = 0; r < 16; ++r) TS[(16 * a + r) * kLd + 16 * a + cc] = x[r];
     }
     __syncthreads();
 #pragma unroll 1
     for (int dist = 1; dist < 4; ++dist) {
       const int nblk = 4 - dist;  // blocks (a, a - dist) for a = dist .. 3
-      for (int it = tid; it < nblk * 256; it += kThreads) {
-        const int blk = it >> 8, r = (it >> 4) & 15, col = it & 15;
-        const int a = dist + blk, b = a - dist;
-        const float* ar = AM + (16 * a + r) * 65;
-        float s = 0.f;
-#pragma unroll 4
-        for (int i = 16 * b; i < 16 * a; ++i) s = fmaf(ar[i], TS[i * 65 + 16 * b + col], s);
-        MS[blk * 272 + r * 17 + col] = s;
+      const bool act = tid < nblk * 64;
+      const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = tid & 3;
+      const int a = dist + blk, b = a - dist;
+      if (act) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* ar = AM + (16 * a + r) * kLd;
+        const float* tc0 = TS + 16 * b + 4 * c4;
+#pragma unroll 2
+        for (int i0 = 16 * b; i0 < 16 * a; i0 += 4) {
+          const float4 av = *reinterpret_cast<const float4*>(ar + i0);
+          const float ae[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 tv = *reinterpret_cast<const float4*>(tc0 + (i0 + e) * kLd);
+            acc.x = fmaf(ae[e], tv.x, acc.x);
+            acc.y = fmaf(ae[e], tv.y, acc.y);
+            acc.z = fmaf(ae[e], tv.z, acc.z);
+            acc.w = fmaf(ae[e], tv.w, acc.w);
+          }
+        }
+        *reinterpret_cast<float4*>(MS + blk * kMsBlk + r * kMsLd + 4 * c4) = acc;
       }
       __syncthreads();
-      for (int it = tid; it < nblk * 256; it += kThreads) {
-        const int blk = it >> 8, r = (it >> 4) & 15, col = it & 15;
-        const int a = dist + blk, b = a - dist;
-        const float* tr = TS + (16 * a + r) * 65 + 16 * a;
-        float s = 0.f;
+      if (act) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* tr = TS + (16 * a + r) * kLd + 16 * a;
+        const float* mc = MS + blk * kMsBlk + 4 * c4;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s = fmaf(tr[i], MS[blk * 272 + i * 17 + col], s);
-        TS[(16 * a + r) * 65 + 16 * b + col] = -s;
+        for (int i0 = 0; i0 < 16; i0 += 4) {
+          const float4 tv4 = *reinterpret_cast<const float4*>(tr + i0);
+          const float te[4] = {tv4.x, tv4.y, tv4.z, tv4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 mv = *reinterpret_cast<const float4*>(mc + (i0 + e) * kMsLd);
+            acc.x = fmaf(te[e], mv.x, acc.x);
+            acc.y = fmaf(te[e], mv.y, acc.y);
+            acc.z = fmaf(te[e], mv.z, acc.z);
+            acc.w = fmaf(te[e], mv.w, acc.w);
+          }
+        }
+        *reinterpret_cast<float4*>(TS + (16 * a + r) * kLd + 16 * b + 4 * c4) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
       __syncthreads();
     }
     // ---- Tb = T diag(beta) as a tf32 K-major operand: rows r, 16-byte chunks of 4 columns
     for (int it = tid; it < kC * 16; it += kThreads) {
       const int r = it >> 4, ck = it & 15;
-      float4 f;
-      f.x = to_tf32(TS[r * 65 + 4 * ck + 0] * bv[4 * ck + 0]);
-      f.y = to_tf32(TS[r * 65 + 4 * ck + 1] * bv[4 * ck + 1]);
-      f.z = to_tf32(TS[r * 65 + 4 * ck + 2] * bv[4 * ck + 2]);
-      f.w = to_tf32(TS[r * 65 + 4 * ck + 3] * bv[4 * ck + 3]);
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if ((ck >> 2) <= (r >> 4)) {  // on or below the block diagonal
+        const float4 t4 = *reinterpret_cast<const float4*>(TS + r * kLd + 4 * ck);
+        f.x = to_tf32(t4.x * bv[4 * ck + 0]);
+        f.y = to_tf32(t4.y * bv[4 * ck + 1]);
+        f.z = to_tf32(t4.z * bv[4 * ck + 2]);
+        f.w = to_tf32(t4.w * bv[4 * ck + 3]);
+      }
       *reinterpret_cast<float4*>(TBb + umma::tile_off(r, ck * 16, 256)) = f;
     }
     // ---- Y = V^T - X (tf32, rows dv), over S0's now-free space
@@ -650,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         for (int e = 0; e < 32; ++e) {
           const int t = half * 32 + e;
           uint16_t* zp = ZS + t * kHeadDim + row;
-          *zp = f32_to_bf16(ov[e] * rinv[t] * gm * silu(bf16_to_f32(*zp)));
+          *zp = f32_to_bf16(ov[e] * rinv[t] * gm * silu_ftz(bf16_to_f32(*zp)));
         }
       }
     }
