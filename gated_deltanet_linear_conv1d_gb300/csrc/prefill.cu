@@ -14,16 +14,19 @@
 // with q, k unit-normalised; the per-token norms are folded into the
 // products' readouts, so the tensor cores take the raw conv outputs.
 //
-// One CTA per (value head h, request n), 256 threads; the G CTAs of a key
-// head form a cluster (only to order the in-place conv-history update). The
-// fp32 state lives in tensor memory (128 lanes x 128 columns) for the whole
-// request. Per chunk:
-//   conv + SiLU (CUDA cores, thread = channel)  -> raw q, k (bf16, channel-major),
-//       k e^g (bf16), k (tf32, channel-major), v (fp32), per-token |q|, |k|
+// One CTA per (value head h, request n), 512 threads (16 warps, four per
+// tensor-memory lane quarter, splitting the columns of every readout); the G
+// CTAs of a key head form a cluster (only to order the in-place conv-history
+// update). The fp32 state lives in tensor memory (128 lanes x 128 columns) for
+// the whole request. The raw QKV0 rows and the z rows of the next chunk are
+// fetched by TMA while the current chunk runs. Per chunk:
+//   conv + SiLU (CUDA cores, thread = channel x token range) -> raw q, k (bf16,
+//       channel-major), k e^g (bf16), k (tf32, channel-major), v (fp32), |q|, |k|
 //   [K;Q] K^T                 tcgen05 bf16  M=128 N=64  K=128  (operands MN-major)
 //   S0 -> bf16 operand, S *= e^{g_C} in tensor memory
 //   X = S0 Kg^T, Z = S0 Q^T   tcgen05 bf16  M=128 N=64  K=128
-//   A, P from K K^T, Q K^T;  T = (I + A)^-1 on CUDA cores (blocked by 16)
+//   A, P from K K^T, Q K^T;  T = (I + A)^-1 on CUDA cores (recursive doubling
+//       over 16-row blocks), written as Tb = T diag(b) in tf32
 //   Y = V^T - X  -> tf32;  E^T = Y Tb^T   tcgen05 tf32 M=128 N=64 K=64
 //   S += (E^T diag(Gamma_C / |k|)) K     tcgen05 tf32 M=128 N=128 K=64 (accumulate)
 //   O' = E^T P^T                tcgen05 bf16 M=128 N=64 K=64
@@ -48,7 +51,7 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 4 per tensor-memory lane quarter
 constexpr int kC = 64;  // chunk length
 constexpr float kInvSqrtDk = 0.08838834764831845f;
 
@@ -64,15 +67,16 @@ constexpr int kS0 = kKT + 32768;        // bf16 [128 dv][128 dk]: S0 (K-major A)
 constexpr int kSCR = kS0 + 32768;
 constexpr int kXS = kSCR;               // raw QKV0 rows, 49152 B
 constexpr int kLd = 68;                 // row stride (floats) of A and T: 16-byte aligned rows
-constexpr int kMsLd = 20, kMsBlk = 16 * kMsLd;  // M blocks [3][16][20]
+constexpr int kMsLd = 36;               // row stride (floats) of the inverse's block products
 constexpr int kAM = kSCR;               // fp32 [64][kLd]
 constexpr int kTS = kAM + 64 * kLd * 4;  // fp32 [64][kLd]
-constexpr int kMS = kTS + 64 * kLd * 4;  // fp32 [3][16][kMsLd]
-static_assert(kMS + 3 * kMsBlk * 4 <= kSCR + 49152, "inverse scratch overlaps the z rows");
-constexpr int kZS = kSCR + 49152;       // bf16 [64][128]: z rows, then Ogate rows
+constexpr int kMS = kTS + 64 * kLd * 4;  // fp32 [32][kMsLd]
+static_assert(kMS + 32 * kMsLd * 4 <= kSCR + 49152, "inverse scratch overlaps the z rows");
+constexpr int kZS = kSCR + 49152;       // bf16 [64][128]: z rows, then Ogate rows (even chunks)
 constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major B)
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
-constexpr int kSmall = kPB + 8192;      // small per-chunk vectors
+constexpr int kZS1 = kPB + 8192;        // bf16 [64][128]: the same for odd chunks
+constexpr int kSmall = kZS1 + 16384;    // small per-chunk vectors
 constexpr int kSmallFloats = 64 * 8 + 8 * 64 + 4 * 64 + 64;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
@@ -165,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const int h = blockIdx.x, n = blockIdx.y;
   const int g = h % p.G, j = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
+  // warp w reads tensor-memory lanes 32 (w % 4) ..; the four warps of a lane
+  // quarter split the columns of every readout (part = w / 4)
+  const int quarter = warp & 3, part = warp >> 2;
   const int row = 32 * quarter + lane;  // tensor-memory lane read by this thread
 
   // ---- request checks (uniform over the cluster: same request)
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   unsigned char* KGb = smem + kKG;
   unsigned char* KTb = smem + kKT;
   const uint16_t* XS = reinterpret_cast<const uint16_t*>(smem + kXS);
-  uint16_t* ZS = reinterpret_cast<uint16_t*>(smem + kZS);
+  auto zs_buf = [&](int zb) { return reinterpret_cast<uint16_t*>(smem + (zb ? kZS1 : kZS)); };
   unsigned char* S0b = smem + kS0;
   float* AM = reinterpret_cast<float*>(smem + kAM);
   float* TS = reinterpret_cast<float*>(smem + kTS);
@@ -205,9 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* npart = scan + 64;      // [8][64] norm partials (warps 0-3: q, 4-7: k)
   float* rpart = npart + 8 * 64; // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
-  // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5: z rows
+  // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5, 6: z rows
+  // of even / odd chunks
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
   const bool want_gate = p.ogate != nullptr;
   // Thread 0: TMA the raw QKV0 rows (q_j, k_j, v_h segments, 64 tokens each, from
   // token tcs) into the scratch area. Rows past the request are masked by the
@@ -218,30 +225,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     tma_load_2d(smem + kXS + 1 * kC * 256, &tmx, (p.Hk + j) * kHeadDim, tcs, &bars[4]);
     tma_load_2d(smem + kXS + 2 * kC * 256, &tmx, (2 * p.Hk + h) * kHeadDim, tcs, &bars[4]);
   };
+  // Thread 0: TMA the z rows of the chunk starting at token tcs into buffer zb.
+  auto issue_z = [&](int tcs, int zb) {
+    mbar_arrive_expect_tx(&bars[5 + zb], (uint32_t)(kC * kHeadDim * 2));
+    tma_load_3d(zs_buf(zb), &tmz, 0, h, tcs, &bars[5 + zb]);
+  };
 
-  // ---- conv channels of this thread: q (tid < 128) and v (tid < 128), or k
-  const bool qv = tid < 128;
-  const int d = qv ? tid : tid - 128;
-  const int gc_a = qv ? j * kHeadDim + d : (p.Hk + j) * kHeadDim + d;  // q or k channel
-  const int gc_v = (2 * p.Hk + h) * kHeadDim + d;                       // v channel (qv threads)
-  const float4 wa = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gc_a * kTaps);
-  const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gc_v * kTaps);
-  uint16_t ha[3] = {0, 0, 0}, hv[3] = {0, 0, 0};  // conv windows, oldest first
-  if (init) {
-    const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc_a) * 3;
-    ha[0] = hp[0]; ha[1] = hp[1]; ha[2] = hp[2];
-    if (qv) {
-      const uint16_t* hq = p.conv_hist + ((size_t)slot * p.CH + gc_v) * 3;
-      hv[0] = hq[0]; hv[1] = hq[1]; hv[2] = hq[2];
-    }
+  // ---- conv channel d = row of this thread: warps 0-3 q, 4-7 k, 8-11 v for the
+  // first 48 tokens of every chunk (each carries its channel's running window),
+  // warps 12-15 all three for the last 16 tokens
+  const int cset = part;
+  const int d = row;
+  const int gq = j * kHeadDim + d, gk = (p.Hk + j) * kHeadDim + d, gvc = (2 * p.Hk + h) * kHeadDim + d;
+  const float4 wq = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gq * kTaps);
+  const float4 wk = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gk * kTaps);
+  const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gvc * kTaps);
+  const int gown = cset == 0 ? gq : (cset == 1 ? gk : gvc);
+  uint16_t hw[3] = {0, 0, 0};  // running window (raw inputs, oldest first) of warps 0-11
+  if (init && cset < 3) {
+    const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gown) * 3;
+    hw[0] = hp[0]; hw[1] = hp[1]; hw[2] = hp[2];
   }
 
   if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
-    for (int b = 0; b < 6; ++b) mbar_init(&bars[b], 1);
+    for (int b = 0; b < 7; ++b) mbar_init(&bars[b], 1);
     fence_mbar_init();
     issue_x(t0);  // raw rows of the first chunk
+    if (want_gate) issue_z(t0, 0);
   }
+  // T diag(beta) above the block diagonal stays zero; the rest is rewritten per chunk
+  for (int it = tid; it < kC * kC / 4; it += kThreads)
+    reinterpret_cast<float4*>(TBb)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
   umma::fence_before_sync();
   // All CTAs of the key-head group have read the old history from here on.
   cg::this_cluster().sync();
@@ -249,19 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const uint32_t tm = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
 
-  // ---- initial state into tensor memory: thread (row, half) owns 64 columns
+  // ---- initial state into tensor memory: thread (row, part) owns 32 columns
   {
-    const float* src = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + half * 64;
+    const float* src = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + part * 32;
+    float v[32];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 f = init ? *reinterpret_cast<const float4*>(src + c * 32 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
-      }
-      umma::st32(tm + lane_base + kTS_S + half * 64 + c * 32, v);
+    for (int i = 0; i < 32; i += 4) {
+      const float4 f = init ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
     }
+    umma::st32(tm + lane_base + kTS_S + part * 32, v);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -277,25 +289,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 
   const int nchunks = (t1 - t0 + kC - 1) / kC;
   bool ok = true;
+  // alpha and beta of the next chunk are loaded one chunk ahead (thread t: token t)
+  float alpha_n = 1.f, beta_n = 0.f;
+  if (tid < min(kC, t1 - t0)) {
+    alpha_n = p.alpha[(size_t)(t0 + tid) * p.Hv + h];
+    beta_n = p.beta[(size_t)(t0 + tid) * p.Hv + h];
+  }
   for (int c = 0; c < nchunks && ok; ++c) {
     const int tc = t0 + c * kC;
     const int L = min(kC, t1 - tc);
     const uint32_t par = c & 1;
 
-    // ---- z rows of the chunk (the previous chunk's Ogate store must have read ZS)
-    if (tid == 0 && want_gate) {
-      bulk_wait_read_all();
-      mbar_arrive_expect_tx(&bars[5], (uint32_t)(kC * kHeadDim * 2));
-      tma_load_3d(ZS, &tmz, 0, h, tc, &bars[5]);
-    }
+    uint16_t* const ZS = zs_buf(c & 1);  // this chunk's z rows (TMA issued one chunk ahead)
 
-    // ---- gates: g = inclusive cumsum of ln(alpha), e^g, beta
+    // ---- gates: g = inclusive cumsum of log2(alpha) (so e^{g ln 2} = prod alpha), beta
     if (tid < kC) {
-      float la = 0.f, b = 0.f;
-      if (tid < L) {
-        const size_t ai = (size_t)(tc + tid) * p.Hv + h;
-        la = fmaxf(log2f(p.alpha[ai]), -115.f);  // log2(alpha), alpha in (0, 1]
-        b = p.beta[ai];
+      const float la = tid < L ? fmaxf(log2f(alpha_n), -115.f) : 0.f;  // alpha in (0, 1]
+      const float b = tid < L ? beta_n : 0.f;
+      if (c + 1 < nchunks && tid < min(kC, t1 - tc - kC)) {
+        alpha_n = p.alpha[(size_t)(tc + kC + tid) * p.Hv + h];
+        beta_n = p.beta[(size_t)(tc + kC + tid) * p.Hv + h];
       }
       float s = la;
 #pragma unroll
@@ -315,103 +328,105 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     __syncthreads();
     if (tid < kC) glv[tid] = tid < L ? ex2(gv[L - 1] - gv[tid]) : 0.f;
 
-    // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time;
-    // q, k written channel-major to shared memory, v to tensor memory. The v
-    // channel of lane d is split by tokens: warps 0-3 (which also carry q) take
-    // tokens 0-31, warps 4-7 (k) take 32-63. Every token row of the staging
-    // area is valid to read (rows past T arrive as zeros), so the loop runs
-    // branch-free over all 64 rows and masks outputs past the chunk end.
+    // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time; q, k
+    // written channel-major to shared memory, v to tensor memory. Every token
+    // row of the staging area is valid to read (rows past T arrive as zeros), so
+    // the loop runs branch-free and masks outputs past the chunk end.
     if (!wait_mma(&bars[4], par)) { ok = false; break; }
-    const uint16_t* xa_s = XS + (qv ? 0 : kC) * kHeadDim + d;  // q or k part, channel d
-    const uint16_t* xv_s = XS + 2 * kC * kHeadDim + d;          // v part
-    auto conv_half = [&](auto qv_c, auto hf_c) {
-      constexpr bool kQV = decltype(qv_c)::value;
-      constexpr int kHF = decltype(hf_c)::value;
-      constexpr bool kV = kQV == (kHF == 0);  // v computed here for these 32 tokens
-      // windows (oldest first): a runs on from the previous half; v starts from
-      // the slot history (q/v warps, tokens 0..) or from rows 29-31 (k warps, 32..)
-      uint16_t wv3[3];
-      if constexpr (kQV) {
-        wv3[0] = hv[0]; wv3[1] = hv[1]; wv3[2] = hv[2];
-      } else {
-        wv3[0] = xv_s[29 * kHeadDim]; wv3[1] = xv_s[30 * kHeadDim]; wv3[2] = xv_s[31 * kHeadDim];
-      }
-      float yv32[32];
+    {
+      // kind 0 q, 1 k, 2 v; tokens kT0 .. kT0 + kNT of channel d, window w3 running on
+      auto conv_seg = [&](auto kind_c, auto t0_c, auto nt_c, const float4 w, uint16_t (&w3)[3]) {
+        constexpr int kKind = decltype(kind_c)::value, kT0 = decltype(t0_c)::value, kNT = decltype(nt_c)::value;
+        const uint16_t* xs = XS + kKind * kC * kHeadDim + d;
+        float yv[kKind == 2 ? kNT : 1];
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi) {
-        const int grp = kHF * 4 + gi;
-        float ya[8];
+        for (int gi = 0; gi < kNT / 8; ++gi) {
+          const int grp = kT0 / 8 + gi;
+          float ya[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int t = grp * 8 + e;
-          const uint16_t xa = xa_s[t * kHeadDim];
-          float pre = wa.x * bf16_to_f32(xa);
-          pre = fmaf(wa.y, bf16_to_f32(ha[2]), pre);
-          pre = fmaf(wa.z, bf16_to_f32(ha[1]), pre);
-          pre = fmaf(wa.w, bf16_to_f32(ha[0]), pre);
-          ya[e] = t < L ? silu_ftz(pre) : 0.f;
-          ha[0] = ha[1]; ha[1] = ha[2]; ha[2] = xa;
-          if constexpr (kV) {
-            const uint16_t xv = xv_s[t * kHeadDim];
-            float pv = wv.x * bf16_to_f32(xv);
-            pv = fmaf(wv.y, bf16_to_f32(wv3[2]), pv);
-            pv = fmaf(wv.z, bf16_to_f32(wv3[1]), pv);
-            pv = fmaf(wv.w, bf16_to_f32(wv3[0]), pv);
-            yv32[gi * 8 + e] = t < L ? silu_ftz(pv) : 0.f;
-            wv3[0] = wv3[1]; wv3[1] = wv3[2]; wv3[2] = xv;
+          for (int e = 0; e < 8; ++e) {
+            const int t = grp * 8 + e;
+            const uint16_t x = xs[t * kHeadDim];
+            float pre = w.x * bf16_to_f32(x);
+            pre = fmaf(w.y, bf16_to_f32(w3[2]), pre);
+            pre = fmaf(w.z, bf16_to_f32(w3[1]), pre);
+            pre = fmaf(w.w, bf16_to_f32(w3[0]), pre);
+            ya[e] = t < L ? silu_ftz(pre) : 0.f;
+            w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
+          }
+          if constexpr (kKind == 2) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) yv[gi * 8 + e] = ya[e];
+          } else {
+            {  // raw q or k, bf16: row d of KQ, tokens (q ? 64 : 0) + 8 grp ...
+              uint4 pk;
+              pk.x = pack_bf16(ya[0], ya[1]);
+              pk.y = pack_bf16(ya[2], ya[3]);
+              pk.z = pack_bf16(ya[4], ya[5]);
+              pk.w = pack_bf16(ya[6], ya[7]);
+              const int col = (kKind == 0 ? 64 : 0) + grp * 8;
+              *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(d, col * 2, 256)) = pk;
+            }
+            if constexpr (kKind == 1) {
+              uint4 pk;
+              const int t = grp * 8;
+              pk.x = pack_bf16(ya[0] * egv[t + 0], ya[1] * egv[t + 1]);
+              pk.y = pack_bf16(ya[2] * egv[t + 2], ya[3] * egv[t + 3]);
+              pk.z = pack_bf16(ya[4] * egv[t + 4], ya[5] * egv[t + 5]);
+              pk.w = pack_bf16(ya[6] * egv[t + 6], ya[7] * egv[t + 7]);
+              *reinterpret_cast<uint4*>(KGb + umma::tile_off(d, t * 2, 128)) = pk;
+              *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4, 256)) =
+                  make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
+              *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
+                  make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+            }
+            // per-token sum of squares over this warp's 32 channels
+            float sq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
+            const float tot = reduce8(sq, lane);
+            if ((lane & 3) == 0) npart[(kKind * 4 + quarter) * 64 + grp * 8 + tok8(lane)] = tot;
           }
         }
-        // raw q or k, bf16: row d of KQ, tokens (q ? 64 : 0) + 8 grp ...
-        {
-          uint4 pk;
-          pk.x = pack_bf16(ya[0], ya[1]);
-          pk.y = pack_bf16(ya[2], ya[3]);
-          pk.z = pack_bf16(ya[4], ya[5]);
-          pk.w = pack_bf16(ya[6], ya[7]);
-          const int col = (kQV ? 64 : 0) + grp * 8;
-          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(d, col * 2, 256)) = pk;
+        if constexpr (kKind == 2) {  // v row d = this thread's lane, columns kT0 ..
+          if constexpr (kNT == 32) umma::st32_nowait(tm + lane_base + kT_V + kT0, yv);
+          else umma::st16_nowait(tm + lane_base + kT_V + kT0, yv);
         }
-        if constexpr (!kQV) {
-          uint4 pk;
-          const int t = grp * 8;
-          pk.x = pack_bf16(ya[0] * egv[t + 0], ya[1] * egv[t + 1]);
-          pk.y = pack_bf16(ya[2] * egv[t + 2], ya[3] * egv[t + 3]);
-          pk.z = pack_bf16(ya[4] * egv[t + 4], ya[5] * egv[t + 5]);
-          pk.w = pack_bf16(ya[6] * egv[t + 6], ya[7] * egv[t + 7]);
-          *reinterpret_cast<uint4*>(KGb + umma::tile_off(d, t * 2, 128)) = pk;
-          *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4, 256)) =
-              make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
-          *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
-              make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+      };
+      using I0 = std::integral_constant<int, 0>;
+      using I1 = std::integral_constant<int, 1>;
+      using I2 = std::integral_constant<int, 2>;
+      using I16 = std::integral_constant<int, 16>;
+      using I32 = std::integral_constant<int, 32>;
+      using I48 = std::integral_constant<int, 48>;
+      if (cset < 3) {
+        // the window carried to the next chunk: raw rows L-3 .. L-1, reaching
+        // back into the previous window when the chunk is shorter than 3
+        const uint16_t* xs = XS + cset * kC * kHeadDim + d;
+        const uint16_t nw[3] = {L >= 3 ? xs[(L - 3) * kHeadDim] : (L == 2 ? hw[2] : hw[1]),
+                                L >= 2 ? xs[(L - 2) * kHeadDim] : hw[2], xs[(L - 1) * kHeadDim]};
+        uint16_t w3[3] = {hw[0], hw[1], hw[2]};
+        if (cset == 0) {
+          conv_seg(I0{}, I0{}, I32{}, wq, w3);
+          conv_seg(I0{}, I32{}, I16{}, wq, w3);
+        } else if (cset == 1) {
+          conv_seg(I1{}, I0{}, I32{}, wk, w3);
+          conv_seg(I1{}, I32{}, I16{}, wk, w3);
+        } else {
+          conv_seg(I2{}, I0{}, I32{}, wv, w3);
+          conv_seg(I2{}, I32{}, I16{}, wv, w3);
         }
-        // per-token sum of squares of the raw q (warps 0-3) or k (warps 4-7)
-        float sq[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
-        const float tot = reduce8(sq, lane);
-        if ((lane & 3) == 0) npart[warp * 64 + grp * 8 + tok8(lane)] = tot;
-      }
-      // v rows d = this thread's lane, columns 32 hf ..
-      if constexpr (kV) umma::st32_nowait(tm + lane_base + kT_V + kHF * 32, yv32);
-    };
-    {
-      // the windows carried to the next chunk: raw rows L-3 .. L-1, reaching
-      // back into the previous window when the chunk is shorter than 3
-      const uint16_t na[3] = {L >= 3 ? xa_s[(L - 3) * kHeadDim] : (L == 2 ? ha[2] : ha[1]),
-                              L >= 2 ? xa_s[(L - 2) * kHeadDim] : ha[2], xa_s[(L - 1) * kHeadDim]};
-      const uint16_t nv[3] = {L >= 3 ? xv_s[(L - 3) * kHeadDim] : (L == 2 ? hv[2] : hv[1]),
-                              L >= 2 ? xv_s[(L - 2) * kHeadDim] : hv[2], xv_s[(L - 1) * kHeadDim]};
-      if (qv) {
-        conv_half(std::true_type{}, std::integral_constant<int, 0>{});
-        conv_half(std::true_type{}, std::integral_constant<int, 1>{});
+        hw[0] = nw[0]; hw[1] = nw[1]; hw[2] = nw[2];
       } else {
-        conv_half(std::false_type{}, std::integral_constant<int, 0>{});
-        conv_half(std::false_type{}, std::integral_constant<int, 1>{});
-      }
-#pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        ha[i] = na[i];
-        hv[i] = nv[i];
+        const uint16_t* xq = XS + d;
+        uint16_t w3[3] = {xq[45 * kHeadDim], xq[46 * kHeadDim], xq[47 * kHeadDim]};
+        conv_seg(I0{}, I48{}, I16{}, wq, w3);
+        const uint16_t* xk = xq + kC * kHeadDim;
+        uint16_t w4[3] = {xk[45 * kHeadDim], xk[46 * kHeadDim], xk[47 * kHeadDim]};
+        conv_seg(I1{}, I48{}, I16{}, wk, w4);
+        const uint16_t* xv = xk + kC * kHeadDim;
+        uint16_t w5[3] = {xv[45 * kHeadDim], xv[46 * kHeadDim], xv[47 * kHeadDim]};
+        conv_seg(I2{}, I48{}, I16{}, wv, w5);
       }
     }
     umma::wait_st();
@@ -435,25 +450,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // ---- S0 as a bf16 operand; S *= e^{g_C} in tensor memory for the update below
     {
       const float decay = egv[L - 1];
+      float v[32];
+      const uint32_t col = kTS_S + part * 32;
+      umma::ld32(tm + lane_base + col, v);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float v[32];
-        const uint32_t col = kTS_S + half * 64 + cc * 32;
-        umma::ld32(tm + lane_base + col, v);
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint4 pk;
-          pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
-          pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
-          pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
-          pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
-          const int dk = half * 64 + cc * 32 + q8 * 8;
-          *reinterpret_cast<uint4*>(S0b + umma::tile_off(row, dk * 2, 256)) = pk;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= decay;
-        umma::st32(tm + lane_base + col, v);
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint4 pk;
+        pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
+        pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
+        pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
+        pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
+        const int dk = part * 32 + q8 * 8;
+        *reinterpret_cast<uint4*>(S0b + umma::tile_off(row, dk * 2, 256)) = pk;
       }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= decay;
+      umma::st32(tm + lane_base + col, v);
     }
     sync_for_mma();
     // ---- X = S0 Kg^T and Z = S0 Q^T (bf16)
@@ -470,30 +482,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // ---- A (for the inverse) and P from K K^T and Q K^T
     if (!wait_mma(&bars[0], par)) { ok = false; break; }
     {
-      float v[32];
-      umma::ld32(tm + lane_base + kT_D1 + half * 32, v);
+      float v[16];
+      umma::ld16(tm + lane_base + kT_D1 + part * 16, v);
       if (row < 64) {
         const int r = row;
         const float br = bv[r], gr = gv[r], ikr = ikv[r];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
+        for (int e4 = 0; e4 < 4; ++e4) {
           float a4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int i = half * 32 + e4 * 4 + e;
+            const int i = part * 16 + e4 * 4 + e;
             a4[e] = i < r ? br * ex2(gr - gv[i]) * v[e4 * 4 + e] * ikr * ikv[i] : 0.f;
           }
-          *reinterpret_cast<float4*>(AM + r * kLd + half * 32 + e4 * 4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+          *reinterpret_cast<float4*>(AM + r * kLd + part * 16 + e4 * 4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
       } else {
         const int r = row - 64;
         const float gr = gv[r], iqr = iqv[r];
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
+        for (int q8 = 0; q8 < 2; ++q8) {
           float pe[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int i = half * 32 + q8 * 8 + e;
+            const int i = part * 16 + q8 * 8 + e;
             pe[e] = i <= r ? ex2(gr - gv[i]) * v[q8 * 8 + e] * iqr * ikv[i] : 0.f;
           }
           uint4 pk;
@@ -501,17 +513,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           pk.y = pack_bf16(pe[2], pe[3]);
           pk.z = pack_bf16(pe[4], pe[5]);
           pk.w = pack_bf16(pe[6], pe[7]);
-          *reinterpret_cast<uint4*>(PBb + umma::tile_off(r, (half * 32 + q8 * 8) * 2, 128)) = pk;
+          *reinterpret_cast<uint4*>(PBb + umma::tile_off(r, (part * 16 + q8 * 8) * 2, 128)) = pk;
         }
       }
     }
     __syncthreads();
-    // ---- T = (I + A)^-1, blocked by 16 (T row-major in TS, rows of kLd floats).
-    // Diagonal blocks by forward substitution (one column per thread); then the
-    // off-diagonal blocks one block diagonal at a time, T_ab = -T_aa M with
-    // M = sum_{b<=c<a} A_ac T_cb, each thread producing 4 adjacent columns from
-    // 16-byte shared-memory loads. The strictly upper blocks are never written:
-    // the Tb pass below masks them.
+    // ---- T = (I + A)^-1 by recursive doubling over 16-row blocks (T row-major
+    // in TS, rows of kLd floats), with T diag(beta) written as the tf32 K-major
+    // operand as each block is finished:
+    //   diagonal blocks T_aa by forward substitution (one column per thread);
+    //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
+    //   then the lower-left 32x32 block = -T_hi (A_lo-left T_lo), T_hi and T_lo
+    //   being the two 32x32 diagonal blocks.
+    // Each thread of a product produces 4 adjacent columns from 16-byte loads.
+    auto put_tb4 = [&](int r, int c0, float4 t4) {  // T[r][c0..c0+3] -> Tb
+      const float4 f = make_float4(to_tf32(t4.x * bv[c0]), to_tf32(t4.y * bv[c0 + 1]), to_tf32(t4.z * bv[c0 + 2]),
+                                   to_tf32(t4.w * bv[c0 + 3]));
+      *reinterpret_cast<float4*>(TBb + umma::tile_off(r, c0 * 4, 256)) = f;
+    };
+    // acc += X[r][i0 .. i1) Y[i0 .. i1)[c4 .. c4+3]
+    auto rowblock = [](float4& acc, const float* xr, const float* yc, int ldy, int i0, int i1) {
+#pragma unroll 2
+      for (int i = i0; i < i1; i += 4) {
+        const float4 xv = *reinterpret_cast<const float4*>(xr + i);
+        const float xe[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 yv = *reinterpret_cast<const float4*>(yc + (i + e) * ldy);
+          acc.x = fmaf(xe[e], yv.x, acc.x);
+          acc.y = fmaf(xe[e], yv.y, acc.y);
+          acc.z = fmaf(xe[e], yv.z, acc.z);
+          acc.w = fmaf(xe[e], yv.w, acc.w);
+        }
+      }
+    };
     if (tid < kC) {
       const int a = tid >> 4, cc = tid & 15;
       const float* Ab = AM + (16 * a) * kLd + 16 * a;
@@ -523,88 +558,73 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         for (int i = 0; i < r; ++i) s = fmaf(Ab[r * kLd + i], x[i], s);
         x[r] = r < cc ? 0.f : (r == cc ? 1.f : -s);
       }
+      const int col = 16 * a + cc;
+      const float bc = bv[col];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) TS[(16 * a + r) * kLd + 16 * a + cc] = x[r];
+      for (int r = 0; r < 16; ++r) {
+        TS[(16 * a + r) * kLd + col] = x[r];
+        *reinterpret_cast<float*>(TBb + umma::tile_off(16 * a + r, col * 4, 256)) = to_tf32(x[r] * bc);
+      }
     }
     __syncthreads();
-#pragma unroll 1
-    for (int dist = 1; dist < 4; ++dist) {
-      const int nblk = 4 - dist;  // blocks (a, a - dist) for a = dist .. 3
-      const bool act = tid < nblk * 64;
-      const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = tid & 3;
-      const int a = dist + blk, b = a - dist;
-      if (act) {
+    {  // 16 -> 32: blocks (1,0) and (3,2); threads 0-127
+      const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+      const int a = 1 + 2 * blk, b = a - 1;
+      if (tid < 128) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* ar = AM + (16 * a + r) * kLd;
-        const float* tc0 = TS + 16 * b + 4 * c4;
-#pragma unroll 2
-        for (int i0 = 16 * b; i0 < 16 * a; i0 += 4) {
-          const float4 av = *reinterpret_cast<const float4*>(ar + i0);
-          const float ae[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 tv = *reinterpret_cast<const float4*>(tc0 + (i0 + e) * kLd);
-            acc.x = fmaf(ae[e], tv.x, acc.x);
-            acc.y = fmaf(ae[e], tv.y, acc.y);
-            acc.z = fmaf(ae[e], tv.z, acc.z);
-            acc.w = fmaf(ae[e], tv.w, acc.w);
-          }
-        }
-        *reinterpret_cast<float4*>(MS + blk * kMsBlk + r * kMsLd + 4 * c4) = acc;
+        rowblock(acc, AM + (16 * a + r) * kLd, TS + 16 * b + c4, kLd, 16 * b, 16 * a);
+        *reinterpret_cast<float4*>(MS + (16 * blk + r) * kMsLd + c4) = acc;
       }
       __syncthreads();
-      if (act) {
+      if (tid < 128) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* tr = TS + (16 * a + r) * kLd + 16 * a;
-        const float* mc = MS + blk * kMsBlk + 4 * c4;
-#pragma unroll
-        for (int i0 = 0; i0 < 16; i0 += 4) {
-          const float4 tv4 = *reinterpret_cast<const float4*>(tr + i0);
-          const float te[4] = {tv4.x, tv4.y, tv4.z, tv4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 mv = *reinterpret_cast<const float4*>(mc + (i0 + e) * kMsLd);
-            acc.x = fmaf(te[e], mv.x, acc.x);
-            acc.y = fmaf(te[e], mv.y, acc.y);
-            acc.z = fmaf(te[e], mv.z, acc.z);
-            acc.w = fmaf(te[e], mv.w, acc.w);
-          }
-        }
-        *reinterpret_cast<float4*>(TS + (16 * a + r) * kLd + 16 * b + 4 * c4) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        rowblock(acc, TS + (16 * a + r) * kLd + 16 * a, MS + 16 * blk * kMsLd + c4, kMsLd, 0, 16);
+        const float4 t4 = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        *reinterpret_cast<float4*>(TS + (16 * a + r) * kLd + 16 * b + c4) = t4;
+        put_tb4(16 * a + r, 16 * b + c4, t4);
       }
       __syncthreads();
     }
-    // ---- Tb = T diag(beta) as a tf32 K-major operand: rows r, 16-byte chunks of 4 columns
-    for (int it = tid; it < kC * 16; it += kThreads) {
-      const int r = it >> 4, ck = it & 15;
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      if ((ck >> 2) <= (r >> 4)) {  // on or below the block diagonal
-        const float4 t4 = *reinterpret_cast<const float4*>(TS + r * kLd + 4 * ck);
-        f.x = to_tf32(t4.x * bv[4 * ck + 0]);
-        f.y = to_tf32(t4.y * bv[4 * ck + 1]);
-        f.z = to_tf32(t4.z * bv[4 * ck + 2]);
-        f.w = to_tf32(t4.w * bv[4 * ck + 3]);
+    {  // 32 -> 64: rows 32-63, columns 0-31; threads 0-255 (row r, columns c4 .. c4+3)
+      const int r = (tid >> 3) & 31, c4 = 4 * (tid & 7);
+      if (tid < 256) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // M = A[32 + r][0..32) T[0..32)[c4..]: T_lo is zero above its block diagonal
+        rowblock(acc, AM + (32 + r) * kLd, TS + c4, kLd, c4 < 16 ? 0 : 16, 32);
+        *reinterpret_cast<float4*>(MS + r * kMsLd + c4) = acc;
       }
-      *reinterpret_cast<float4*>(TBb + umma::tile_off(r, ck * 16, 256)) = f;
+      __syncthreads();
+      if (tid < 256) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // -T_hi[r][0..32) M[0..32)[c4..]: T_hi is zero above its block diagonal
+        rowblock(acc, TS + (32 + r) * kLd + 32, MS + c4, kMsLd, 0, r < 16 ? 16 : 32);
+        const float4 t4 = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        put_tb4(32 + r, c4, t4);
+      }
     }
     // ---- Y = V^T - X (tf32, rows dv), over S0's now-free space
     if (!wait_mma(&bars[1], par)) { ok = false; break; }
     // the scratch area is free again (A and T consumed): raw rows of the next chunk
-    if (tid == 0 && c + 1 < nchunks) issue_x(tc + kC);
+    if (tid == 0 && c + 1 < nchunks) {
+      issue_x(tc + kC);
+      if (want_gate) {
+        bulk_wait_read_all();  // the Ogate store of the previous chunk has read that buffer
+        issue_z(tc + kC, (c + 1) & 1);
+      }
+    }
     {
-      float v[32], vv[32];
-      umma::ld32(tm + lane_base + kT_X + half * 32, v);
-      umma::ld32(tm + lane_base + kT_V + half * 32, vv);
+      float v[16], vv[16];
+      umma::ld16(tm + lane_base + kT_X + part * 16, v);
+      umma::ld16(tm + lane_base + kT_V + part * 16, vv);
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
+      for (int q4 = 0; q4 < 4; ++q4) {
         float y4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int t = half * 32 + q4 * 4 + e;
+          const int t = part * 16 + q4 * 4 + e;
           y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * ikv[t]);
         }
-        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (half * 32 + q4 * 4) * 4, 256)) =
+        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (part * 16 + q4 * 4) * 4, 256)) =
             make_float4(y4[0], y4[1], y4[2], y4[3]);
       }
     }
@@ -620,26 +640,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (!wait_mma(&bars[2], par)) { ok = false; break; }
     // ---- E as bf16 (A of O' = E^T P^T) and E' = E diag(Gamma_C / |k|) as tf32 (A of the update)
     {
-      float v[32];
-      umma::ld32(tm + lane_base + kT_E + half * 32, v);
+      float v[16];
+      umma::ld16(tm + lane_base + kT_E + part * 16, v);
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
+      for (int q8 = 0; q8 < 2; ++q8) {
         uint4 pk;
         pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
         pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
         pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
         pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(KGb + umma::tile_off(row, (half * 32 + q8 * 8) * 2, 128)) = pk;
+        *reinterpret_cast<uint4*>(KGb + umma::tile_off(row, (part * 16 + q8 * 8) * 2, 128)) = pk;
       }
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
+      for (int q4 = 0; q4 < 4; ++q4) {
         float e4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int t = half * 32 + q4 * 4 + e;
+          const int t = part * 16 + q4 * 4 + e;
           e4[e] = to_tf32(v[q4 * 4 + e] * glv[t] * ikv[t]);
         }
-        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (half * 32 + q4 * 4) * 4, 256)) =
+        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (part * 16 + q4 * 4) * 4, 256)) =
             make_float4(e4[0], e4[1], e4[2], e4[3]);
       }
     }
@@ -658,45 +678,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     }
     if (!wait_mma(&bars[3], par)) { ok = false; break; }
     // ---- o = (e^g Z / |q| + O') / sqrt(dk), then the gated RMSNorm over dv
-    float ov[32];
+    float ov[16];
     {
-      float z[32];
-      umma::ld32(tm + lane_base + kT_Z + half * 32, z);
-      umma::ld32(tm + lane_base + kT_O + half * 32, ov);
+      float z[16];
+      umma::ld16(tm + lane_base + kT_Z + part * 16, z);
+      umma::ld16(tm + lane_base + kT_O + part * 16, ov);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = half * 32 + e;
+      for (int e = 0; e < 16; ++e) {
+        const int t = part * 16 + e;
         ov[e] = fmaf(egv[t] * iqv[t], z[e], ov[e]) * kInvSqrtDk;
       }
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
+      for (int q8 = 0; q8 < 2; ++q8) {
         float sq[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) sq[e] = ov[q8 * 8 + e] * ov[q8 * 8 + e];
         const float tot = reduce8(sq, lane);
-        if ((lane & 3) == 0) rpart[quarter * 64 + half * 32 + q8 * 8 + tok8(lane)] = tot;
+        if ((lane & 3) == 0) rpart[quarter * 64 + part * 16 + q8 * 8 + tok8(lane)] = tot;
       }
     }
     __syncthreads();
     if (tid < kC)
       rinv[tid] = rsqrtf(((rpart[tid] + rpart[64 + tid]) + (rpart[128 + tid] + rpart[192 + tid])) *
                              (1.0f / kHeadDim) + p.eps);
-    if (want_gate && !wait_mma(&bars[5], par)) { ok = false; break; }  // z rows landed (also syncs)
+    if (want_gate && !wait_mma(&bars[5 + (c & 1)], (c >> 1) & 1)) { ok = false; break; }  // z rows landed (also syncs)
     if (!want_gate) __syncthreads();
     {
       if (p.o) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = half * 32 + e;
+        for (int e = 0; e < 16; ++e) {
+          const int t = part * 16 + e;
           if (t < L) p.o[((size_t)(tc + t) * p.Hv + h) * kHeadDim + row] = f32_to_bf16(ov[e]);
         }
       }
       if (want_gate) {
-        // Ogate over the z rows in place (thread: column `row` of 32 token rows) ...
+        // Ogate over the z rows in place (thread: column `row` of 16 token rows) ...
         const float gm = p.gamma[row];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = half * 32 + e;
+        for (int e = 0; e < 16; ++e) {
+          const int t = part * 16 + e;
           uint16_t* zp = ZS + t * kHeadDim + row;
           *zp = f32_to_bf16(ov[e] * rinv[t] * gm * silu_ftz(bf16_to_f32(*zp)));
         }
@@ -720,27 +740,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 
   if (ok) {
     // ---- final state back to the slot, history to the owners' channels
-    float* dst = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + half * 64;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
+    float* dst = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + part * 32;
+    {
       float v[32];
-      umma::ld32(tm + lane_base + kTS_S + half * 64 + cc * 32, v);
+      umma::ld32(tm + lane_base + kTS_S + part * 32, v);
 #pragma unroll
       for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(dst + cc * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
-    if (g == 0) {  // q and k history: the group's first CTA
-      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc_a) * 3;
-      hp[0] = ha[0]; hp[1] = ha[1]; hp[2] = ha[2];
-    }
-    if (qv) {  // v history: the head's own CTA
-      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gc_v) * 3;
-      hp[0] = hv[0]; hp[1] = hv[1]; hp[2] = hv[2];
+    // history: q and k channels by the group's first CTA, v channels by the head's own
+    if (cset < 3 && (cset == 2 || g == 0)) {
+      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gown) * 3;
+      hp[0] = hw[0]; hp[1] = hw[1]; hp[2] = hw[2];
     }
   } else {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
     // give MMAs still in flight a second bounded chance before the memory is freed
-    for (int b = 0; b < 6; ++b) mbar_wait_bounded(&bars[b], 0);
+    for (int b = 0; b < 7; ++b) mbar_wait_bounded(&bars[b], 0);
   }
   if (tid == 0) bulk_wait_all();  // Ogate rows stored
   umma::fence_before_sync();
