@@ -134,13 +134,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return d;
 }
 
-// SiLU(x) = x / (1 + e^-x) with e^-x = 2^(-x log2 e), on the flush-to-zero
-// ex2 and reciprocal approximations. Large negative x gives -0.
+// SiLU(x) = x sigmoid(x) = x/2 (1 + tanh(x/2)), on the hardware tanh
+// approximation (one special-function op; its relative error, about 2^-11,
+// bounds the absolute error by |x| 2^-12).
 __device__ __forceinline__ float silu_ftz(float x) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
-  return x * r;
+  const float hx = 0.5f * x;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hx));
+  return fmaf(hx, t, hx);
 }
 
 // Waits for an MMA-completion phase; the verdict is uniform over the CTA.

@@ -49,6 +49,7 @@ def check_out(got, ref, what: str):
     e = rel_l2(got, ref)
     m = float(np.max(np.abs(got - ref))) if ref.size else 0.0
     bound = OUT_MAX_ABS_FRAC * float(np.max(np.abs(ref))) if ref.size else 0.0
+    print(f"[parity] {what}: rel-L2 {e:.3e}, max-abs {m:.3e} (bound {bound:.3e})")
     assert e <= OUT_REL_L2, f"{what}: rel-L2 {e:.3e} > {OUT_REL_L2}"
     assert m <= bound, f"{what}: max-abs {m:.3e} > {bound:.3e}"
     return e, m
@@ -56,6 +57,7 @@ def check_out(got, ref, what: str):
 
 def check_state(got, ref, tol: float, what: str):
     e = rel_l2(got, ref)
+    print(f"[parity] {what}: state rel-L2 {e:.3e} (tolerance {tol})")
     assert np.all(np.isfinite(got)), f"{what}: non-finite state"
     assert e <= tol, f"{what}: state rel-L2 {e:.3e} > {tol}"
     return e
