@@ -119,7 +119,8 @@ gdn_status gdn_conv_update(const gdn_dims* d, const uint16_t* x, const float* co
   if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
   if (!conv_w || !conv_hist || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
   if (num_tokens > 0 && (!x || !y)) return GDN_ERR_INVALID_ARG;
-  if (!aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(conv_w, 16) || !aligned(conv_hist, 4)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!aligned(x, 8) || !aligned(y, 8))) return GDN_ERR_INVALID_ARG;
   ConvArgs a{x, conv_w, conv_hist, qsl, slot_idx, has_init, y, dev_err, channels(d), d->num_slots, num_seqs,
              num_tokens};
   return from_cuda(launch_conv(a, static_cast<cudaStream_t>(stream)));

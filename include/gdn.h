@@ -109,6 +109,8 @@ typedef enum gdn_status {
  *   has_init        [num_seqs] uint8 or NULL (= all 1); 0 starts from a zero
  *                   history without reading the slot
  *   y               [T][CH] bf16 out: SiLU(conv)
+ * x and y must be 8-byte aligned, conv_hist 4-byte and conv_w 16-byte aligned
+ * (GDN_ERR_INVALID_ARG otherwise).
  */
 gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *x, const float *conv_w,
                            uint16_t *conv_hist, const int32_t *query_start_loc,

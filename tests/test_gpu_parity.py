@@ -28,7 +28,7 @@ def _dev_err():
 
 # ---------------------------------------------------------------- standalone pieces
 
-@pytest.mark.parametrize("lengths", [[64], [1, 2, 3, 70, 0, 129]])
+@pytest.mark.parametrize("lengths", [[64], [1, 2, 3, 70, 0, 129], [1] * 40, [513, 2, 64, 65, 190, 4]])
 def test_conv_update_matches_oracle(b, lengths):
     dims = synth.FULL_HEADS
     w = synth.prefill_workload(dims, lengths, seed=31)
