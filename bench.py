@@ -362,10 +362,12 @@ def measure_prefill(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
     og = torch.empty((T, geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     D = b.make_dims(geom, Rs)
+    ws = torch.empty(b.gdn_prefill_workspace_bytes(D, N, T), dtype=torch.uint8, device=dev)
 
     def run():
         b.gdn_chunk_prefill(D, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], qsl, slots, w["alpha"],
-                            w["beta"], w["z"], w["gamma"], 1e-6, ogate=og, has_init=hi, dev_err=err, stream=stream)
+                            w["beta"], w["z"], w["gamma"], 1e-6, ogate=og, has_init=hi, workspace=ws, dev_err=err,
+                            stream=stream)
 
     ms = timed(run, steps, warmup, stream)
     if b.gdn_read_device_error(err) != 0:
@@ -409,6 +411,7 @@ def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
     pog = torch.empty((int(lengths.sum()), geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     D, Dp = b.make_dims(geom, Rs), b.make_dims(geom, 16)
+    pws = torch.empty(b.gdn_prefill_workspace_bytes(Dp, 8, int(lengths.sum())), dtype=torch.uint8, device=dev)
 
     def spec_only():
         b.gdn_spec_verify(D, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], slots, spec, w["alpha"],
@@ -419,8 +422,8 @@ def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
     def mixed():
         spec_only()
         b.gdn_chunk_prefill(Dp, wp["qkv0"], wp["conv_w"], wp["conv_hist"], wp["state"], pqsl, pslots,
-                            wp["alpha"], wp["beta"], wp["z"], wp["gamma"], 1e-6, ogate=pog, dev_err=err,
-                            stream=stream)
+                            wp["alpha"], wp["beta"], wp["z"], wp["gamma"], 1e-6, ogate=pog, workspace=pws,
+                            dev_err=err, stream=stream)
 
     ms_spec = timed(spec_only, steps, warmup, stream)
     ms_mixed = timed(mixed, steps, warmup, stream)

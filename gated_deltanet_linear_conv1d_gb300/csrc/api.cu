@@ -76,10 +76,9 @@ size_t gdn_conv_hist_bytes(const gdn_dims* d) {
 }
 
 size_t gdn_prefill_workspace_bytes(const gdn_dims* d, int32_t num_seqs, int32_t num_tokens) {
-  (void)d;
-  (void)num_seqs;
   (void)num_tokens;
-  return 0;
+  if (check_dims(d) != GDN_OK || num_seqs <= 0) return 0;
+  return ((size_t)num_seqs * sizeof(int32_t) + 255) / 256 * 256;  // the schedule: requests, longest first
 }
 
 const char* gdn_status_string(gdn_status s) {
@@ -209,7 +208,7 @@ gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const floa
     return GDN_ERR_INVALID_ARG;
   PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
                 dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
-                d->num_slots, num_seqs, num_tokens};
+                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace)};
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

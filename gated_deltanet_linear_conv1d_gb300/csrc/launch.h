@@ -65,6 +65,7 @@ struct PrefillArgs {
   uint16_t* ogate;            // or nullptr
   int32_t* dev_err;
   int Hk, Hv, G, CH, Rs, N, T;
+  int32_t* order;             // [N] scratch: requests, longest first (filled by launch_prefill), or nullptr
 };
 
 struct NormArgs {

@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
                                                                   const __grid_constant__ CUtensorMap tmz,
                                                                   const __grid_constant__ CUtensorMap tmo) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int h = blockIdx.x, n = blockIdx.y;
+  const int h = blockIdx.x, n = p.order ? p.order[blockIdx.y] : blockIdx.y;
   const int g = h % p.G, j = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // warp w reads tensor-memory lanes 32 (w % 4) ..; the four warps of a lane
@@ -823,6 +823,53 @@ bool encode_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Writes the request indices into order[] longest first (by 64-token chunk
+// count, capped at kOrderBuckets - 1; ties in any order), so that the prefill's
+// CTAs, dispatched in blockIdx order, start the longest (request, head) chains
+// first and the short ones fill in behind them. One CTA: a counting sort.
+constexpr int kOrderThreads = 1024, kOrderBuckets = 2 * kOrderThreads;
+
+__global__ void __launch_bounds__(kOrderThreads) prefill_order_kernel(const int32_t* qsl, int N, int32_t* order) {
+  __shared__ int cnt[kOrderBuckets];
+  __shared__ int wsum[kOrderThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto key = [&](int n) {
+    const int len = qsl[n + 1] - qsl[n];
+    return len <= 0 ? 0 : min((len + kC - 1) / kC, kOrderBuckets - 1);
+  };
+  for (int b = tid; b < kOrderBuckets; b += kOrderThreads) cnt[b] = 0;
+  __syncthreads();
+  for (int n = tid; n < N; n += kOrderThreads) atomicAdd(&cnt[key(n)], 1);
+  __syncthreads();
+  // first position of each bucket in descending key order: thread t owns the
+  // buckets at descending positions 2t and 2t + 1
+  const int b0 = kOrderBuckets - 1 - 2 * tid, b1 = b0 - 1;
+  const int c0 = cnt[b0], c1 = cnt[b1];
+  int incl = c0 + c1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
+    }
+    wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - (c0 + c1) + (warp > 0 ? wsum[warp - 1] : 0);
+  cnt[b0] = excl;
+  cnt[b1] = excl + c0;
+  __syncthreads();
+  for (int n = tid; n < N; n += kOrderThreads) order[atomicAdd(&cnt[key(n)], 1)] = n;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
@@ -842,6 +889,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   }
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(&prefill_tc_kernel), kSmemBytes);
   if (err != cudaSuccess) return err;
+  if (a.order) {
+    prefill_order_kernel<<<1, kOrderThreads, 0, stream>>>(a.qsl, a.N, a.order);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hv, a.N, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

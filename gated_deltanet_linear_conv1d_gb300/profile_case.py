@@ -75,6 +75,7 @@ def main(argv=None):
         T = int(np.sum(lengths))
         og = torch.empty((T, geom.num_v_heads * 128), dtype=torch.bfloat16, device=dev)
         y = torch.empty((T, geom.channels), dtype=torch.bfloat16, device=dev) if args.case == "conv" else None
+        ws = torch.empty(b.gdn_prefill_workspace_bytes(D, len(lengths), T), dtype=torch.uint8, device=dev)
 
         def run():
             if args.case == "conv":
@@ -83,7 +84,7 @@ def main(argv=None):
             else:
                 b.gdn_chunk_prefill(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["query_start_loc"],
                                     d["slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og,
-                                    has_init=d["has_init"], dev_err=err)
+                                    has_init=d["has_init"], workspace=ws, dev_err=err)
     elif args.case == "spec":
         w = synth.spec_workload(geom, args.requests, num_pos=4, seed=4)
         d = _dev(w, dev)

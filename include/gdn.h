@@ -154,9 +154,11 @@ gdn_status gdn_decode_step(const gdn_dims *dims, const uint16_t *qkv0, const flo
  *             NULL);  gamma [dv];  eps
  *   o [T][Hv][dv] bf16 or NULL;  ogate [T][Hv*dv] bf16 or NULL (not both NULL)
  *   workspace, workspace_bytes: device scratch of at least
- *             gdn_prefill_workspace_bytes(dims, N, T) bytes, 256-byte aligned
- *             (may be NULL when that size is 0). Contents need not be zeroed
- *             and are clobbered.
+ *             gdn_prefill_workspace_bytes(dims, N, T) bytes, 256-byte aligned.
+ *             Contents need not be zeroed and are clobbered: the call writes
+ *             there the order in which the (request, head) chains are started,
+ *             longest request first. Two calls in flight at once need two
+ *             workspaces.
  */
 gdn_status gdn_chunk_prefill(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
                              uint16_t *conv_hist, float *state, const int32_t *query_start_loc,
@@ -225,7 +227,8 @@ size_t gdn_state_bytes(const gdn_dims *dims);
 /* Bytes of one slot of the bf16 conv-history pool: CH*(K-1)*2. 0 for invalid dims. */
 size_t gdn_conv_hist_bytes(const gdn_dims *dims);
 
-/* Device scratch gdn_chunk_prefill needs for N requests and T packed tokens. */
+/* Device scratch gdn_chunk_prefill needs for N requests and T packed tokens:
+ * N int32 rounded up to 256 bytes (0 for invalid dims or N <= 0). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t num_seqs, int32_t num_tokens);
 
 /* Static, human-readable name of a status code. */

@@ -37,6 +37,15 @@ def test_size_queries_match_the_page(b):
     assert b.gdn_state_bytes(b.GdnDims(0, 0, 0, 0, 0, 0)) == 0
 
 
+def test_prefill_workspace_holds_one_int_per_request(b):
+    d = b.make_dims(synth.FULL_HEADS, 512)
+    assert b.gdn_prefill_workspace_bytes(d, 64, 71068) == 256
+    assert b.gdn_prefill_workspace_bytes(d, 65, 100) == 512
+    assert b.gdn_prefill_workspace_bytes(d, 1000, 1000) == 4096
+    assert b.gdn_prefill_workspace_bytes(d, 0, 0) == 0
+    assert b.gdn_prefill_workspace_bytes(b.GdnDims(0, 0, 0, 0, 0, 0), 64, 64) == 0
+
+
 def test_status_strings(b):
     for s in range(6):
         assert b._lib.gdn_status_string(s).decode().startswith("GDN_")
