@@ -212,6 +212,34 @@ gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const floa
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w,
+                                     uint16_t* conv_hist, float* state, const int32_t* qsl,
+                                     const int32_t* slot_idx, const uint8_t* has_init, const float* alpha,
+                                     const float* beta, const uint16_t* z, const float* gamma, float eps,
+                                     uint16_t* o, uint16_t* ogate, int32_t num_seqs, int32_t num_tokens,
+                                     int32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
+  if (num_seqs > gdn::kStaticPrefillMaxSeqs) return GDN_ERR_INVALID_ARG;  // beyond the fixed schedule array
+  if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!qkv0 || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+  if (!o && !ogate) return GDN_ERR_INVALID_ARG;
+  if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && !aligned(qkv0, 16)) return GDN_ERR_INVALID_ARG;
+  if ((o && !aligned(o, 8)) || (ogate && (!aligned(ogate, 16) || !aligned(z, 16) || !aligned(gamma, 16))))
+    return GDN_ERR_INVALID_ARG;
+  int32_t* order = nullptr;
+  if (gdn::static_prefill_order(&order) != cudaSuccess) return GDN_ERR_CUDA;
+  PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
+                dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
+                d->num_slots, num_seqs, num_tokens, order};
+  return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
 gdn_status gdn_gated_rmsnorm(const uint16_t* o, const uint16_t* z, const float* gamma, float eps, uint16_t* out,
                              int32_t num_tokens, int32_t num_heads, int32_t head_dim, void* stream) {
   if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0) return GDN_ERR_INVALID_ARG;

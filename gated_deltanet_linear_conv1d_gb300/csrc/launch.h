@@ -89,6 +89,13 @@ cudaError_t launch_stream(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// Largest request count the allocation-free prefill accepts: the size of its
+// file-scope schedule array (one int32 per request, 256 KiB).
+constexpr int kStaticPrefillMaxSeqs = 65536;
+// Device address of that array on the current device, looked up once per
+// device with cudaGetSymbolAddress and cached.
+cudaError_t static_prefill_order(int32_t** out);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream);
 
 }  // namespace gdn

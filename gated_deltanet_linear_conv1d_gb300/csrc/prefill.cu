@@ -872,6 +872,33 @@ __global__ void __launch_bounds__(kOrderThreads) prefill_order_kernel(const int3
 
 }  // namespace
 
+// Schedule scratch of gdn_chunk_prefill_noalloc, for callers that cannot hand
+// the library a workspace because they cannot allocate device memory at the
+// call site (a host whose device memory is all reserved up front by its own
+// pool, with no allocation hook). Fixed size, one per device; it needs no
+// clearing (the order kernel writes all N entries before the prefill reads
+// them), and two such calls in flight at once on one device race on it.
+static __device__ __align__(256) int32_t g_static_prefill_order[kStaticPrefillMaxSeqs];
+
+cudaError_t static_prefill_order(int32_t** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int32_t* cache[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    err = cudaGetSymbolAddress(&ptr, g_static_prefill_order);
+    if (err != cudaSuccess) return err;
+    cache[dev] = static_cast<int32_t*>(ptr);
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   CUtensorMap tmx{}, tmz{}, tmo{};
   {

@@ -169,6 +169,32 @@ gdn_status gdn_chunk_prefill(const gdn_dims *dims, const uint16_t *qkv0, const f
                              void *stream);
 
 /*
+ * gdn_chunk_prefill_noalloc - gdn_chunk_prefill without a workspace argument,
+ * for callers that cannot allocate device memory at the call site (a host
+ * whose device memory is all reserved up front by its own pool, with no
+ * allocation hook). It has no counterpart in the pages: it is an interface
+ * convenience of this library, and computes exactly what gdn_chunk_prefill
+ * computes.
+ *
+ * Its schedule scratch is a fixed file-scope device array of 65536 int32
+ * (256 KiB) per device: num_seqs above that is rejected with
+ * GDN_ERR_INVALID_ARG. The library allocates nothing; the first call on each
+ * device looks up the array's address (cudaGetSymbolAddress) and caches it, so
+ * make that first call before any stream capture. The scratch needs no
+ * clearing. Calls that overlap in time on one device (two streams, or two
+ * threads) race on the one array: serialise them.
+ *
+ * Arguments, layouts, errors: as gdn_chunk_prefill, without workspace and
+ * workspace_bytes.
+ */
+gdn_status gdn_chunk_prefill_noalloc(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
+                                     uint16_t *conv_hist, float *state, const int32_t *query_start_loc,
+                                     const int32_t *slot_idx, const uint8_t *has_init, const float *alpha,
+                                     const float *beta, const uint16_t *z, const float *gamma, float eps,
+                                     uint16_t *o, uint16_t *ogate, int32_t num_seqs, int32_t num_tokens,
+                                     int32_t *dev_err, void *stream);
+
+/*
  * gdn_spec_verify - speculative verify: P = num_pos positions per request (the
  * last sampled token and P-1 drafts, verified in one forward) through the
  * whole mixer core, keeping the state and conv history after EVERY position p
