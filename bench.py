@@ -441,6 +441,68 @@ def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
             "mixed_ms": ms_mixed, "mixed_tokens_per_s": (N * P + int(lengths.sum())) / (ms_mixed / 1e3)}
 
 
+def measure_conv(b, dev, stream, steps: int = 10, warmup: int = 3) -> dict:
+    """Standalone varlen conv + SiLU with the history update, on the prefill batch's packing."""
+    import torch
+    geom = synth.FULL_HEADS
+    lengths = synth.loguniform_lengths(np.random.default_rng(3), 64, 16, 8192)
+    N, T = len(lengths), int(lengths.sum())
+    w = device_workload(geom, 2 * N, T, seed=3, dev=dev)
+    slots = torch.from_numpy(synth.slot_permutation(np.random.default_rng(3), N, 2 * N)).to(dev)
+    qsl = torch.from_numpy(synth.pack_offsets(lengths)).to(dev)
+    y = torch.empty((T, geom.channels), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    D = b.make_dims(geom, 2 * N)
+
+    def run():
+        b.gdn_conv_update(D, w["qkv0"], w["conv_w"], w["conv_hist"], qsl, slots, y, dev_err=err, stream=stream)
+
+    ms = timed(run, steps, warmup, stream)
+    if b.gdn_read_device_error(err) != 0:
+        raise RuntimeError("device error flagged during the conv measurement")
+    hist = geom.channels * (geom.conv_kernel - 1) * 2
+    nbytes = T * geom.channels * 4 + N * 2 * hist + geom.channels * geom.conv_kernel * 4
+    hbm_peak, hbm_kind = load_peaks()
+    return {"workload": f"{N} requests, log-uniform lengths in [16, 8192] (seed 3), {T} tokens, 10240 channels",
+            "kernel": "conv_kernel (gdn_conv_update)", "value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "hbm": {"achieved_gbs": nbytes / (ms / 1e3) / 1e9, "algorithmic_bytes": nbytes, "peak": hbm_peak,
+                    "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "peak_kind": hbm_kind}}
+
+
+def measure_out_proj(b, dev, stream) -> dict:
+    """Wo projection + residual add (6144 -> 5120, bf16, cuBLASLt) at the decode batch (weight-streaming:
+    four distinct weight matrices in rotation, 252 MB, so no step finds its weights in L2) and at the
+    prefill batch's token count (tensor-bound)."""
+    import torch
+    K, N = 6144, 5120
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device=dev)
+    weights = [(torch.randn((N, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16) for _ in range(4)]
+    res = {}
+    p_bf16, _, kind = load_bf16_peak()
+    hbm_peak, hbm_kind = load_peaks()
+    for name, T, steps in (("decode", NUM_REQ, 40), ("prefill", 71068, 5)):
+        a = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+        hidden = torch.randn((T, N), generator=g, device=dev).to(torch.bfloat16)
+        it = [0]
+
+        def run():
+            b.gdn_out_proj(a, weights[it[0] % 4], hidden, residual=hidden, workspace=ws, stream=stream)
+            it[0] += 1
+
+        ms = timed(run, steps, 4, stream)
+        flops = 2.0 * T * K * N
+        nbytes = N * K * 2 + T * K * 2 + 2 * T * N * 2
+        res[name] = {"tokens": T, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                     "tensor_frac": flops / (ms / 1e3) / 1e12 / p_bf16,
+                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+        del a, hidden
+    return {"workload": "out = Ogate Wo^T + residual, K=6144 -> N=5120, bf16 in/out, fp32 accumulation",
+            "kernel": "cuBLASLt (gdn_out_proj)", "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
+            "hbm_peak_gbs": hbm_peak, **res}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -552,6 +614,10 @@ def run_gpu(args):
         extra["prefill"] = measure_prefill(b, dev, stream)
         torch.cuda.empty_cache()
         extra["spec_mixed"] = measure_spec_mixed(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["conv"] = measure_conv(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["out_proj"] = measure_out_proj(b, dev, stream)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",

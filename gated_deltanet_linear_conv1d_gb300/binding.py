@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "gdn_spec_verify": [D, P, P, P, P, P, P, P, P, P, P, f32, P, P, i32, i32, P, P],
         "gdn_spec_commit": [D, P, P, P, P, P, i32, i32, i32, P, P],
         "gdn_gated_rmsnorm": [P, P, P, f32, P, i32, i32, i32, P],
+        "gdn_out_proj": [P, P, P, P, i32, i32, i32, P, sz, P],
         "gdn_read_device_error": [P, ctypes.POINTER(i32), i32, P],
     }
     for name, args in sigs.items():
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
         getattr(lib, name).restype = sz
     lib.gdn_prefill_workspace_bytes.argtypes = [D, i32, i32]
     lib.gdn_prefill_workspace_bytes.restype = sz
+    lib.gdn_out_proj_workspace_bytes.argtypes = []
+    lib.gdn_out_proj_workspace_bytes.restype = sz
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_status_string.restype = ctypes.c_char_p
     return lib
@@ -221,6 +224,23 @@ def gdn_chunk_prefill_noalloc(dims, qkv0, conv_w, conv_hist, state, query_start_
                                           _ptr(alpha), _ptr(beta), _ptr(z), _ptr(gamma), float(eps), _ptr(o),
                                           _ptr(ogate), N, T, _ptr(dev_err), _stream(stream)),
            "gdn_chunk_prefill_noalloc")
+
+
+def gdn_out_proj_workspace_bytes() -> int:
+    return int(_lib.gdn_out_proj_workspace_bytes())
+
+
+def gdn_out_proj(ogate, w, out, residual=None, workspace=None, stream=None):
+    """out[T][N] = ogate[T][K] w[N][K]^T (+ residual[T][N]); residual may be out itself."""
+    T, K = ogate.shape
+    N = w.shape[0]
+    _need(ogate, "ogate", torch.bfloat16, (T, K))
+    _need(w, "w", torch.bfloat16, (N, K))
+    _need(out, "out", torch.bfloat16, (T, N))
+    _need(residual, "residual", torch.bfloat16, (T, N), optional=True)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_out_proj(_ptr(ogate), _ptr(w), _ptr(residual), _ptr(out), T, K, N, _ptr(workspace), ws_bytes,
+                             _stream(stream)), "gdn_out_proj")
 
 
 def gdn_spec_verify(dims, qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma, eps,

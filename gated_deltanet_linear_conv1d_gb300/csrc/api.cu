@@ -240,6 +240,26 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t gdn_out_proj_workspace_bytes(void) { return (size_t)32 << 20; }
+
+gdn_status gdn_out_proj(const uint16_t* ogate, const uint16_t* w, const uint16_t* residual, uint16_t* out,
+                        int32_t num_tokens, int32_t in_features, int32_t out_features, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (num_tokens < 0 || in_features <= 0 || out_features <= 0) return GDN_ERR_INVALID_ARG;
+  if (in_features % 8 != 0 || out_features % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return GDN_OK;
+  if (!ogate || !w || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned(ogate, 16) || !aligned(w, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
+    return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return GDN_ERR_INVALID_ARG;
+  bool unsupported = false;
+  const cudaError_t e = launch_out_proj(ogate, w, residual, out, num_tokens, in_features, out_features,
+                                        workspace_bytes ? workspace : nullptr, workspace_bytes,
+                                        static_cast<cudaStream_t>(stream), &unsupported);
+  if (unsupported) return GDN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 gdn_status gdn_gated_rmsnorm(const uint16_t* o, const uint16_t* z, const float* gamma, float eps, uint16_t* out,
                              int32_t num_tokens, int32_t num_heads, int32_t head_dim, void* stream) {
   if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0) return GDN_ERR_INVALID_ARG;

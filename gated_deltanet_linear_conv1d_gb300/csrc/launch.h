@@ -96,6 +96,12 @@ constexpr int kStaticPrefillMaxSeqs = 65536;
 // Device address of that array on the current device, looked up once per
 // device with cudaGetSymbolAddress and cached.
 cudaError_t static_prefill_order(int32_t** out);
+
+// out[T][N] = ogate[T][K] w[N][K]^T (+ residual[T][N]) through cuBLASLt; sets
+// *unsupported when the library offers no algorithm for the shape.
+cudaError_t launch_out_proj(const uint16_t* ogate, const uint16_t* w, const uint16_t* residual, uint16_t* out,
+                            int T, int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                            bool* unsupported);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream);
 
 }  // namespace gdn

@@ -246,6 +246,32 @@ gdn_status gdn_gated_rmsnorm(const uint16_t *o, const uint16_t *z, const float *
                              uint16_t *out, int32_t num_tokens, int32_t num_heads,
                              int32_t head_dim, void *stream);
 
+/*
+ * gdn_out_proj - the output projection after the mixer core and the residual
+ * add: out = ogate W^T (+ residual), bf16 operands, fp32 accumulation, bf16
+ * out (round to nearest even). Page: section 01 GDN operator table, the Wo row
+ * ([T,6144] -> [T,5120]) and the residual stream around the mixer. The gated
+ * RMSNorm that the page puts before Wo is fused into the mixer entry points'
+ * ogate output, so this is a plain GEMM; it runs through cuBLASLt.
+ *
+ *   ogate     [T][K] bf16 (T = num_tokens, K = in_features)
+ *   w         [N][K] bf16, the nn.Linear weight layout (N = out_features)
+ *   residual  [T][N] bf16 or NULL; may equal out (in-place residual add)
+ *   out       [T][N] bf16
+ *   workspace device scratch of workspace_bytes (may be 0 / NULL; the
+ *             library's choice of algorithm can depend on it), 256-byte aligned;
+ *             gdn_out_proj_workspace_bytes() is the recommended size. Two
+ *             calls in flight at once need two workspaces.
+ * Pointers 16-byte aligned; K and N multiples of 8 (GDN_ERR_UNSUPPORTED
+ * otherwise, and when the library has no algorithm for the shape).
+ */
+gdn_status gdn_out_proj(const uint16_t *ogate, const uint16_t *w, const uint16_t *residual, uint16_t *out,
+                        int32_t num_tokens, int32_t in_features, int32_t out_features, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* Recommended workspace for gdn_out_proj: 32 MiB. */
+size_t gdn_out_proj_workspace_bytes(void);
+
 /* Bytes of one slot of the fp32 state pool: Hv*dv*dk*4 (3 MiB at 48x128x128,
  * the L00 table's "3 MiB per sequence per layer"). 0 for invalid dims. */
 size_t gdn_state_bytes(const gdn_dims *dims);

@@ -10,6 +10,9 @@ import this module. The GPU product path never does.
 * ``spec_commit`` applies the greedy accept rule of the "Qwen3.8 MTP" page,
   section 5 (accept / reject): a request keeps the state after its accepted
   position.
+* ``out_proj`` is the output projection after the mixer and the residual add
+  (first page, section 01 GDN operator table, the Wo row): a plain fp64 matrix
+  product of the bf16 inputs.
 * ``chunked_delta_rule`` is a separate fp64 numpy statement of the chunked
   (WY / UT) form of the same recurrence, used only to check the chunk algebra
   against the token-by-token form. The first page only says that the block
@@ -212,6 +215,24 @@ def spec_commit(state, conv_hist, slot_idx, spec_slot_idx, accepted, mode: str =
     else:
         raise ValueError(mode)
     return st, hist, slots
+
+
+def out_proj(ogate_bits, w_bits, residual_bits=None):
+    """out = ogate W^T (+ residual) in fp64 from bf16 bits; ogate [T, K], W [N, K]
+    (nn.Linear layout), residual [T, N]. The Wo row of the GDN operator table
+    maps [T,6144] to [T,5120]; the residual stream adds the layer input back."""
+    a = _bf16(ogate_bits)
+    w = _bf16(w_bits)
+    out = a @ w.T
+    if residual_bits is not None:
+        out = out + _bf16(residual_bits)
+    return out
+
+
+def _bf16(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) to fp64 values."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def chunked_delta_rule(q, k, v, alpha, beta, S0, chunk: int = 64):

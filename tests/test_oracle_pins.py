@@ -392,3 +392,31 @@ def test_empty_request_leaves_its_slot_untouched():
         _, h = oracle.conv_update(TINY, w["qkv0"], w["conv_w"], w["conv_hist"], qsl, slots,
                                   np.array([init, 1], np.uint8))
         np.testing.assert_array_equal(h[1], w["conv_hist"][1])
+
+
+# ---------------------------------------------------------------- output projection (Wo row)
+
+def _bits(x):
+    return synth.bf16_bits(np.asarray(x, np.float32))
+
+
+def test_out_proj_hand_example_and_residual():
+    """A 2x3 times (2x3)^T product written out by hand, then the residual add."""
+    a = np.array([[1.0, 2.0, -1.0], [0.5, 0.0, 4.0]])
+    w = np.array([[1.0, 0.0, 2.0], [-1.0, 3.0, 0.25]])  # [N=2][K=3]
+    expect = np.array([[1 + 0 - 2, -1 + 6 - 0.25], [0.5 + 0 + 8, -0.5 + 0 + 1]])
+    np.testing.assert_array_equal(oracle.out_proj(_bits(a), _bits(w)), expect)
+    r = np.array([[10.0, -2.0], [0.0, 1.5]])
+    np.testing.assert_array_equal(oracle.out_proj(_bits(a), _bits(w), _bits(r)), expect + r)
+
+
+def test_out_proj_one_hot_rows_select_input_columns():
+    """Row n of W a one-hot at k: output column n is input column k (W is [N][K], not [K][N])."""
+    rng = np.random.default_rng(71)
+    T, K, N = 5, 16, 8
+    a = rng.normal(size=(T, K))
+    cols = rng.permutation(K)[:N]
+    w = np.zeros((N, K))
+    w[np.arange(N), cols] = 1.0
+    got = oracle.out_proj(_bits(a), _bits(w))
+    np.testing.assert_array_equal(got, synth.bf16_to_f32(_bits(a)).astype(np.float64)[:, cols])
