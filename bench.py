@@ -373,6 +373,34 @@ def measure_prefill(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
     if b.gdn_read_device_error(err) != 0:
         raise RuntimeError("device error flagged during the prefill measurement")
     f_bf16, f_tf32 = prefill_flops(geom, lengths)
+    # align mode: the same batch with a state + history snapshot after every 512 tokens of each request
+    block = 512
+    nsnap = lengths // block
+    max_snaps = int(nsnap.max())
+    del w
+    torch.cuda.empty_cache()
+    Rs2 = Rs + int(nsnap.sum())
+    w2 = device_workload(geom, Rs2, T, seed=3, dev=dev)
+    D2 = b.make_dims(geom, Rs2)
+    snap = np.full((N, max(max_snaps, 1)), -1, np.int32)
+    nxt = Rs
+    for n in range(N):
+        for k in range(int(nsnap[n])):
+            snap[n, k] = nxt
+            nxt += 1
+    snap_d = torch.from_numpy(snap).to(dev)
+
+    def run_align():
+        b.gdn_chunk_prefill_align(D2, w2["qkv0"], w2["conv_w"], w2["conv_hist"], w2["state"], qsl, slots,
+                                  w2["alpha"], w2["beta"], w2["z"], w2["gamma"], 1e-6, block, snap_slot=snap_d,
+                                  ogate=og, has_init=hi, workspace=ws, dev_err=err, stream=stream)
+
+    ms_align = timed(run_align, steps, warmup, stream)
+    if b.gdn_read_device_error(err) != 0:
+        raise RuntimeError("device error flagged during the align-mode prefill measurement")
+    snap_bytes = int(nsnap.sum()) * geom.num_v_heads * geom.head_v_dim * geom.head_k_dim * 4
+    del w2
+    torch.cuda.empty_cache()
     p_bf16, _, kind = load_bf16_peak()
     p_tf32 = p_bf16 * TF32_PER_BF16
     t_peak = f_bf16 / (p_bf16 * 1e12) + f_tf32 / (p_tf32 * 1e12)
@@ -387,7 +415,10 @@ def measure_prefill(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
                        "frac": t_peak / (ms / 1e3),
                        "peak_kind": f"{kind} bf16 burst; tf32 = bf16 x 1.1/2.25 (nominal ratio)"},
             "hbm": {"achieved_gbs": nbytes / (ms / 1e3) / 1e9, "algorithmic_bytes": nbytes, "peak": hbm_peak,
-                    "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "peak_kind": hbm_kind}}
+                    "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "peak_kind": hbm_kind},
+            "align_mode": {"block_tokens": block, "snapshots": int(nsnap.sum()), "snapshot_state_bytes": snap_bytes,
+                           "ms_per_step": ms_align, "value": T / (ms_align / 1e3),
+                           "overhead_vs_plain": ms_align / ms - 1.0}}
 
 
 def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:

@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
         "gdn_decode_step": [D, P, P, P, P, P, P, P, P, P, f32, P, P, i32, P, P],
         "gdn_chunk_prefill": [D, P, P, P, P, P, P, P, P, P, P, P, f32, P, P, i32, i32, P, sz, P, P],
         "gdn_chunk_prefill_noalloc": [D, P, P, P, P, P, P, P, P, P, P, P, f32, P, P, i32, i32, P, P],
+        "gdn_chunk_prefill_align": [D, P, P, P, P, P, P, P, P, P, P, P, f32, P, P, i32, i32, P, i32, P, i32, P, sz,
+                                    P, P],
         "gdn_spec_verify": [D, P, P, P, P, P, P, P, P, P, P, f32, P, P, i32, i32, P, P],
         "gdn_spec_commit": [D, P, P, P, P, P, i32, i32, i32, P, P],
         "gdn_gated_rmsnorm": [P, P, P, f32, P, i32, i32, i32, P],
@@ -201,6 +203,38 @@ def gdn_chunk_prefill(dims, qkv0, conv_w, conv_hist, state, query_start_loc, slo
                                   _ptr(beta), _ptr(z), _ptr(gamma), float(eps), _ptr(o), _ptr(ogate), N, T,
                                   _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
            "gdn_chunk_prefill")
+
+
+def gdn_chunk_prefill_align(dims, qkv0, conv_w, conv_hist, state, query_start_loc, slot_idx, alpha, beta, z,
+                            gamma, eps, block_tokens, snap_slot=None, prefix_len=None, o=None, ogate=None,
+                            has_init=None, workspace=None, dev_err=None, stream=None):
+    N = slot_idx.shape[0]
+    T = qkv0.shape[0]
+    Hv, dv = dims.num_v_heads, dims.head_v_dim
+    _common(dims, conv_w, conv_hist, state, gamma)
+    _need(qkv0, "qkv0", torch.bfloat16, (T, dims.channels))
+    _need(query_start_loc, "query_start_loc", torch.int32, (N + 1,))
+    _need(slot_idx, "slot_idx", torch.int32, (N,))
+    _need(has_init, "has_init", (torch.uint8, torch.bool), (N,), optional=True)
+    _need(alpha, "alpha", torch.float32, (T, Hv))
+    _need(beta, "beta", torch.float32, (T, Hv))
+    _need(z, "z", torch.bfloat16, (T, Hv, dv), optional=ogate is None)
+    _need(o, "o", torch.bfloat16, (T, Hv, dv), optional=True)
+    _need(ogate, "ogate", torch.bfloat16, (T, Hv * dv), optional=True)
+    _need(prefix_len, "prefix_len", torch.int32, (N,), optional=True)
+    max_snaps = 0 if snap_slot is None else snap_slot.shape[1]
+    _need(snap_slot, "snap_slot", torch.int32, (N, max_snaps), optional=True)
+    _need(dev_err, "dev_err", torch.int32, (1,), optional=True)
+    need = gdn_prefill_workspace_bytes(dims, N, T)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qkv0.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_chunk_prefill_align(ctypes.byref(dims), _ptr(qkv0), _ptr(conv_w), _ptr(conv_hist), _ptr(state),
+                                        _ptr(query_start_loc), _ptr(slot_idx), _ptr(has_init), _ptr(alpha),
+                                        _ptr(beta), _ptr(z), _ptr(gamma), float(eps), _ptr(o), _ptr(ogate), N, T,
+                                        _ptr(prefix_len), int(block_tokens), _ptr(snap_slot), max_snaps,
+                                        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
+           "gdn_chunk_prefill_align")
 
 
 def gdn_chunk_prefill_noalloc(dims, qkv0, conv_w, conv_hist, state, query_start_loc, slot_idx, alpha, beta, z,

@@ -208,7 +208,39 @@ gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const floa
     return GDN_ERR_INVALID_ARG;
   PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
                 dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
-                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace)};
+                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace), nullptr, nullptr, 0, 0};
+  return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_chunk_prefill_align(const gdn_dims* d, const uint16_t* qkv0, const float* conv_w, uint16_t* conv_hist,
+                                   float* state, const int32_t* qsl, const int32_t* slot_idx, const uint8_t* has_init,
+                                   const float* alpha, const float* beta, const uint16_t* z, const float* gamma,
+                                   float eps, uint16_t* o, uint16_t* ogate, int32_t num_seqs, int32_t num_tokens,
+                                   const int32_t* prefix_len, int32_t block_tokens, const int32_t* snap_slot,
+                                   int32_t max_snaps, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                   void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
+  if (block_tokens <= 0 || block_tokens % 64 != 0 || max_snaps < 0 || (max_snaps > 0 && !snap_slot))
+    return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!qkv0 || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+  if (!o && !ogate) return GDN_ERR_INVALID_ARG;
+  if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && !aligned(qkv0, 16)) return GDN_ERR_INVALID_ARG;
+  if ((o && !aligned(o, 8)) || (ogate && (!aligned(ogate, 16) || !aligned(z, 16) || !aligned(gamma, 16))))
+    return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_workspace_bytes(d, num_seqs, num_tokens);
+  if (workspace_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 256))))
+    return GDN_ERR_INVALID_ARG;
+  PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
+                dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
+                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace), prefix_len,
+                max_snaps > 0 ? snap_slot : nullptr, block_tokens, max_snaps};
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -236,7 +268,7 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
   if (gdn::static_prefill_order(&order) != cudaSuccess) return GDN_ERR_CUDA;
   PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
                 dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
-                d->num_slots, num_seqs, num_tokens, order};
+                d->num_slots, num_seqs, num_tokens, order, nullptr, nullptr, 0, 0};
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -66,6 +66,12 @@ struct PrefillArgs {
   int32_t* dev_err;
   int Hk, Hv, G, CH, Rs, N, T;
   int32_t* order;             // [N] scratch: requests, longest first (filled by launch_prefill), or nullptr
+  // align mode (all nullptr / 0 otherwise): pos0[n] tokens already in request n's slot; chunks end on
+  // absolute multiples of 64, and after every absolute multiple of snap_block the state and history go
+  // to snap_slot[n][j] (j-th such boundary of this call; -1 skips)
+  const int32_t* pos0;
+  const int32_t* snap_slot;   // [N][max_snaps]
+  int snap_block, max_snaps;
 };
 
 struct NormArgs {

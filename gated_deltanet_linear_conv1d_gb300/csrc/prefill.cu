@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     return;
   }
   if (t1 == t0) return;  // no tokens: the slot is left untouched
+  const int p0 = p.pos0 ? p.pos0[n] : 0;  // tokens of the request before this call
+  if (p0 < 0) {
+    if (tid == 0 && g == 0) report(p.dev_err, GDN_DEVERR_OFFSETS);
+    return;
+  }
   const bool init = p.has_init ? p.has_init[n] != 0 : true;
 
   uint16_t* KQ = reinterpret_cast<uint16_t*>(smem + kKQ);
@@ -288,17 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const uint32_t sKQ = smem_u32(KQ), sKG = smem_u32(KGb), sKT = smem_u32(KTb), sS0 = smem_u32(S0b);
   const uint32_t sTB = smem_u32(TBb), sPB = smem_u32(PBb);
 
-  const int nchunks = (t1 - t0 + kC - 1) / kC;
+  // chunks end on absolute multiples of 64 (p0 tokens precede this call), so
+  // the first one may be short
+  const int first = min(kC - p0 % kC, t1 - t0);
+  const int nchunks = 1 + (t1 - t0 - first + kC - 1) / kC;
   bool ok = true;
   // alpha and beta of the next chunk are loaded one chunk ahead (thread t: token t)
   float alpha_n = 1.f, beta_n = 0.f;
-  if (tid < min(kC, t1 - t0)) {
+  if (tid < first) {
     alpha_n = p.alpha[(size_t)(t0 + tid) * p.Hv + h];
     beta_n = p.beta[(size_t)(t0 + tid) * p.Hv + h];
   }
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int tc = t0 + c * kC;
-    const int L = min(kC, t1 - tc);
+  int tc = t0, L = first;  // this chunk: tokens tc .. tc + L - 1
+  for (int c = 0; c < nchunks && ok; ++c, tc += L, L = min(kC, t1 - tc)) {
     const uint32_t par = c & 1;
 
     uint16_t* const ZS = zs_buf(c & 1);  // this chunk's z rows (TMA issued one chunk ahead)
@@ -307,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (tid < kC) {
       const float la = tid < L ? fmaxf(log2f(alpha_n), -115.f) : 0.f;  // alpha in (0, 1]
       const float b = tid < L ? beta_n : 0.f;
-      if (c + 1 < nchunks && tid < min(kC, t1 - tc - kC)) {
-        alpha_n = p.alpha[(size_t)(tc + kC + tid) * p.Hv + h];
-        beta_n = p.beta[(size_t)(tc + kC + tid) * p.Hv + h];
+      if (c + 1 < nchunks && tid < min(kC, t1 - tc - L)) {
+        alpha_n = p.alpha[(size_t)(tc + L + tid) * p.Hv + h];
+        beta_n = p.beta[(size_t)(tc + L + tid) * p.Hv + h];
       }
       float s = la;
 #pragma unroll
@@ -639,10 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (!wait_mma(&bars[1], par)) { ok = false; break; }
     // the scratch area is free again (A and T consumed): raw rows of the next chunk
     if (tid == 0 && c + 1 < nchunks) {
-      issue_x(tc + kC);
+      issue_x(tc + L);
       if (want_gate) {
         bulk_wait_read_all();  // the Ogate store of the previous chunk has read that buffer
-        issue_z(tc + kC, (c + 1) & 1);
+        issue_z(tc + L, (c + 1) & 1);
       }
     }
     {
@@ -768,6 +775,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           bulk_s2g(p.ogate + ((size_t)(tc + t) * p.Hv + h) * kHeadDim, ZS + t * kHeadDim, 256);
       }
       bulk_commit();
+    }
+    // ---- align mode: after an absolute multiple of the block, the state (tensor
+    // memory, updated by this chunk's MMAs) and the conv windows go to a snapshot slot
+    if (p.snap_slot) {
+      const int done = p0 + (tc + L - t0);
+      if (done % p.snap_block == 0) {
+        const int js = done / p.snap_block - p0 / p.snap_block - 1;
+        const int ss = js < p.max_snaps ? p.snap_slot[(size_t)n * p.max_snaps + js] : -1;
+        if (ss >= p.Rs) {
+          if (tid == 0 && g == 0) report(p.dev_err, GDN_DEVERR_SLOT);
+        } else if (ss >= 0) {
+          float* sd = p.state + (((size_t)ss * p.Hv + h) * kHeadDim + row) * kHeadDim + part * 32;
+          float v[32];
+          umma::ld32(tm + lane_base + kTS_S + part * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(sd + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          if (cset < 3 && (cset == 2 || g == 0)) {
+            uint16_t* hp = p.conv_hist + ((size_t)ss * p.CH + gown) * 3;
+            hp[0] = hw[0]; hp[1] = hw[1]; hp[2] = hw[2];
+          }
+        }
+      }
     }
   }
 

@@ -169,6 +169,42 @@ gdn_status gdn_chunk_prefill(const gdn_dims *dims, const uint16_t *qkv0, const f
                              void *stream);
 
 /*
+ * gdn_chunk_prefill_align - gdn_chunk_prefill in "align" prefix-cache mode:
+ * snapshots of the recurrent state at block-aligned positions, so that a later
+ * request sharing a block-aligned prefix can start from a snapshot instead of
+ * recomputing the prefix. Pages: "Qwen3.8-27B: from model structure to vLLM
+ * inference data flow", section 05 (a prefix hit reuses whole computed blocks
+ * and skips their prefill); "how the 64 layers are dispatched in vLLM"
+ * (Qwen3.5 refuses the "all" prefix-cache mode for its GDN layers and asks for
+ * --mamba-cache-mode=align). The pages do not spell out the snapshot rule; the
+ * reading implemented: after every absolute position that is a multiple of
+ * block_tokens, the state of every value head and the conv history are copied
+ * to a snapshot slot of the same pools.
+ *
+ *   arguments as gdn_chunk_prefill, plus
+ *   prefix_len   [N] int32 >= 0 or NULL (= 0): tokens of request n already
+ *                folded into its slot before this call (its absolute start).
+ *                Chunks end on absolute multiples of 64 (the first chunk of a
+ *                request may be short); the results do not depend on it.
+ *   block_tokens snapshot period, a positive multiple of 64
+ *   snap_slot    [N][max_snaps] int32: slot receiving the j-th block boundary
+ *                crossed by request n in this call (state after the token at
+ *                absolute position b*block_tokens - 1); -1 skips; boundaries
+ *                past max_snaps are skipped; >= num_slots sets
+ *                GDN_DEVERR_SLOT. Snapshot slots must differ from every live
+ *                slot of the call.
+ *   max_snaps    >= 0 (0: no snapshots, snap_slot may be NULL)
+ */
+gdn_status gdn_chunk_prefill_align(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
+                                   uint16_t *conv_hist, float *state, const int32_t *query_start_loc,
+                                   const int32_t *slot_idx, const uint8_t *has_init, const float *alpha,
+                                   const float *beta, const uint16_t *z, const float *gamma, float eps,
+                                   uint16_t *o, uint16_t *ogate, int32_t num_seqs, int32_t num_tokens,
+                                   const int32_t *prefix_len, int32_t block_tokens,
+                                   const int32_t *snap_slot, int32_t max_snaps, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
  * gdn_chunk_prefill_noalloc - gdn_chunk_prefill without a workspace argument,
  * for callers that cannot allocate device memory at the call site (a host
  * whose device memory is all reserved up front by its own pool, with no

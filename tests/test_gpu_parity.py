@@ -341,3 +341,52 @@ def test_spec_verify_positions(b, P):
     idx = torch.from_numpy(ck.astype(np.int64)).cuda()
     U.check_state(d["state"][idx].cpu().numpy(), ref["state"][ck], U.STATE_REL_L2_DECODE, "checkpoints")
     np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), ref["conv_hist"][ck])
+
+
+# ---------------------------------------------------------------- align-mode snapshots (prefix caching)
+
+def test_prefill_align_snapshots_equal_prefix_runs(b):
+    """Snapshots after every absolute multiple of the block (128) equal the oracle run on that prefix;
+    chunks start on absolute multiples of 64 (first chunks of 28, 36 and 1 tokens here); skipped and
+    unused snapshot slots stay untouched; the live results equal a plain prefill's."""
+    dims = synth.RANK_HEADS
+    lengths = [300, 70, 129, 64, 5]
+    prefix = np.array([0, 64, 100, 256, 127], np.int32)
+    B = 128
+    w = synth.prefill_workload(dims, lengths, seed=55)
+    N = len(lengths)
+    free = np.setdiff1d(np.arange(w["num_slots"]), w["slot_idx"]).astype(np.int32)
+    snap = np.full((N, 2), -1, np.int32)
+    snap[0] = free[0:2]
+    snap[1, 0] = free[2]
+    snap[4, 0] = free[3]  # request 2 crosses 128 too but its snapshot is skipped (-1)
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    T = int(sum(lengths))
+    og = torch.zeros((T, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err = _dev_err()
+    b.gdn_chunk_prefill_align(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["query_start_loc"],
+                              d["slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], B,
+                              snap_slot=U.dev(snap), prefix_len=U.dev(prefix), ogate=og, has_init=d["has_init"],
+                              dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    _check_prefill(w, d, None, og, np.arange(N))
+    qsl = w["query_start_loc"]
+    for n in range(N):
+        for j in range(2):
+            if snap[n, j] < 0:
+                continue
+            rel = (prefix[n] // B + 1 + j) * B - prefix[n]
+            toks = np.arange(qsl[n], qsl[n] + rel)
+            s = int(w["slot_idx"][n])
+            r = oracle.forward(dims, w["qkv0"][toks], w["conv_w"], np.ascontiguousarray(w["conv_hist"][[s]]),
+                               np.ascontiguousarray(w["state"][[s]]), np.array([0, rel], np.int32),
+                               np.zeros(1, np.int32), w["alpha"][toks], w["beta"][toks], w["z"][toks], w["gamma"],
+                               w["eps"], has_init=w["has_init"][[n]], inplace=True)
+            k = int(snap[n, j])
+            U.check_state(d["state"][k].cpu().numpy(), r["state"][0], U.STATE_REL_L2_PREFILL, f"snapshot {n}.{j}")
+            np.testing.assert_array_equal(U.host_bits(d["conv_hist"][k]), r["conv_hist"][0])
+    untouched = np.setdiff1d(free, snap[snap >= 0])
+    idx = torch.from_numpy(untouched.astype(np.int64)).cuda()
+    np.testing.assert_array_equal(d["state"][idx].cpu().numpy(), w["state"][untouched])
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), w["conv_hist"][untouched])
