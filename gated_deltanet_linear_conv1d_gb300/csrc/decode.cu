@@ -22,12 +22,17 @@
 //    fp32 = 32 KiB each) through a ring of shared-memory stages with bulk (TMA)
 //    copies completing on mbarriers, running ahead of the consumers; it also
 //    stages the unit's QKV0, conv history and z segments (double-buffered);
-//  - sixteen consumer warps compute the conv + L2 norm of the unit for all P
-//    positions, then each warp takes 4 rows of a half-tile (8 lanes per row):
-//    four 16-byte shared loads per lane, then per position the two dot
-//    products (S k, S q) reduced over the 8 lanes, the update kept in
-//    registers, and four coalesced 16-byte stores per lane straight to HBM;
-//    then the gated RMSNorm of each head and position.
+//  - sixteen consumer warps compute the conv of the unit for all P positions
+//    and |q|^2, |k|^2, k . q in one reduction pass (q and k are normalised as
+//    they are loaded into registers), then each warp takes 4 rows of a
+//    half-tile (8 lanes per row): four 16-byte shared loads per lane, then per
+//    position the two dot products (S k, S q) reduced over the 8 lanes, the
+//    update kept in registers, and four coalesced 16-byte stores per lane
+//    straight to HBM; then the gated RMSNorm of all the unit's heads and
+//    positions at once. Four consumer barriers per unit; the next unit's slot,
+//    alpha and beta are loaded while the current one runs, so the consumers
+//    keep pace with the copies and the producer, not the consumers, sets the
+//    rate.
 // Every wait is bounded: a stalled copy sets GDN_DEVERR_TIMEOUT and the CTA
 // leaves instead of hanging.
 #include "device.cuh"
@@ -62,8 +67,8 @@ struct Layout {
     q = rest;        rest += P * kHeadDim * 4;              // [P][128] fp32
     k = rest;        rest += P * kHeadDim * 4;              // [P][128] fp32
     v = rest;        rest += G * P * kHeadDim * 4;          // [G][P][128] fp32
-    o = rest;        rest += P * kHeadDim * 4;              // [P][128] fp32
-    red = rest;      rest += P * 32 * 4;                    // [P][32] fp32 partial sums
+    o = rest;        rest += G * P * kHeadDim * 4;          // [G][P][128] fp32
+    red = rest;      rest += (P * 16 + G * P * 4) * 4;      // [P][16] norm and [G*P][4] RMS partial sums
     ab = rest;       rest += kMaxGroup * kMaxPos * 4 * 4;   // [G][P][4] alpha, beta
     bars = rest;     rest += (2 * kMaxStages + 4) * 8 + 16; // mbarriers + abort flag
     stages = (kSmemLimit - rest) / (int)kHalfBytes;
@@ -208,21 +213,35 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
   // work but still passes every barrier, so no thread is left waiting at one.
   const int ctid = tid;  // 0 .. kConsumers-1
   const uint64_t wpol = l2_policy_evict_first();
+  float* rms_part = red + P * 16;  // [G*P][4]
   bool dead = false;
   int t = 0, kin = 0;
+  // the next unit's slot and (threads < G*P) its alpha, beta are loaded one unit ahead
+  int slot_nx = -1;
+  float a_nx = 0.f, b_nx = 0.f;
+  auto prefetch = [&](int i) {
+    const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
+    slot_nx = p.slot_idx[n];
+    if (ctid < G * P) {
+      const size_t ai = (size_t)(n * P + ctid % P) * p.Hv + G * j + ctid / P;
+      a_nx = p.alpha[ai];
+      b_nx = p.beta[ai];
+    }
+  };
+  if (nunits > 0) prefetch(0);
   for (int i = 0; i < nunits; ++i) {
     const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
-    if (!unit_slots_ok(p, n)) {
-      if (ctid == 0 && p.slot_idx[n] >= 0) report(p.dev_err, GDN_DEVERR_SLOT);
+    const int slot = slot_nx;
+    const float a_cur = a_nx, b_cur = b_nx;
+    if (i + 1 < nunits) prefetch(i + 1);
+    if (slot < 0 || slot >= p.Rs || (p.spec_slot && !unit_slots_ok(p, n))) {
+      if (ctid == 0 && slot >= 0) report(p.dev_err, GDN_DEVERR_SLOT);
       continue;
     }
-    const int slot = p.slot_idx[n];
     const int b = kin & 1;
     if (ctid < G * P) {
-      const int g = ctid / P, q = ctid % P;
-      const size_t ai = (size_t)(n * P + q) * p.Hv + G * j + g;
-      ab[ctid * 4 + 0] = p.alpha[ai];
-      ab[ctid * 4 + 1] = p.beta[ai];
+      ab[ctid * 4 + 0] = a_cur;  // [g][q] with g = ctid / P, q = ctid % P
+      ab[ctid * 4 + 1] = b_cur;
     }
     dead = dead || *abort_flag;
     if (!dead && !mbar_wait_bounded(&in_full[b], (kin >> 1) & 1)) {
@@ -269,27 +288,27 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
       }
     }
     consumer_sync();
-    // ---- L2 norm of q (warps 0-3) and k (warps 4-7) per position, then k . q
-    for (int q = 0; q < P; ++q)
-      if (warp < 8) {
-        const float x = (warp < 4 ? qs : ks)[q * kHeadDim + (warp & 3) * 32 + lane];
-        const float ss = warp_sum(x * x);
-        if (lane == 0) red[q * 32 + warp] = ss;
-      }
-    consumer_sync();
-    for (int q = 0; q < P; ++q)
-      if (warp < 8) {
-        const float* r = red + q * 32 + (warp < 4 ? 0 : 4);
-        (warp < 4 ? qs : ks)[q * kHeadDim + (warp & 3) * 32 + lane] *=
-            rsqrtf(((r[0] + r[1]) + (r[2] + r[3])) + 1e-12f);
-      }
-    consumer_sync();
+    // ---- |q|^2, |k|^2 and k . q of the raw conv outputs per position in one
+    // pass (warps 0-3, a quarter of the channels each); q and k are normalised
+    // where they are loaded into registers below
     for (int q = 0; q < P; ++q)
       if (warp < 4) {
-        const float kqp = warp_sum(ks[q * kHeadDim + warp * 32 + lane] * qs[q * kHeadDim + warp * 32 + lane]);
-        if (lane == 0) red[q * 32 + 8 + warp] = kqp;
+        const float xq = qs[q * kHeadDim + warp * 32 + lane], xk = ks[q * kHeadDim + warp * 32 + lane];
+        const float sq = warp_sum(xq * xq), sk = warp_sum(xk * xk), skq = warp_sum(xk * xq);
+        if (lane == 0) {
+          red[q * 16 + warp] = sq;
+          red[q * 16 + 4 + warp] = sk;
+          red[q * 16 + 8 + warp] = skq;
+        }
       }
     consumer_sync();
+    // per position: 1/|q|, 1/|k| (L2 norm, eps 1e-12 under the root) and the normalised k . q
+    auto norms = [&](int q, float& iq, float& ik, float& kqn) {
+      const float* r = red + q * 16;
+      iq = rsqrtf(((r[0] + r[1]) + (r[2] + r[3])) + 1e-12f);
+      ik = rsqrtf(((r[4] + r[5]) + (r[6] + r[7])) + 1e-12f);
+      kqn = ((r[8] + r[9]) + (r[10] + r[11])) * iq * ik;
+    };
 
     // Row layout: the 8 lanes 8r..8r+7 of a warp share one state row; lane
     // c = lane & 7 holds columns 4c + 32m .. 4c + 32m + 3 for m = 0..3, so each
@@ -300,12 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
     float4 kk1[4], qq1[4];
     float kq1 = 0.f;
     if constexpr (kOne) {
+      float iq, ik;
+      norms(0, iq, ik, kq1);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        kk1[m] = reinterpret_cast<const float4*>(ks)[cl + 8 * m];
-        qq1[m] = reinterpret_cast<const float4*>(qs)[cl + 8 * m];
+        const float4 kr = reinterpret_cast<const float4*>(ks)[cl + 8 * m];
+        const float4 qr = reinterpret_cast<const float4*>(qs)[cl + 8 * m];
+        kk1[m] = make_float4(kr.x * ik, kr.y * ik, kr.z * ik, kr.w * ik);
+        qq1[m] = make_float4(qr.x * iq, qr.y * iq, qr.z * iq, qr.w * iq);
       }
-      kq1 = (red[8] + red[9]) + (red[10] + red[11]);
     }
     for (int g = 0; g < G; ++g) {
       const int h = G * j + g;
@@ -336,11 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
                 qq[m] = qq1[m];
               }
             } else {
-              kq = (red[q * 32 + 8] + red[q * 32 + 9]) + (red[q * 32 + 10] + red[q * 32 + 11]);
+              float iq, ik;
+              norms(q, iq, ik, kq);
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
-                kk[m] = reinterpret_cast<const float4*>(ks + q * kHeadDim)[cl + 8 * m];
-                qq[m] = reinterpret_cast<const float4*>(qs + q * kHeadDim)[cl + 8 * m];
+                const float4 kr = reinterpret_cast<const float4*>(ks + q * kHeadDim)[cl + 8 * m];
+                const float4 qr = reinterpret_cast<const float4*>(qs + q * kHeadDim)[cl + 8 * m];
+                kk[m] = make_float4(kr.x * ik, kr.y * ik, kr.z * ik, kr.w * ik);
+                qq[m] = make_float4(qr.x * iq, qr.y * iq, qr.z * iq, qr.w * iq);
               }
             }
             float pk = 0.f, pq = 0.f;
@@ -372,37 +397,35 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
               sv[m].w = fmaf(be, kk[m].w, a * sv[m].w);
               st_global_v4_hint(grow + 4 * (cl + 8 * m), sv[m], wpol);
             }
-            if (cl == 0) os[q * kHeadDim + ri] = fmaf(be, kq, a * pq) * kInvSqrtDk;
+            if (cl == 0) os[(g * P + q) * kHeadDim + ri] = fmaf(be, kq, a * pq) * kInvSqrtDk;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
-      consumer_sync();
-      // ---- gated RMSNorm of head h at every position; thread (q, i) for q < 4
-      for (int q0 = 0; q0 < P; q0 += 4) {
-        const int q = q0 + (ctid >> 7), i = ctid & 127;
-        float oi = 0.f;
-        if (q < P) {
-          oi = os[q * kHeadDim + i];
-          const float ss = warp_sum(oi * oi);
-          if (lane == 0) red[q * 32 + 16 + ((ctid >> 5) & 3)] = ss;
-        }
-        consumer_sync();
-        if (q < P && !dead) {
-          const float* r = red + q * 32 + 16;
-          const float ms = ((r[0] + r[1]) + (r[2] + r[3])) * (1.0f / kHeadDim);
-          const float rinv = rsqrtf(ms + p.eps);
-          const size_t row = ((size_t)(n * P + q) * p.Hv + h) * kHeadDim + i;
-          if (p.o) p.o[row] = f32_to_bf16(oi);
-          if (p.ogate) {
-            const float zz = bf16_to_f32(zs[((b * P + q) * G + g) * kHeadDim + i]);
-            p.ogate[row] = f32_to_bf16(oi * rinv * p.gamma[i] * silu(zz));
-          }
-        }
-        consumer_sync();
+    }
+    consumer_sync();
+    // ---- gated RMSNorm of every (head, position) of the unit: thread (gq, i)
+    const int GP = G * P;
+    for (int r = ctid; r < GP * kHeadDim; r += kConsumers) {  // whole warps: 128 | r's step
+      const float oi = os[r];
+      const float ss = warp_sum(oi * oi);
+      if (lane == 0) rms_part[(r >> 7) * 4 + ((r >> 5) & 3)] = ss;
+    }
+    consumer_sync();
+    for (int r = ctid; r < GP * kHeadDim && !dead; r += kConsumers) {
+      const int gq = r >> 7, i = r & 127, g = gq / P, q = gq % P;
+      const float* rp = rms_part + gq * 4;
+      const float rinv = rsqrtf(((rp[0] + rp[1]) + (rp[2] + rp[3])) * (1.0f / kHeadDim) + p.eps);
+      const float oi = os[r];
+      const size_t orow = ((size_t)(n * P + q) * p.Hv + G * j + g) * kHeadDim + i;
+      if (p.o) p.o[orow] = f32_to_bf16(oi);
+      if (p.ogate) {
+        const float zz = bf16_to_f32(zs[((b * P + q) * G + g) * kHeadDim + i]);
+        p.ogate[orow] = f32_to_bf16(oi * rinv * p.gamma[i] * silu(zz));
       }
     }
+    consumer_sync();  // the unit's staged inputs (z above) are no longer read
     if (ctid == 0) mbar_arrive(&in_empty[b]);
     ++kin;
   }
