@@ -77,12 +77,14 @@ constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
 constexpr int kZS1 = kPB + 8192;        // bf16 [64][128]: the same for odd chunks
 constexpr int kSmall = kZS1 + 16384;    // small per-chunk vectors
-constexpr int kSmallFloats = 64 * 8 + 8 * 64 + 4 * 64 + 64;
+constexpr int kSmallFloats = 64 * 8 + 4 * 64 + 64;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
 
 // Tensor-memory columns (v, fp32 channel-major, lives in the last 64).
-constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_X = 192, kT_Z = 256, kT_E = 320, kT_O = 384, kT_V = 448,
+// D1 = [K;Q][K;Q]^T takes 128 columns; E reuses its first 64 once A, P and the
+// norms have been read out of it.
+constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_E = 128, kT_X = 256, kT_Z = 320, kT_O = 384, kT_V = 448,
                    kTmemCols = 512;
 
 __device__ __forceinline__ float to_tf32(float x) { return umma::to_tf32(x); }
@@ -214,8 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* ikv = iqv + 64;         // [64] 1/|k|
   float* rinv = ikv + 64;        // [64] gate 1/rms
   float* scan = rinv + 64;       // [64] scan scratch
-  float* npart = scan + 64;      // [8][64] norm partials (warps 0-3: q, 4-7: k)
-  float* rpart = npart + 8 * 64; // [4][64] gate partials
+  float* rpart = scan + 64;      // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
   // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5, 6: z rows
   // of even / odd chunks
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   __syncthreads();
   umma::fence_after_sync();
 
-  const uint32_t id_kk = umma::idesc(umma::kBF16, true, true, 128, 64);
+  const uint32_t id_kk = umma::idesc(umma::kBF16, true, true, 128, 128);
   const uint32_t id_xz = umma::idesc(umma::kBF16, false, true, 128, 64);
   const uint32_t id_e = umma::idesc(umma::kTF32, false, false, 128, 64);
   const uint32_t id_s = umma::idesc(umma::kTF32, false, false, 128, 128);
@@ -388,12 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
               *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
                   make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
             }
-            // per-token sum of squares over this warp's 32 channels
-            float sq[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sq[e] = ya[e] * ya[e];
-            const float tot = reduce8(sq, lane);
-            if ((lane & 3) == 0) npart[(kKind * 4 + quarter) * 64 + grp * 8 + tok8(lane)] = tot;
           }
         }
         if constexpr (kKind == 2) {  // v row d = this thread's lane, columns kT0 ..
@@ -440,7 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     umma::wait_st();
     sync_for_mma();
 
-    // ---- [K;Q] K^T (bf16): D1 lanes 0-63 = K K^T rows, lanes 64-127 = Q K^T rows
+    // ---- [K;Q][K;Q]^T (bf16): D1 lanes 0-63 = K rows, 64-127 = Q rows; columns
+    // 0-63 against K, 64-127 against Q. A and P use columns 0-63, the per-token
+    // norms |k|^2 and |q|^2 are its diagonal.
     if (tid == 0) {
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk) {
@@ -448,12 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         umma::mma<umma::kBF16>(tm + kT_D1, a, a, id_kk, kk > 0);
       }
       umma::commit(&bars[0]);
-    }
-    if (tid < kC) {
-      const float sq = (npart[0 * 64 + tid] + npart[1 * 64 + tid]) + (npart[2 * 64 + tid] + npart[3 * 64 + tid]);
-      const float sk = (npart[4 * 64 + tid] + npart[5 * 64 + tid]) + (npart[6 * 64 + tid] + npart[7 * 64 + tid]);
-      iqv[tid] = rsqrtf(sq + 1e-12f);
-      ikv[tid] = rsqrtf(sk + 1e-12f);
     }
     // ---- S0 as a bf16 operand; S *= e^{g_C} in tensor memory for the update below
     {
@@ -487,8 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       umma::commit(&bars[1]);
     }
 
-    // ---- A (for the inverse) and P from K K^T and Q K^T
+    // ---- 1/|k|, 1/|q| (L2 norm, eps 1e-12 under the root) from the diagonal of
+    // D1: warp (quarter, part 0) reads the 32 columns of its own rows
     if (!wait_mma(&bars[0], par)) { ok = false; break; }
+    if (part == 0) {
+      float v[32];
+      umma::ld32(tm + lane_base + kT_D1 + 32 * quarter, v);
+      float dg = v[0];
+#pragma unroll
+      for (int e = 1; e < 32; ++e) dg = e == lane ? v[e] : dg;
+      const float inv = rsqrtf(dg + 1e-12f);
+      if (row < 64) ikv[row] = inv;
+      else iqv[row - 64] = inv;
+    }
+    __syncthreads();
+    // ---- A (for the inverse) and P from K K^T and Q K^T
     {
       float v[16];
       umma::ld16(tm + lane_base + kT_D1 + part * 16, v);
