@@ -52,6 +52,7 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 512;  // 16 warps: 4 per tensor-memory lane quarter
+constexpr int kTmaThread = kThreads - 32;  // issues the in-loop TMA copies (thread 0 issues the MMAs)
 constexpr int kC = 64;  // chunk length
 constexpr float kInvSqrtDk = 0.08838834764831845f;
 
@@ -77,7 +78,7 @@ constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
 constexpr int kZS1 = kPB + 8192;        // bf16 [64][128]: the same for odd chunks
 constexpr int kSmall = kZS1 + 16384;    // small per-chunk vectors
-constexpr int kSmallFloats = 64 * 8 + 4 * 64 + 64;
+constexpr int kSmallFloats = 64 * 7 + 4 * 64;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
 
@@ -126,6 +127,14 @@ __device__ __forceinline__ int tok8(int lane) {
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// log2(x) via the hardware approximation (lg2.approx); its absolute error is
+// far below the rounding of the products the gates scale.
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -215,8 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* iqv = bv + 64;          // [64] 1/|q|
   float* ikv = iqv + 64;         // [64] 1/|k|
   float* rinv = ikv + 64;        // [64] gate 1/rms
-  float* scan = rinv + 64;       // [64] scan scratch
-  float* rpart = scan + 64;      // [4][64] gate partials
+  float* rpart = rinv + 64;      // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
   // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5, 6: z rows
   // of even / odd chunks
@@ -300,10 +308,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const int nchunks = 1 + (t1 - t0 - first + kC - 1) / kC;
   bool ok = true;
   // alpha and beta of the next chunk are loaded one chunk ahead (thread t: token t)
-  float alpha_n = 1.f, beta_n = 0.f;
-  if (tid < first) {
-    alpha_n = p.alpha[(size_t)(t0 + tid) * p.Hv + h];
-    beta_n = p.beta[(size_t)(t0 + tid) * p.Hv + h];
+  // (warp 0, lane l: tokens l and l + 32 of the chunk)
+  float alpha_n0 = 1.f, beta_n0 = 0.f, alpha_n1 = 1.f, beta_n1 = 0.f;
+  if (warp == 0) {
+    if (lane < first) {
+      alpha_n0 = p.alpha[(size_t)(t0 + lane) * p.Hv + h];
+      beta_n0 = p.beta[(size_t)(t0 + lane) * p.Hv + h];
+    }
+    if (lane + 32 < first) {
+      alpha_n1 = p.alpha[(size_t)(t0 + lane + 32) * p.Hv + h];
+      beta_n1 = p.beta[(size_t)(t0 + lane + 32) * p.Hv + h];
+    }
   }
   int tc = t0, L = first;  // this chunk: tokens tc .. tc + L - 1
   for (int c = 0; c < nchunks && ok; ++c, tc += L, L = min(kC, t1 - tc)) {
@@ -311,31 +326,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 
     uint16_t* const ZS = zs_buf(c & 1);  // this chunk's z rows (TMA issued one chunk ahead)
 
-    // ---- gates: g = inclusive cumsum of log2(alpha) (so e^{g ln 2} = prod alpha), beta
-    if (tid < kC) {
-      const float la = tid < L ? fmaxf(log2f(alpha_n), -115.f) : 0.f;  // alpha in (0, 1]
-      const float b = tid < L ? beta_n : 0.f;
-      if (c + 1 < nchunks && tid < min(kC, t1 - tc - L)) {
-        alpha_n = p.alpha[(size_t)(tc + L + tid) * p.Hv + h];
-        beta_n = p.beta[(size_t)(tc + L + tid) * p.Hv + h];
+    // ---- gates (warp 0, two tokens per lane, no CTA barrier): g = inclusive
+    // cumsum of log2(alpha) (so e^{g ln 2} = prod alpha), e^g, e^{g_C - g_t}, beta
+    if (warp == 0) {
+      const float la0 = lane < L ? fmaxf(lg2(alpha_n0), -115.f) : 0.f;  // alpha in (0, 1]
+      const float la1 = lane + 32 < L ? fmaxf(lg2(alpha_n1), -115.f) : 0.f;
+      bv[lane] = lane < L ? beta_n0 : 0.f;
+      bv[lane + 32] = lane + 32 < L ? beta_n1 : 0.f;
+      const int nl = c + 1 < nchunks ? min(kC, t1 - tc - L) : 0;  // next chunk, loaded ahead
+      if (lane < nl) {
+        alpha_n0 = p.alpha[(size_t)(tc + L + lane) * p.Hv + h];
+        beta_n0 = p.beta[(size_t)(tc + L + lane) * p.Hv + h];
       }
-      float s = la;
+      if (lane + 32 < nl) {
+        alpha_n1 = p.alpha[(size_t)(tc + L + lane + 32) * p.Hv + h];
+        beta_n1 = p.beta[(size_t)(tc + L + lane + 32) * p.Hv + h];
+      }
+      float s0 = la0, s1 = la1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += u;
+        const float u0 = __shfl_up_sync(0xffffffffu, s0, o), u1 = __shfl_up_sync(0xffffffffu, s1, o);
+        if (lane >= o) {
+          s0 += u0;
+          s1 += u1;
+        }
       }
-      scan[tid] = s;
-      bv[tid] = b;
+      s1 += __shfl_sync(0xffffffffu, s0, 31);
+      const float gl = __shfl_sync(0xffffffffu, L - 1 < 32 ? s0 : s1, (L - 1) & 31);  // g at the chunk end
+      gv[lane] = s0;
+      gv[lane + 32] = s1;
+      egv[lane] = ex2(s0);
+      egv[lane + 32] = ex2(s1);
+      glv[lane] = lane < L ? ex2(gl - s0) : 0.f;
+      glv[lane + 32] = lane + 32 < L ? ex2(gl - s1) : 0.f;
     }
-    __syncthreads();
-    if (tid < kC) {
-      const float gt = scan[tid] + (tid >= 32 ? scan[31] : 0.f);
-      gv[tid] = gt;
-      egv[tid] = ex2(gt);
-    }
-    __syncthreads();
-    if (tid < kC) glv[tid] = tid < L ? ex2(gv[L - 1] - gv[tid]) : 0.f;
 
     // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time; q, k
     // written channel-major to shared memory, v to tensor memory. Every token
@@ -649,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // ---- Y = V^T - X (tf32, rows dv), over S0's now-free space
     if (!wait_mma(&bars[1], par)) { ok = false; break; }
     // the scratch area is free again (A and T consumed): raw rows of the next chunk
-    if (tid == 0 && c + 1 < nchunks) {
+    if (tid == kTmaThread && c + 1 < nchunks) {
       issue_x(tc + L);
       if (want_gate) {
         bulk_wait_read_all();  // the Ogate store of the previous chunk has read that buffer
@@ -771,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // ... then stored with one tensor copy (a partial last chunk row by row, so
     // that the next request's rows are not touched); the next chunk's z rows
     // wait until these stores have read ZS
-    if (tid == 0 && want_gate) {
+    if (tid == kTmaThread && want_gate) {
       if (L == kC) {
         tma_store_3d(&tmo, 0, h, tc, ZS);
       } else {
@@ -825,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // give MMAs still in flight a second bounded chance before the memory is freed
     for (int b = 0; b < 7; ++b) mbar_wait_bounded(&bars[b], 0);
   }
-  if (tid == 0) bulk_wait_all();  // Ogate rows stored
+  if (tid == kTmaThread) bulk_wait_all();  // Ogate rows stored
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
