@@ -155,6 +155,10 @@ __device__ __forceinline__ float silu_ftz(float x) {
   return fmaf(hx, t, hx);
 }
 
+// Barrier 1 over warps 0-7 only (the triangular inverse runs there while the
+// other warps form Y).
+__device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 // Waits for an MMA-completion phase; the verdict is uniform over the CTA.
 __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity) {
   const int ok = __syncthreads_and(mbar_wait_bounded(bar, parity) ? 1 : 0);
@@ -554,124 +558,154 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       }
     }
     __syncthreads();
-    // ---- T = (I + A)^-1 by recursive doubling over 16-row blocks (T row-major
-    // in TS, rows of kLd floats), with T diag(beta) written as the tf32 K-major
-    // operand as each block is finished:
-    //   diagonal blocks T_aa by forward substitution (one column per thread);
-    //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
-    //   then the lower-left 32x32 block = -T_hi (A_lo-left T_lo), T_hi and T_lo
-    //   being the two 32x32 diagonal blocks.
-    // A product thread owns a 4x4 tile over a share of the inner index (the
-    // partners' shares are summed with shuffles); operands come in 16-byte loads.
-    auto put_tb4 = [&](int r, int c0, float4 t4) {  // T[r][c0..c0+3] -> Tb
-      const float4 f = make_float4(to_tf32(t4.x * bv[c0]), to_tf32(t4.y * bv[c0 + 1]), to_tf32(t4.z * bv[c0 + 2]),
-                                   to_tf32(t4.w * bv[c0 + 3]));
-      *reinterpret_cast<float4*>(TBb + umma::tile_off(r, c0 * 4, 256)) = f;
-    };
-    // acc[rr][cc] += X[rr][i] Y[i][cc] for i = i0, i0 + step, ... (4 at a time) below i1
-    auto mm44 = [](float (&acc)[4][4], const float* X, int ldx, const float* Y, int ldy, int i0, int i1,
-                   int step) {
-      for (int i = i0; i < i1; i += step) {
-        float xs[4][4];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const float4 xv = *reinterpret_cast<const float4*>(X + rr * ldx + i);
-          xs[rr][0] = xv.x; xs[rr][1] = xv.y; xs[rr][2] = xv.z; xs[rr][3] = xv.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 yv = *reinterpret_cast<const float4*>(Y + (i + e) * ldy);
-#pragma unroll
+    // ---- warps 0-7 invert (I + A) while warps 8-15 form Y (the two are
+    // independent; the inverse synchronises on named barrier 1 only)
+    bool part_ok = true;
+    if (warp < 8) {
+      // ---- T = (I + A)^-1 by recursive doubling over 16-row blocks (T row-major
+      // in TS, rows of kLd floats), with T diag(beta) written as the tf32 K-major
+      // operand as each block is finished:
+      //   diagonal blocks T_aa by forward substitution (one column per thread);
+      //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
+      //   then the lower-left 32x32 block = -T_hi (A_lo-left T_lo), T_hi and T_lo
+      //   being the two 32x32 diagonal blocks.
+      // A product thread owns a 4x4 tile over a share of the inner index (the
+      // partners' shares are summed with shuffles); operands come in 16-byte loads.
+      auto put_tb4 = [&](int r, int c0, float4 t4) {  // T[r][c0..c0+3] -> Tb
+        const float4 f = make_float4(to_tf32(t4.x * bv[c0]), to_tf32(t4.y * bv[c0 + 1]), to_tf32(t4.z * bv[c0 + 2]),
+                                     to_tf32(t4.w * bv[c0 + 3]));
+        *reinterpret_cast<float4*>(TBb + umma::tile_off(r, c0 * 4, 256)) = f;
+      };
+      // acc[rr][cc] += X[rr][i] Y[i][cc] for i = i0, i0 + step, ... (4 at a time) below i1
+      auto mm44 = [](float (&acc)[4][4], const float* X, int ldx, const float* Y, int ldy, int i0, int i1,
+                     int step) {
+        for (int i = i0; i < i1; i += step) {
+          float xs[4][4];
+  #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
-            acc[rr][0] = fmaf(xs[rr][e], yv.x, acc[rr][0]);
-            acc[rr][1] = fmaf(xs[rr][e], yv.y, acc[rr][1]);
-            acc[rr][2] = fmaf(xs[rr][e], yv.z, acc[rr][2]);
-            acc[rr][3] = fmaf(xs[rr][e], yv.w, acc[rr][3]);
+            const float4 xv = *reinterpret_cast<const float4*>(X + rr * ldx + i);
+            xs[rr][0] = xv.x; xs[rr][1] = xv.y; xs[rr][2] = xv.z; xs[rr][3] = xv.w;
+          }
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 yv = *reinterpret_cast<const float4*>(Y + (i + e) * ldy);
+  #pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              acc[rr][0] = fmaf(xs[rr][e], yv.x, acc[rr][0]);
+              acc[rr][1] = fmaf(xs[rr][e], yv.y, acc[rr][1]);
+              acc[rr][2] = fmaf(xs[rr][e], yv.z, acc[rr][2]);
+              acc[rr][3] = fmaf(xs[rr][e], yv.w, acc[rr][3]);
+            }
+          }
+        }
+      };
+      // sum over the kp partner lanes (lane bits below kp)
+      auto ksum = [](float (&acc)[4][4], int kp) {
+        for (int m = 1; m < kp; m <<= 1)
+  #pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+  #pragma unroll
+            for (int cc = 0; cc < 4; ++cc) acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], m);
+      };
+      auto row4 = [](const float (&acc)[4][4], int rr) {  // a runtime row of the tile
+        float4 o = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+  #pragma unroll
+        for (int q = 1; q < 4; ++q)
+          if (rr == q) o = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+        return o;
+      };
+      if (tid < kC) {
+        const int a = tid >> 4, cc = tid & 15;
+        const float* Ab = AM + (16 * a) * kLd + 16 * a;
+        float x[16];
+  #pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float s = 0.f;
+  #pragma unroll
+          for (int i = 0; i < r; ++i) s = fmaf(Ab[r * kLd + i], x[i], s);
+          x[r] = r < cc ? 0.f : (r == cc ? 1.f : -s);
+        }
+        const int col = 16 * a + cc;
+        const float bc = bv[col];
+  #pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          TS[(16 * a + r) * kLd + col] = x[r];
+          *reinterpret_cast<float*>(TBb + umma::tile_off(16 * a + r, col * 4, 256)) = to_tf32(x[r] * bc);
+        }
+      }
+      inv_sync();
+      {  // 16 -> 32: blocks (1,0) and (3,2); threads 0-127 = block x 16 tiles x 4 shares
+        const int blk = tid >> 6, r0 = 4 * ((tid >> 4) & 3), c0 = 4 * ((tid >> 2) & 3), kq = tid & 3;
+        const int a = 1 + 2 * blk, b = a - 1;
+        if (tid < 128) {
+          float acc[4][4] = {};
+          mm44(acc, AM + (16 * a + r0) * kLd, kLd, TS + 16 * b + c0, kLd, 16 * b + 4 * kq, 16 * b + 4 * kq + 4, 4);
+          ksum(acc, 4);
+          *reinterpret_cast<float4*>(MS + (16 * blk + r0 + kq) * kMsLd + c0) = row4(acc, kq);
+        }
+        inv_sync();
+        if (tid < 128) {
+          float acc[4][4] = {};
+          mm44(acc, TS + (16 * a + r0) * kLd + 16 * a, kLd, MS + 16 * blk * kMsLd + c0, kMsLd, 4 * kq, 4 * kq + 4, 4);
+          ksum(acc, 4);
+          const float4 m4 = row4(acc, kq);
+          const float4 t4 = make_float4(-m4.x, -m4.y, -m4.z, -m4.w);
+          *reinterpret_cast<float4*>(TS + (16 * a + r0 + kq) * kLd + 16 * b + c0) = t4;
+          put_tb4(16 * a + r0 + kq, 16 * b + c0, t4);
+        }
+        inv_sync();
+      }
+      {  // 32 -> 64: rows 32-63, columns 0-31; threads 0-127 = 64 tiles x 2 shares
+        const int r0 = 4 * (tid >> 4 & 7), c0 = 4 * ((tid >> 1) & 7), kq = tid & 1;
+        if (tid < 128) {
+          // M = A[32 + r][0..32) T[0..32)[c..]: T_lo is zero above its block diagonal
+          float acc[4][4] = {};
+          mm44(acc, AM + (32 + r0) * kLd, kLd, TS + c0, kLd, (c0 < 16 ? 0 : 16) + 4 * kq, 32, 8);
+          ksum(acc, 2);
+          *reinterpret_cast<float4*>(MS + (r0 + 2 * kq) * kMsLd + c0) = row4(acc, 2 * kq);
+          *reinterpret_cast<float4*>(MS + (r0 + 2 * kq + 1) * kMsLd + c0) = row4(acc, 2 * kq + 1);
+        }
+        inv_sync();
+        if (tid < 128) {
+          // -T_hi[r][0..32) M[0..32)[c..]: T_hi is zero above its block diagonal
+          float acc[4][4] = {};
+          mm44(acc, TS + (32 + r0) * kLd + 32, kLd, MS + c0, kMsLd, 4 * kq, r0 < 16 ? 16 : 32, 8);
+          ksum(acc, 2);
+  #pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float4 m4 = row4(acc, 2 * kq + h2);
+            put_tb4(32 + r0 + 2 * kq + h2, c0, make_float4(-m4.x, -m4.y, -m4.z, -m4.w));
           }
         }
       }
-    };
-    // sum over the kp partner lanes (lane bits below kp)
-    auto ksum = [](float (&acc)[4][4], int kp) {
-      for (int m = 1; m < kp; m <<= 1)
+    } else {
+      // ---- Y = V^T - X (tf32, rows dv), over S0's space once X, Z are done;
+      // warps 8-11 take columns 0-31, warps 12-15 columns 32-63
+      part_ok = mbar_wait_bounded(&bars[1], par);
+      umma::fence_after_sync();
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr)
+      for (int hq = 0; hq < 2; ++hq) {
+        const int c0 = (part - 2) * 32 + hq * 16;
+        float v[16], vv[16];
+        umma::ld16(tm + lane_base + kT_X + c0, v);
+        umma::ld16(tm + lane_base + kT_V + c0, vv);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], m);
-    };
-    auto row4 = [](const float (&acc)[4][4], int rr) {  // a runtime row of the tile
-      float4 o = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float y4[4];
 #pragma unroll
-      for (int q = 1; q < 4; ++q)
-        if (rr == q) o = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-      return o;
-    };
-    if (tid < kC) {
-      const int a = tid >> 4, cc = tid & 15;
-      const float* Ab = AM + (16 * a) * kLd + 16 * a;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < r; ++i) s = fmaf(Ab[r * kLd + i], x[i], s);
-        x[r] = r < cc ? 0.f : (r == cc ? 1.f : -s);
-      }
-      const int col = 16 * a + cc;
-      const float bc = bv[col];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        TS[(16 * a + r) * kLd + col] = x[r];
-        *reinterpret_cast<float*>(TBb + umma::tile_off(16 * a + r, col * 4, 256)) = to_tf32(x[r] * bc);
-      }
-    }
-    __syncthreads();
-    {  // 16 -> 32: blocks (1,0) and (3,2); threads 0-127 = block x 16 tiles x 4 shares
-      const int blk = tid >> 6, r0 = 4 * ((tid >> 4) & 3), c0 = 4 * ((tid >> 2) & 3), kq = tid & 3;
-      const int a = 1 + 2 * blk, b = a - 1;
-      if (tid < 128) {
-        float acc[4][4] = {};
-        mm44(acc, AM + (16 * a + r0) * kLd, kLd, TS + 16 * b + c0, kLd, 16 * b + 4 * kq, 16 * b + 4 * kq + 4, 4);
-        ksum(acc, 4);
-        *reinterpret_cast<float4*>(MS + (16 * blk + r0 + kq) * kMsLd + c0) = row4(acc, kq);
-      }
-      __syncthreads();
-      if (tid < 128) {
-        float acc[4][4] = {};
-        mm44(acc, TS + (16 * a + r0) * kLd + 16 * a, kLd, MS + 16 * blk * kMsLd + c0, kMsLd, 4 * kq, 4 * kq + 4, 4);
-        ksum(acc, 4);
-        const float4 m4 = row4(acc, kq);
-        const float4 t4 = make_float4(-m4.x, -m4.y, -m4.z, -m4.w);
-        *reinterpret_cast<float4*>(TS + (16 * a + r0 + kq) * kLd + 16 * b + c0) = t4;
-        put_tb4(16 * a + r0 + kq, 16 * b + c0, t4);
-      }
-      __syncthreads();
-    }
-    {  // 32 -> 64: rows 32-63, columns 0-31; threads 0-127 = 64 tiles x 2 shares
-      const int r0 = 4 * (tid >> 4 & 7), c0 = 4 * ((tid >> 1) & 7), kq = tid & 1;
-      if (tid < 128) {
-        // M = A[32 + r][0..32) T[0..32)[c..]: T_lo is zero above its block diagonal
-        float acc[4][4] = {};
-        mm44(acc, AM + (32 + r0) * kLd, kLd, TS + c0, kLd, (c0 < 16 ? 0 : 16) + 4 * kq, 32, 8);
-        ksum(acc, 2);
-        *reinterpret_cast<float4*>(MS + (r0 + 2 * kq) * kMsLd + c0) = row4(acc, 2 * kq);
-        *reinterpret_cast<float4*>(MS + (r0 + 2 * kq + 1) * kMsLd + c0) = row4(acc, 2 * kq + 1);
-      }
-      __syncthreads();
-      if (tid < 128) {
-        // -T_hi[r][0..32) M[0..32)[c..]: T_hi is zero above its block diagonal
-        float acc[4][4] = {};
-        mm44(acc, TS + (32 + r0) * kLd + 32, kLd, MS + c0, kMsLd, 4 * kq, r0 < 16 ? 16 : 32, 8);
-        ksum(acc, 2);
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const float4 m4 = row4(acc, 2 * kq + h2);
-          put_tb4(32 + r0 + 2 * kq + h2, c0, make_float4(-m4.x, -m4.y, -m4.z, -m4.w));
+          for (int e = 0; e < 4; ++e) {
+            const int t = c0 + q4 * 4 + e;
+            y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * ikv[t]);
+          }
+          *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (c0 + q4 * 4) * 4, 256)) =
+              make_float4(y4[0], y4[1], y4[2], y4[3]);
         }
       }
     }
-    // ---- Y = V^T - X (tf32, rows dv), over S0's now-free space
-    if (!wait_mma(&bars[1], par)) { ok = false; break; }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
+    if (__syncthreads_or(part_ok ? 0 : 1)) { ok = false; break; }
+    umma::fence_after_sync();
     // the scratch area is free again (A and T consumed): raw rows of the next chunk
     if (tid == kTmaThread && c + 1 < nchunks) {
       issue_x(tc + L);
@@ -680,23 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         issue_z(tc + L, (c + 1) & 1);
       }
     }
-    {
-      float v[16], vv[16];
-      umma::ld16(tm + lane_base + kT_X + part * 16, v);
-      umma::ld16(tm + lane_base + kT_V + part * 16, vv);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float y4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = part * 16 + q4 * 4 + e;
-          y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * ikv[t]);
-        }
-        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (part * 16 + q4 * 4) * 4, 256)) =
-            make_float4(y4[0], y4[1], y4[2], y4[3]);
-      }
-    }
-    sync_for_mma();
     // ---- E^T = Y Tb^T (tf32)
     if (tid == 0) {
 #pragma unroll
