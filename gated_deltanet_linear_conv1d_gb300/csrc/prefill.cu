@@ -569,51 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
       //   then the lower-left 32x32 block = -T_hi (A_lo-left T_lo), T_hi and T_lo
       //   being the two 32x32 diagonal blocks.
-      // A product thread owns a 4x4 tile over a share of the inner index (the
-      // partners' shares are summed with shuffles); operands come in 16-byte loads.
-      auto put_tb4 = [&](int r, int c0, float4 t4) {  // T[r][c0..c0+3] -> Tb
-        const float4 f = make_float4(to_tf32(t4.x * bv[c0]), to_tf32(t4.y * bv[c0 + 1]), to_tf32(t4.z * bv[c0 + 2]),
-                                     to_tf32(t4.w * bv[c0 + 3]));
-        *reinterpret_cast<float4*>(TBb + umma::tile_off(r, c0 * 4, 256)) = f;
-      };
-      // acc[rr][cc] += X[rr][i] Y[i][cc] for i = i0, i0 + step, ... (4 at a time) below i1
-      auto mm44 = [](float (&acc)[4][4], const float* X, int ldx, const float* Y, int ldy, int i0, int i1,
-                     int step) {
-        for (int i = i0; i < i1; i += step) {
-          float xs[4][4];
-  #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const float4 xv = *reinterpret_cast<const float4*>(X + rr * ldx + i);
-            xs[rr][0] = xv.x; xs[rr][1] = xv.y; xs[rr][2] = xv.z; xs[rr][3] = xv.w;
-          }
-  #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 yv = *reinterpret_cast<const float4*>(Y + (i + e) * ldy);
-  #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-              acc[rr][0] = fmaf(xs[rr][e], yv.x, acc[rr][0]);
-              acc[rr][1] = fmaf(xs[rr][e], yv.y, acc[rr][1]);
-              acc[rr][2] = fmaf(xs[rr][e], yv.z, acc[rr][2]);
-              acc[rr][3] = fmaf(xs[rr][e], yv.w, acc[rr][3]);
-            }
-          }
-        }
-      };
-      // sum over the kp partner lanes (lane bits below kp)
-      auto ksum = [](float (&acc)[4][4], int kp) {
-        for (int m = 1; m < kp; m <<= 1)
-  #pragma unroll
-          for (int rr = 0; rr < 4; ++rr)
-  #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], m);
-      };
-      auto row4 = [](const float (&acc)[4][4], int rr) {  // a runtime row of the tile
-        float4 o = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-  #pragma unroll
-        for (int q = 1; q < 4; ++q)
-          if (rr == q) o = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-        return o;
-      };
+      // A product thread owns a 2x2 (16 -> 32) or 4x2 (32 -> 64) tile over half of
+      // the inner index (the partner lane's half is added with shuffles); rows of
+      // the left operand come in 16-byte loads.
       if (tid < kC) {
         const int a = tid >> 4, cc = tid & 15;
         const float* Ab = AM + (16 * a) * kLd + 16 * a;
@@ -634,47 +592,109 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         }
       }
       inv_sync();
-      {  // 16 -> 32: blocks (1,0) and (3,2); threads 0-127 = block x 16 tiles x 4 shares
-        const int blk = tid >> 6, r0 = 4 * ((tid >> 4) & 3), c0 = 4 * ((tid >> 2) & 3), kq = tid & 3;
+      {  // 16 -> 32: blocks (1,0) and (3,2); 256 threads = block x 64 tiles of 2x2 x 2 shares
+        const int kq = tid & 1, c0 = 2 * ((tid >> 1) & 7), r0 = 2 * ((tid >> 4) & 7), blk = tid >> 7;
         const int a = 1 + 2 * blk, b = a - 1;
-        if (tid < 128) {
-          float acc[4][4] = {};
-          mm44(acc, AM + (16 * a + r0) * kLd, kLd, TS + 16 * b + c0, kLd, 16 * b + 4 * kq, 16 * b + 4 * kq + 4, 4);
-          ksum(acc, 4);
-          *reinterpret_cast<float4*>(MS + (16 * blk + r0 + kq) * kMsLd + c0) = row4(acc, kq);
+        // acc[rr][cc] += X[rr][i] Y[i][cc] for i = i0, i0 + 8 below i1 (4 at a time)
+        auto mm22 = [](float (&acc)[2][2], const float* X, int ldx, const float* Y, int ldy, int i0, int i1) {
+#pragma unroll
+          for (int i = i0; i < i1; i += 8) {
+            float xs[2][4];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const float4 xv = *reinterpret_cast<const float4*>(X + rr * ldx + i);
+              xs[rr][0] = xv.x; xs[rr][1] = xv.y; xs[rr][2] = xv.z; xs[rr][3] = xv.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 yv = *reinterpret_cast<const float2*>(Y + (i + e) * ldy);
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                acc[rr][0] = fmaf(xs[rr][e], yv.x, acc[rr][0]);
+                acc[rr][1] = fmaf(xs[rr][e], yv.y, acc[rr][1]);
+              }
+            }
+          }
+        };
+        {
+          float acc[2][2] = {};
+          mm22(acc, AM + (16 * a + r0) * kLd, kLd, TS + 16 * b + c0, kLd, 16 * b + 4 * kq, 16 * a);
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], 1);
+          *reinterpret_cast<float2*>(MS + (16 * blk + r0 + kq) * kMsLd + c0) =
+              kq ? make_float2(acc[1][0], acc[1][1]) : make_float2(acc[0][0], acc[0][1]);
         }
         inv_sync();
-        if (tid < 128) {
-          float acc[4][4] = {};
-          mm44(acc, TS + (16 * a + r0) * kLd + 16 * a, kLd, MS + 16 * blk * kMsLd + c0, kMsLd, 4 * kq, 4 * kq + 4, 4);
-          ksum(acc, 4);
-          const float4 m4 = row4(acc, kq);
-          const float4 t4 = make_float4(-m4.x, -m4.y, -m4.z, -m4.w);
-          *reinterpret_cast<float4*>(TS + (16 * a + r0 + kq) * kLd + 16 * b + c0) = t4;
-          put_tb4(16 * a + r0 + kq, 16 * b + c0, t4);
+        {
+          float acc[2][2] = {};
+          mm22(acc, TS + (16 * a + r0) * kLd + 16 * a, kLd, MS + 16 * blk * kMsLd + c0, kMsLd, 4 * kq, 16);
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], 1);
+          const float t0v = -(kq ? acc[1][0] : acc[0][0]), t1v = -(kq ? acc[1][1] : acc[0][1]);
+          const int r = 16 * a + r0 + kq, cb = 16 * b + c0;
+          *reinterpret_cast<float2*>(TS + r * kLd + cb) = make_float2(t0v, t1v);
+          *reinterpret_cast<float2*>(TBb + umma::tile_off(r, cb * 4, 256)) =
+              make_float2(to_tf32(t0v * bv[cb]), to_tf32(t1v * bv[cb + 1]));
         }
         inv_sync();
       }
-      {  // 32 -> 64: rows 32-63, columns 0-31; threads 0-127 = 64 tiles x 2 shares
-        const int r0 = 4 * (tid >> 4 & 7), c0 = 4 * ((tid >> 1) & 7), kq = tid & 1;
-        if (tid < 128) {
+      {  // 32 -> 64: rows 32-63, columns 0-31; 256 threads = 128 tiles of 4x2 x 2 shares
+        const int kq = tid & 1, c0 = 2 * ((tid >> 1) & 15), r0 = 4 * (tid >> 5);
+        // acc[rr][cc] += X[rr][i] Y[i][cc] for i = i0, i0 + 8, ... below i1 (4 at a time)
+        auto mm42 = [](float (&acc)[4][2], const float* X, int ldx, const float* Y, int ldy, int i0, int i1) {
+#pragma unroll 2
+          for (int i = i0; i < i1; i += 8) {
+            float xs[4][4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const float4 xv = *reinterpret_cast<const float4*>(X + rr * ldx + i);
+              xs[rr][0] = xv.x; xs[rr][1] = xv.y; xs[rr][2] = xv.z; xs[rr][3] = xv.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 yv = *reinterpret_cast<const float2*>(Y + (i + e) * ldy);
+#pragma unroll
+              for (int rr = 0; rr < 4; ++rr) {
+                acc[rr][0] = fmaf(xs[rr][e], yv.x, acc[rr][0]);
+                acc[rr][1] = fmaf(xs[rr][e], yv.y, acc[rr][1]);
+              }
+            }
+          }
+        };
+        auto share2 = [](float (&acc)[4][2]) {  // sum with the partner lane (the other half of i)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], 1);
+        };
+        {
           // M = A[32 + r][0..32) T[0..32)[c..]: T_lo is zero above its block diagonal
-          float acc[4][4] = {};
-          mm44(acc, AM + (32 + r0) * kLd, kLd, TS + c0, kLd, (c0 < 16 ? 0 : 16) + 4 * kq, 32, 8);
-          ksum(acc, 2);
-          *reinterpret_cast<float4*>(MS + (r0 + 2 * kq) * kMsLd + c0) = row4(acc, 2 * kq);
-          *reinterpret_cast<float4*>(MS + (r0 + 2 * kq + 1) * kMsLd + c0) = row4(acc, 2 * kq + 1);
+          float acc[4][2] = {};
+          mm42(acc, AM + (32 + r0) * kLd, kLd, TS + c0, kLd, (c0 < 16 ? 0 : 16) + 4 * kq, 32);
+          share2(acc);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int rr = 2 * kq + h2;  // lane kq writes rows 2kq, 2kq + 1 of the tile
+            *reinterpret_cast<float2*>(MS + (r0 + rr) * kMsLd + c0) =
+                make_float2(kq ? acc[2 + h2][0] : acc[h2][0], kq ? acc[2 + h2][1] : acc[h2][1]);
+          }
         }
         inv_sync();
-        if (tid < 128) {
+        {
           // -T_hi[r][0..32) M[0..32)[c..]: T_hi is zero above its block diagonal
-          float acc[4][4] = {};
-          mm44(acc, TS + (32 + r0) * kLd + 32, kLd, MS + c0, kMsLd, 4 * kq, r0 < 16 ? 16 : 32, 8);
-          ksum(acc, 2);
-  #pragma unroll
+          float acc[4][2] = {};
+          mm42(acc, TS + (32 + r0) * kLd + 32, kLd, MS + c0, kMsLd, 4 * kq, r0 < 16 ? 16 : 32);
+          share2(acc);
+#pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const float4 m4 = row4(acc, 2 * kq + h2);
-            put_tb4(32 + r0 + 2 * kq + h2, c0, make_float4(-m4.x, -m4.y, -m4.z, -m4.w));
+            const int rr = 2 * kq + h2;
+            const float t0v = -(kq ? acc[2 + h2][0] : acc[h2][0]), t1v = -(kq ? acc[2 + h2][1] : acc[h2][1]);
+            *reinterpret_cast<float2*>(TBb + umma::tile_off(32 + r0 + rr, c0 * 4, 256)) =
+                make_float2(to_tf32(t0v * bv[c0]), to_tf32(t1v * bv[c0 + 1]));
           }
         }
       }
