@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (!wait_mma(&bars[4], par)) { ok = false; break; }
     {
       // kind 0 q, 1 k, 2 v; tokens kT0 .. kT0 + kNT of channel d, window w3 running on
-      auto conv_seg = [&](auto kind_c, auto t0_c, auto nt_c, const float4 w, uint16_t (&w3)[3]) {
+      auto conv_seg = [&](auto kind_c, auto t0_c, auto nt_c, const float4 w, float (&w3)[3]) {
         constexpr int kKind = decltype(kind_c)::value, kT0 = decltype(t0_c)::value, kNT = decltype(nt_c)::value;
         const uint16_t* xs = XS + kKind * kC * kHeadDim + d;
         float yv[kKind == 2 ? kNT : 1];
@@ -383,11 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int t = grp * 8 + e;
-            const uint16_t x = xs[t * kHeadDim];
-            float pre = w.x * bf16_to_f32(x);
-            pre = fmaf(w.y, bf16_to_f32(w3[2]), pre);
-            pre = fmaf(w.z, bf16_to_f32(w3[1]), pre);
-            pre = fmaf(w.w, bf16_to_f32(w3[0]), pre);
+            const float x = bf16_to_f32(xs[t * kHeadDim]);
+            float pre = w.x * x;
+            pre = fmaf(w.y, w3[2], pre);
+            pre = fmaf(w.z, w3[1], pre);
+            pre = fmaf(w.w, w3[0], pre);
             ya[e] = t < L ? silu_ftz(pre) : 0.f;
             w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
           }
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         const uint16_t* xs = XS + cset * kC * kHeadDim + d;
         const uint16_t nw[3] = {L >= 3 ? xs[(L - 3) * kHeadDim] : (L == 2 ? hw[2] : hw[1]),
                                 L >= 2 ? xs[(L - 2) * kHeadDim] : hw[2], xs[(L - 1) * kHeadDim]};
-        uint16_t w3[3] = {hw[0], hw[1], hw[2]};
+        float w3[3] = {bf16_to_f32(hw[0]), bf16_to_f32(hw[1]), bf16_to_f32(hw[2])};
         if (cset == 0) {
           conv_seg(I0{}, I0{}, I32{}, wq, w3);
           conv_seg(I0{}, I32{}, I16{}, wq, w3);
@@ -449,14 +449,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         }
         hw[0] = nw[0]; hw[1] = nw[1]; hw[2] = nw[2];
       } else {
+        auto win45 = [&](const uint16_t* x, float (&w3)[3]) {  // raw rows 45-47
+          w3[0] = bf16_to_f32(x[45 * kHeadDim]);
+          w3[1] = bf16_to_f32(x[46 * kHeadDim]);
+          w3[2] = bf16_to_f32(x[47 * kHeadDim]);
+        };
+        float w3[3], w4[3], w5[3];
         const uint16_t* xq = XS + d;
-        uint16_t w3[3] = {xq[45 * kHeadDim], xq[46 * kHeadDim], xq[47 * kHeadDim]};
+        win45(xq, w3);
         conv_seg(I0{}, I48{}, I16{}, wq, w3);
-        const uint16_t* xk = xq + kC * kHeadDim;
-        uint16_t w4[3] = {xk[45 * kHeadDim], xk[46 * kHeadDim], xk[47 * kHeadDim]};
+        win45(xq + kC * kHeadDim, w4);
         conv_seg(I1{}, I48{}, I16{}, wk, w4);
-        const uint16_t* xv = xk + kC * kHeadDim;
-        uint16_t w5[3] = {xv[45 * kHeadDim], xv[46 * kHeadDim], xv[47 * kHeadDim]};
+        win45(xq + 2 * kC * kHeadDim, w5);
         conv_seg(I2{}, I48{}, I16{}, wv, w5);
       }
     }
