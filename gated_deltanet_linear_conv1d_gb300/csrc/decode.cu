@@ -69,7 +69,7 @@ struct Layout {
     v = rest;        rest += G * P * kHeadDim * 4;          // [G][P][128] fp32
     o = rest;        rest += G * P * kHeadDim * 4;          // [G][P][128] fp32
     red = rest;      rest += (P * 16 + G * P * 4) * 4;      // [P][16] norm and [G*P][4] RMS partial sums
-    ab = rest;       rest += kMaxGroup * kMaxPos * 4 * 4;   // [G][P][4] alpha, beta
+    ab = rest;       rest += kMaxGroup * kMaxPos * 4 * 4 + kMaxPos * 4;  // [G][P][4] alpha, beta; [P] output slots
     bars = rest;     rest += (2 * kMaxStages + 4) * 8 + 16; // mbarriers + abort flag
     stages = (kSmemLimit - rest) / (int)kHalfBytes;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -214,14 +214,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
   const int ctid = tid;  // 0 .. kConsumers-1
   const uint64_t wpol = l2_policy_evict_first();
   float* rms_part = red + P * 16;  // [G*P][4]
+  int* out_slot = reinterpret_cast<int*>(ab + kMaxGroup * kMaxPos * 4);  // [P] slot written after position q
   bool dead = false;
   int t = 0, kin = 0;
   // the next unit's slot and (threads < G*P) its alpha, beta are loaded one unit ahead
-  int slot_nx = -1;
+  int slot_nx = -1, oslot_nx = -1;
   float a_nx = 0.f, b_nx = 0.f;
   auto prefetch = [&](int i) {
     const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
     slot_nx = p.slot_idx[n];
+    if (p.spec_slot && ctid < P) oslot_nx = p.spec_slot[n * P + ctid];
     if (ctid < G * P) {
       const size_t ai = (size_t)(n * P + ctid % P) * p.Hv + G * j + ctid / P;
       a_nx = p.alpha[ai];
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
   if (nunits > 0) prefetch(0);
   for (int i = 0; i < nunits; ++i) {
     const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
-    const int slot = slot_nx;
+    const int slot = slot_nx, oslot_cur = oslot_nx;
     const float a_cur = a_nx, b_cur = b_nx;
     if (i + 1 < nunits) prefetch(i + 1);
     if (slot < 0 || slot >= p.Rs || (p.spec_slot && !unit_slots_ok(p, n))) {
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
       ab[ctid * 4 + 0] = a_cur;  // [g][q] with g = ctid / P, q = ctid % P
       ab[ctid * 4 + 1] = b_cur;
     }
+    if (ctid < P) out_slot[ctid] = p.spec_slot ? oslot_cur : slot;
     dead = dead || *abort_flag;
     if (!dead && !mbar_wait_bounded(&in_full[b], (kin >> 1) & 1)) {
       dead = true;
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
             }
             const float e = vs[(g * P + q) * kHeadDim + ri] - a * pk;  // v - Sbar k
             const float be = bb * e;
-            const int oslot = p.spec_slot ? p.spec_slot[n * P + q] : slot;
+            const int oslot = out_slot[q];
             float* grow = p.state + (((size_t)oslot * p.Hv + h) * kHeadDim + ri) * kHeadDim;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
