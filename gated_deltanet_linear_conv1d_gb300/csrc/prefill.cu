@@ -78,7 +78,7 @@ constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
 constexpr int kZS1 = kPB + 8192;        // bf16 [64][128]: the same for odd chunks
 constexpr int kSmall = kZS1 + 16384;    // small per-chunk vectors
-constexpr int kSmallFloats = 64 * 7 + 4 * 64;
+constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 3 + 4 * 64;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
 
@@ -221,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   unsigned char* TBb = smem + kTB;
   unsigned char* PBb = smem + kPB;
   float* small = reinterpret_cast<float*>(smem + kSmall);
-  float* gv = small;             // [64] g / ln 2 (cumulative log2 of alpha)
-  float* egv = gv + 64;          // [64] e^g
-  float* glv = egv + 64;         // [64] e^{g_C - g_t} (0 past the chunk end)
-  float* bv = glv + 64;          // [64] beta
-  float* iqv = bv + 64;          // [64] 1/|q|
+  // per-chunk gate vectors, double-buffered by chunk parity (chunk c + 1's are
+  // computed while chunk c runs): [64] g / ln 2 (cumulative log2 of alpha), [64]
+  // e^g, [64] e^{g_C - g_t} (0 past the chunk end), [64] beta
+  float* gates = small;          // [2][4][64]
+  float* iqv = gates + 2 * 4 * 64;  // [64] 1/|q|
   float* ikv = iqv + 64;         // [64] 1/|k|
   float* rinv = ikv + 64;        // [64] gate 1/rms
   float* rpart = rinv + 64;      // [4][64] gate partials
@@ -311,18 +311,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const int first = min(kC - p0 % kC, t1 - t0);
   const int nchunks = 1 + (t1 - t0 - first + kC - 1) / kC;
   bool ok = true;
-  // alpha and beta of the next chunk are loaded one chunk ahead (thread t: token t)
-  // (warp 0, lane l: tokens l and l + 32 of the chunk)
+  // ---- gates of a chunk (warp 15, two tokens per lane, no CTA barrier): g =
+  // inclusive cumsum of log2(alpha) (so e^{g ln 2} = prod alpha), e^g,
+  // e^{g_C - g_t}, beta. The chunk's alpha and beta sit in the lanes' registers,
+  // loaded one chunk before they are needed.
+  constexpr int kGateWarp = kThreads / 32 - 1;
   float alpha_n0 = 1.f, beta_n0 = 0.f, alpha_n1 = 1.f, beta_n1 = 0.f;
-  if (warp == 0) {
-    if (lane < first) {
-      alpha_n0 = p.alpha[(size_t)(t0 + lane) * p.Hv + h];
-      beta_n0 = p.beta[(size_t)(t0 + lane) * p.Hv + h];
+  auto load_ab = [&](int ts, int len) {  // alpha, beta of tokens ts .. ts + len - 1
+    if (lane < len) {
+      alpha_n0 = p.alpha[(size_t)(ts + lane) * p.Hv + h];
+      beta_n0 = p.beta[(size_t)(ts + lane) * p.Hv + h];
     }
-    if (lane + 32 < first) {
-      alpha_n1 = p.alpha[(size_t)(t0 + lane + 32) * p.Hv + h];
-      beta_n1 = p.beta[(size_t)(t0 + lane + 32) * p.Hv + h];
+    if (lane + 32 < len) {
+      alpha_n1 = p.alpha[(size_t)(ts + lane + 32) * p.Hv + h];
+      beta_n1 = p.beta[(size_t)(ts + lane + 32) * p.Hv + h];
     }
+  };
+  auto make_gates = [&](float* gb, int len) {
+    float* g_ = gb;
+    float* eg = gb + 64;
+    float* gl_ = gb + 128;
+    float* b_ = gb + 192;
+    const float la0 = lane < len ? fmaxf(lg2(alpha_n0), -115.f) : 0.f;  // alpha in (0, 1]
+    const float la1 = lane + 32 < len ? fmaxf(lg2(alpha_n1), -115.f) : 0.f;
+    b_[lane] = lane < len ? beta_n0 : 0.f;
+    b_[lane + 32] = lane + 32 < len ? beta_n1 : 0.f;
+    float s0 = la0, s1 = la1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u0 = __shfl_up_sync(0xffffffffu, s0, o), u1 = __shfl_up_sync(0xffffffffu, s1, o);
+      if (lane >= o) {
+        s0 += u0;
+        s1 += u1;
+      }
+    }
+    s1 += __shfl_sync(0xffffffffu, s0, 31);
+    const float gl = __shfl_sync(0xffffffffu, len - 1 < 32 ? s0 : s1, (len - 1) & 31);  // g at the chunk end
+    g_[lane] = s0;
+    g_[lane + 32] = s1;
+    eg[lane] = ex2(s0);
+    eg[lane + 32] = ex2(s1);
+    gl_[lane] = lane < len ? ex2(gl - s0) : 0.f;
+    gl_[lane + 32] = lane + 32 < len ? ex2(gl - s1) : 0.f;
+  };
+  if (warp == kGateWarp) {  // chunk 0's gates now, chunk 1's alpha and beta into the registers
+    load_ab(t0, first);
+    make_gates(gates, first);
+    if (nchunks > 1) load_ab(t0 + first, min(kC, t1 - t0 - first));
   }
   int tc = t0, L = first;  // this chunk: tokens tc .. tc + L - 1
   for (int c = 0; c < nchunks && ok; ++c, tc += L, L = min(kC, t1 - tc)) {
@@ -330,40 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 
     uint16_t* const ZS = zs_buf(c & 1);  // this chunk's z rows (TMA issued one chunk ahead)
 
-    // ---- gates (warp 0, two tokens per lane, no CTA barrier): g = inclusive
-    // cumsum of log2(alpha) (so e^{g ln 2} = prod alpha), e^g, e^{g_C - g_t}, beta
-    if (warp == 0) {
-      const float la0 = lane < L ? fmaxf(lg2(alpha_n0), -115.f) : 0.f;  // alpha in (0, 1]
-      const float la1 = lane + 32 < L ? fmaxf(lg2(alpha_n1), -115.f) : 0.f;
-      bv[lane] = lane < L ? beta_n0 : 0.f;
-      bv[lane + 32] = lane + 32 < L ? beta_n1 : 0.f;
-      const int nl = c + 1 < nchunks ? min(kC, t1 - tc - L) : 0;  // next chunk, loaded ahead
-      if (lane < nl) {
-        alpha_n0 = p.alpha[(size_t)(tc + L + lane) * p.Hv + h];
-        beta_n0 = p.beta[(size_t)(tc + L + lane) * p.Hv + h];
-      }
-      if (lane + 32 < nl) {
-        alpha_n1 = p.alpha[(size_t)(tc + L + lane + 32) * p.Hv + h];
-        beta_n1 = p.beta[(size_t)(tc + L + lane + 32) * p.Hv + h];
-      }
-      float s0 = la0, s1 = la1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u0 = __shfl_up_sync(0xffffffffu, s0, o), u1 = __shfl_up_sync(0xffffffffu, s1, o);
-        if (lane >= o) {
-          s0 += u0;
-          s1 += u1;
-        }
-      }
-      s1 += __shfl_sync(0xffffffffu, s0, 31);
-      const float gl = __shfl_sync(0xffffffffu, L - 1 < 32 ? s0 : s1, (L - 1) & 31);  // g at the chunk end
-      gv[lane] = s0;
-      gv[lane + 32] = s1;
-      egv[lane] = ex2(s0);
-      egv[lane + 32] = ex2(s1);
-      glv[lane] = lane < L ? ex2(gl - s0) : 0.f;
-      glv[lane + 32] = lane + 32 < L ? ex2(gl - s1) : 0.f;
-    }
+    // this chunk's gate vectors (written before the loop or during the previous chunk)
+    const float* gv = gates + (c & 1) * 256;
+    const float* egv = gv + 64;
+    const float* glv = gv + 128;
+    const float* bv = gv + 192;
 
     // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time; q, k
     // written channel-major to shared memory, v to tensor memory. Every token
@@ -724,6 +730,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (c0 + q4 * 4) * 4, 256)) =
               make_float4(y4[0], y4[1], y4[2], y4[3]);
         }
+      }
+      // the next chunk's gates while the inverse runs (published by the barrier below),
+      // and the alpha, beta of the one after into the registers
+      if (warp == kGateWarp && c + 1 < nchunks) {
+        const int tn = tc + L, ln = min(kC, t1 - tn);
+        make_gates(gates + ((c + 1) & 1) * 256, ln);
+        if (c + 2 < nchunks) load_ab(tn + ln, min(kC, t1 - tn - ln));
       }
     }
     umma::fence_proxy_async_smem();
