@@ -1012,6 +1012,7 @@ cudaError_t static_prefill_order(int32_t** out) {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;  // every request is empty: nothing is read or written
   CUtensorMap tmx{}, tmz{}, tmo{};
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.CH, (cuuint64_t)a.T};

@@ -153,6 +153,7 @@ gdn_status gdn_decode_step(const gdn_dims *dims, const uint16_t *qkv0, const flo
  *   alpha, beta [T][Hv] fp32;  z [T][Hv][dv] bf16 or NULL (then ogate must be
  *             NULL);  gamma [dv];  eps
  *   o [T][Hv][dv] bf16 or NULL;  ogate [T][Hv*dv] bf16 or NULL (not both NULL)
+ *   num_tokens 0: every request is empty; nothing is read or written.
  *   workspace, workspace_bytes: device scratch of at least
  *             gdn_prefill_workspace_bytes(dims, N, T) bytes, 256-byte aligned.
  *             Contents need not be zeroed and are clobbered: the call writes

@@ -287,6 +287,22 @@ def test_prefill_then_decode_continues_the_request(b):
     np.testing.assert_array_equal(U.host_bits(d["conv_hist"][slot]), full["conv_hist"][0])
 
 
+def test_prefill_with_no_tokens_touches_nothing(b):
+    """N requests, all empty (T = 0): the call succeeds and every slot is left as it was."""
+    dims = synth.RANK_HEADS
+    w = synth.prefill_workload(dims, [0, 0, 0], seed=57)
+    d = U.to_device(w)
+    D = b.make_dims(dims, w["num_slots"])
+    err = _dev_err()
+    og = torch.zeros((0, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    b.gdn_chunk_prefill(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["query_start_loc"], d["slot_idx"],
+                        d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og, has_init=d["has_init"],
+                        dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    np.testing.assert_array_equal(d["state"].cpu().numpy(), w["state"])
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"]), w["conv_hist"])
+
+
 def test_prefill_bad_offsets_are_flagged(b):
     geom = synth.RANK_HEADS
     w = synth.prefill_workload(geom, [5, 7], seed=52)
