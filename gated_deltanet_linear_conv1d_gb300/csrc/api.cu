@@ -195,7 +195,8 @@ gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const floa
   if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
   if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
   if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
-  if (num_tokens > 0 && (!qkv0 || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return GDN_OK;  // every request is empty: nothing is read or written
+  if (!qkv0 || !alpha || !beta) return GDN_ERR_INVALID_ARG;
   if (!o && !ogate) return GDN_ERR_INVALID_ARG;
   if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
   if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
@@ -226,7 +227,8 @@ gdn_status gdn_chunk_prefill_align(const gdn_dims* d, const uint16_t* qkv0, cons
     return GDN_ERR_INVALID_ARG;
   if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
   if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
-  if (num_tokens > 0 && (!qkv0 || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return GDN_OK;  // every request is empty: nothing is read or written
+  if (!qkv0 || !alpha || !beta) return GDN_ERR_INVALID_ARG;
   if (!o && !ogate) return GDN_ERR_INVALID_ARG;
   if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
   if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
@@ -256,7 +258,8 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
   if (num_seqs > gdn::kStaticPrefillMaxSeqs) return GDN_ERR_INVALID_ARG;  // beyond the fixed schedule array
   if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
   if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
-  if (num_tokens > 0 && (!qkv0 || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return GDN_OK;  // every request is empty: nothing is read or written
+  if (!qkv0 || !alpha || !beta) return GDN_ERR_INVALID_ARG;
   if (!o && !ogate) return GDN_ERR_INVALID_ARG;
   if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
   if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
