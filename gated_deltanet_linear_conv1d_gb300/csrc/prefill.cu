@@ -78,7 +78,7 @@ constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
 constexpr int kZS1 = kPB + 8192;        // bf16 [64][128]: the same for odd chunks
 constexpr int kSmall = kZS1 + 16384;    // small per-chunk vectors
-constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 3 + 4 * 64;
+constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 2 + 4 * 64;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
 
@@ -227,8 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* gates = small;          // [2][4][64]
   float* iqv = gates + 2 * 4 * 64;  // [64] 1/|q|
   float* ikv = iqv + 64;         // [64] 1/|k|
-  float* rinv = ikv + 64;        // [64] gate 1/rms
-  float* rpart = rinv + 64;      // [4][64] gate partials
+  float* rpart = ikv + 64;       // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
   // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5, 6: z rows
   // of even / odd chunks
@@ -359,6 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     make_gates(gates, first);
     if (nchunks > 1) load_ab(t0 + first, min(kC, t1 - t0 - first));
   }
+  // Ogate rows of a chunk waiting to be stored (TMA thread): a full chunk with one
+  // tensor copy, a partial one row by row so that the next request's rows are
+  // not touched. Issued after the CTA barrier that follows the rows' writes.
+  int st_tc = -1, st_len = 0, st_buf = 0;
+  auto store_pending = [&]() {
+    if (st_tc < 0) return;
+    const uint16_t* zsb = zs_buf(st_buf);
+    if (st_len == kC) {
+      tma_store_3d(&tmo, 0, h, st_tc, zsb);
+    } else {
+      for (int t = 0; t < st_len; ++t)
+        bulk_s2g(p.ogate + ((size_t)(st_tc + t) * p.Hv + h) * kHeadDim, zsb + t * kHeadDim, 256);
+    }
+    bulk_commit();
+    st_tc = -1;
+  };
   int tc = t0, L = first;  // this chunk: tokens tc .. tc + L - 1
   for (int c = 0; c < nchunks && ok; ++c, tc += L, L = min(kC, t1 - tc)) {
     const uint32_t par = c & 1;
@@ -376,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // row of the staging area is valid to read (rows past T arrive as zeros), so
     // the loop runs branch-free and masks outputs past the chunk end.
     if (!wait_mma(&bars[4], par)) { ok = false; break; }
+    if (tid == kTmaThread) store_pending();  // the previous chunk's Ogate rows
     {
       // kind 0 q, 1 k, 2 v; tokens kT0 .. kT0 + kNT of channel d, window w3 running on
       auto conv_seg = [&](auto kind_c, auto t0_c, auto nt_c, const float4 w, float (&w3)[3]) {
@@ -819,12 +835,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         if ((lane & 3) == 0) rpart[quarter * 64 + part * 16 + q8 * 8 + tok8(lane)] = tot;
       }
     }
-    __syncthreads();
-    if (tid < kC)
-      rinv[tid] = rsqrtf(((rpart[tid] + rpart[64 + tid]) + (rpart[128 + tid] + rpart[192 + tid])) *
-                             (1.0f / kHeadDim) + p.eps);
-    if (want_gate && !wait_mma(&bars[5 + (c & 1)], (c >> 1) & 1)) { ok = false; break; }  // z rows landed (also syncs)
-    if (!want_gate) __syncthreads();
+    // one barrier: the RMS partials are published and (when gating) the z rows have landed
+    if (want_gate) {
+      if (!wait_mma(&bars[5 + (c & 1)], (c >> 1) & 1)) { ok = false; break; }
+    } else {
+      __syncthreads();
+    }
+    // 1/rms of this warp's 16 tokens: lane e < 16 takes token 16 part + e (shuffled out below)
+    float rinv_l = 0.f;
+    if (lane < 16) {
+      const int t = part * 16 + lane;
+      rinv_l = rsqrtf(((rpart[t] + rpart[64 + t]) + (rpart[128 + t] + rpart[192 + t])) * (1.0f / kHeadDim) + p.eps);
+    }
     {
       if (p.o) {
 #pragma unroll
@@ -840,23 +862,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         for (int e = 0; e < 16; ++e) {
           const int t = part * 16 + e;
           uint16_t* zp = ZS + t * kHeadDim + row;
-          *zp = f32_to_bf16(ov[e] * rinv[t] * gm * silu_ftz(bf16_to_f32(*zp)));
+          const float rinv = __shfl_sync(0xffffffffu, rinv_l, e);
+          *zp = f32_to_bf16(ov[e] * rinv * gm * silu_ftz(bf16_to_f32(*zp)));
         }
       }
     }
+    // ... then stored with one tensor copy after the next CTA barrier (the next
+    // chunk's first, or the one after the loop), which the rows' writes precede
     umma::fence_proxy_async_smem();
-    __syncthreads();
-    // ... then stored with one tensor copy (a partial last chunk row by row, so
-    // that the next request's rows are not touched); the next chunk's z rows
-    // wait until these stores have read ZS
     if (tid == kTmaThread && want_gate) {
-      if (L == kC) {
-        tma_store_3d(&tmo, 0, h, tc, ZS);
-      } else {
-        for (int t = 0; t < L; ++t)
-          bulk_s2g(p.ogate + ((size_t)(tc + t) * p.Hv + h) * kHeadDim, ZS + t * kHeadDim, 256);
-      }
-      bulk_commit();
+      st_tc = tc;
+      st_len = L;
+      st_buf = c & 1;
     }
     // ---- align mode: after an absolute multiple of the block, the state (tensor
     // memory, updated by this chunk's MMAs) and the conv windows go to a snapshot slot
@@ -883,6 +900,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     }
   }
 
+  __syncthreads();  // the last chunk's Ogate rows are written
+  if (ok && tid == kTmaThread) store_pending();
   if (ok) {
     // ---- final state back to the slot, history to the owners' channels
     float* dst = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + part * 32;
