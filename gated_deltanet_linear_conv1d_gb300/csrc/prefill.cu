@@ -61,23 +61,24 @@ constexpr int kKQ = 0;                  // bf16 [128 dk][128 t]: k tokens 0-63, 
 constexpr int kKG = kKQ + 32768;        // bf16 [128 dk][64 t]: k e^g (MN-major B)      | later E bf16 [128 dv][64 t]
 constexpr int kKT = kKG + 16384;        // tf32 [128 dk][64 t]: raw k (K-major B)
 constexpr int kS0 = kKT + 32768;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
-// Scratch: raw QKV0 rows of a chunk [3 parts][64 t][128] bf16 (bulk-copied, read by
-// the conv), later the inverse's A [64][68], T [64][68] and block products [3][16][20];
-// then the raw rows of the next chunk. Its tail holds the chunk's z rows [64][128]
-// bf16, overwritten in place by Ogate before they are bulk-stored.
+// Scratch: raw q and k rows of a chunk [2 parts][64 t][128] bf16 (TMA, read by
+// the conv), later the inverse's A [64][68], T [64][68] and block products
+// [32][36]; then the q and k rows of the next chunk.
 constexpr int kSCR = kS0 + 32768;
-constexpr int kXS = kSCR;               // raw QKV0 rows, 49152 B
+constexpr int kScrBytes = 40960;
+constexpr int kXS = kSCR;               // raw q, k rows, 32768 B
 constexpr int kLd = 68;                 // row stride (floats) of A and T: 16-byte aligned rows
 constexpr int kMsLd = 36;               // row stride (floats) of the inverse's block products
 constexpr int kAM = kSCR;               // fp32 [64][kLd]
 constexpr int kTS = kAM + 64 * kLd * 4;  // fp32 [64][kLd]
 constexpr int kMS = kTS + 64 * kLd * 4;  // fp32 [32][kMsLd]
-static_assert(kMS + 32 * kMsLd * 4 <= kSCR + 49152, "inverse scratch overlaps the z rows");
-constexpr int kZS = kSCR + 49152;       // bf16 [64][128]: z rows, then Ogate rows (even chunks)
-constexpr int kTB = kSCR + 65536;       // tf32 [64 r][64 i]: T diag(b) (K-major B)
+static_assert(kMS + 32 * kMsLd * 4 <= kSCR + kScrBytes, "inverse scratch overruns its region");
+static_assert(2 * kC * kHeadDim * 2 <= kScrBytes, "q, k rows overrun the scratch region");
+constexpr int kXV = kSCR + kScrBytes;   // bf16 [64 t][128]: raw v rows of the next chunk (TMA)
+constexpr int kZS = kXV + 16384;        // bf16 [64][128]: z rows, then Ogate rows
+constexpr int kTB = kZS + 16384;        // tf32 [64 r][64 i]: T diag(b) (K-major B)
 constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
-constexpr int kZS1 = kPB + 8192;        // bf16 [64][128]: the same for odd chunks
-constexpr int kSmall = kZS1 + 16384;    // small per-chunk vectors
+constexpr int kSmall = kPB + 8192;      // small per-chunk vectors
 constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 2 + 4 * 64;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
@@ -214,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   unsigned char* KGb = smem + kKG;
   unsigned char* KTb = smem + kKT;
   const uint16_t* XS = reinterpret_cast<const uint16_t*>(smem + kXS);
-  auto zs_buf = [&](int zb) { return reinterpret_cast<uint16_t*>(smem + (zb ? kZS1 : kZS)); };
+  uint16_t* const ZS = reinterpret_cast<uint16_t*>(smem + kZS);
+  const uint16_t* XV = reinterpret_cast<const uint16_t*>(smem + kXV);
   unsigned char* S0b = smem + kS0;
   float* AM = reinterpret_cast<float*>(smem + kAM);
   float* TS = reinterpret_cast<float*>(smem + kTS);
@@ -229,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* ikv = iqv + 64;         // [64] 1/|k|
   float* rpart = ikv + 64;       // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
-  // MMA completions 0: [K;Q]K^T  1: X,Z  2: E  3: S, O';  copies 4: raw QKV0 rows  5, 6: z rows
-  // of even / odd chunks
+  // MMA completions 0: [K;Q][K;Q]^T  1: X,Z  2: E  3: S, O';  copies 4: raw q, k rows
+  // 5: z rows  6: raw v rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
   const bool want_gate = p.ogate != nullptr;
@@ -238,31 +240,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   // token tcs) into the scratch area. Rows past the request are masked by the
   // conv; rows past T arrive as zeros.
   auto issue_x = [&](int tcs) {
-    mbar_arrive_expect_tx(&bars[4], (uint32_t)(3 * kC * kHeadDim * 2));
+    mbar_arrive_expect_tx(&bars[4], (uint32_t)(2 * kC * kHeadDim * 2));
     tma_load_2d(smem + kXS + 0 * kC * 256, &tmx, j * kHeadDim, tcs, &bars[4]);
     tma_load_2d(smem + kXS + 1 * kC * 256, &tmx, (p.Hk + j) * kHeadDim, tcs, &bars[4]);
-    tma_load_2d(smem + kXS + 2 * kC * 256, &tmx, (2 * p.Hk + h) * kHeadDim, tcs, &bars[4]);
+  };
+  // The v rows of the chunk starting at token tcs into XV (their conv runs one chunk early).
+  auto issue_v = [&](int tcs) {
+    mbar_arrive_expect_tx(&bars[6], (uint32_t)(kC * kHeadDim * 2));
+    tma_load_2d(smem + kXV, &tmx, (2 * p.Hk + h) * kHeadDim, tcs, &bars[6]);
   };
   // Thread 0: TMA the z rows of the chunk starting at token tcs into buffer zb.
-  auto issue_z = [&](int tcs, int zb) {
-    mbar_arrive_expect_tx(&bars[5 + zb], (uint32_t)(kC * kHeadDim * 2));
-    tma_load_3d(zs_buf(zb), &tmz, 0, h, tcs, &bars[5 + zb]);
+  auto issue_z = [&](int tcs) {
+    mbar_arrive_expect_tx(&bars[5], (uint32_t)(kC * kHeadDim * 2));
+    tma_load_3d(ZS, &tmz, 0, h, tcs, &bars[5]);
   };
 
-  // ---- conv channel d = row of this thread: warps 0-3 q, 4-7 k, 8-11 v for the
-  // first 48 tokens of every chunk (each carries its channel's running window),
-  // warps 12-15 all three for the last 16 tokens
-  const int cset = part;
+  // ---- conv work of this thread. q and k at the start of every chunk: thread t
+  // takes channel t % 256 (q below 128, k above) for tokens 32 (t / 256) .. + 31.
+  // v one chunk early, during the previous chunk's triangular inverse: warps
+  // 8-15, channel d = row (its tensor-memory lane), tokens 32 (part - 2) .. + 31.
   const int d = row;
-  const int gq = j * kHeadDim + d, gk = (p.Hk + j) * kHeadDim + d, gvc = (2 * p.Hk + h) * kHeadDim + d;
-  const float4 wq = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gq * kTaps);
-  const float4 wk = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gk * kTaps);
+  const int qch = tid & 255, dq = qch & 127, qhalf = tid >> 8;
+  const bool isq = qch < 128;
+  const int gqk = isq ? j * kHeadDim + dq : (p.Hk + j) * kHeadDim + dq;
+  const float4 wqk = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gqk * kTaps);
+  const int gvc = (2 * p.Hk + h) * kHeadDim + d;
   const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gvc * kTaps);
-  const int gown = cset == 0 ? gq : (cset == 1 ? gk : gvc);
-  uint16_t hw[3] = {0, 0, 0};  // running window (raw inputs, oldest first) of warps 0-11
-  if (init && cset < 3) {
-    const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gown) * 3;
-    hw[0] = hp[0]; hw[1] = hp[1]; hw[2] = hp[2];
+  const bool own_qk = qhalf == 0;  // carries channel qch's running q/k window
+  const bool own_v = part == 2;    // carries channel d's running v window
+  // running windows (raw inputs, oldest first); hv_end is the v window at the end
+  // of the current chunk once hv has moved on to the next one
+  uint16_t hqk[3] = {0, 0, 0}, hv[3] = {0, 0, 0}, hv_end[3] = {0, 0, 0};
+  if (init) {
+    if (own_qk) {
+      const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gqk) * 3;
+      hqk[0] = hp[0]; hqk[1] = hp[1]; hqk[2] = hp[2];
+    }
+    if (own_v) {
+      const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gvc) * 3;
+      hv[0] = hp[0]; hv[1] = hp[1]; hv[2] = hp[2];
+    }
   }
 
   if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
@@ -270,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     for (int b = 0; b < 7; ++b) mbar_init(&bars[b], 1);
     fence_mbar_init();
     issue_x(t0);  // raw rows of the first chunk
-    if (want_gate) issue_z(t0, 0);
+    issue_v(t0);
+    if (want_gate) issue_z(t0);
   }
   // T diag(beta) above the block diagonal stays zero; the rest is rewritten per chunk
   for (int it = tid; it < kC * kC / 4; it += kThreads)
@@ -361,10 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   // Ogate rows of a chunk waiting to be stored (TMA thread): a full chunk with one
   // tensor copy, a partial one row by row so that the next request's rows are
   // not touched. Issued after the CTA barrier that follows the rows' writes.
-  int st_tc = -1, st_len = 0, st_buf = 0;
+  int st_tc = -1, st_len = 0;
   auto store_pending = [&]() {
     if (st_tc < 0) return;
-    const uint16_t* zsb = zs_buf(st_buf);
+    const uint16_t* zsb = ZS;
     if (st_len == kC) {
       tma_store_3d(&tmo, 0, h, st_tc, zsb);
     } else {
@@ -374,11 +392,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     bulk_commit();
     st_tc = -1;
   };
+  // the window carried past a chunk of len tokens: raw rows len-3 .. len-1,
+  // reaching back into the previous window when the chunk is shorter than 3
+  auto next_window = [&](const uint16_t* x, const uint16_t (&w)[3], uint16_t (&nw)[3], int len) {
+    nw[0] = len >= 3 ? x[(len - 3) * kHeadDim] : (len == 2 ? w[2] : w[1]);
+    nw[1] = len >= 2 ? x[(len - 2) * kHeadDim] : w[2];
+    nw[2] = x[(len - 1) * kHeadDim];
+  };
+  // ---- v conv + SiLU of the chunk whose raw v rows are in XV (len tokens), into
+  // tensor memory (warps 8-15; the caller has waited for XV)
+  auto v_conv = [&](int len) {
+    const uint16_t* xv = XV + d;
+    const int tb = 32 * (part - 2);
+    float w3[3];
+    if (own_v) {
+      w3[0] = bf16_to_f32(hv[0]); w3[1] = bf16_to_f32(hv[1]); w3[2] = bf16_to_f32(hv[2]);
+    } else {
+      w3[0] = bf16_to_f32(xv[29 * kHeadDim]); w3[1] = bf16_to_f32(xv[30 * kHeadDim]);
+      w3[2] = bf16_to_f32(xv[31 * kHeadDim]);
+    }
+    float yv[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int t = tb + e;
+      const float x = bf16_to_f32(xv[t * kHeadDim]);
+      float pre = wv.x * x;
+      pre = fmaf(wv.y, w3[2], pre);
+      pre = fmaf(wv.z, w3[1], pre);
+      pre = fmaf(wv.w, w3[0], pre);
+      yv[e] = t < len ? silu_ftz(pre) : 0.f;
+      w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
+    }
+    umma::st32_nowait(tm + lane_base + kT_V + tb, yv);  // v row d = this thread's lane
+    umma::wait_st();
+    if (own_v) {
+      uint16_t nw[3];
+      next_window(xv, hv, nw, len);
+      hv_end[0] = hv[0]; hv_end[1] = hv[1]; hv_end[2] = hv[2];
+      hv[0] = nw[0]; hv[1] = nw[1]; hv[2] = nw[2];
+    }
+  };
+  if (warp >= 8) {  // chunk 0's v
+    if (!mbar_wait_bounded(&bars[6], 0)) ok = false;
+    if (ok) v_conv(first);
+  }
+  if (!__syncthreads_and(ok ? 1 : 0)) ok = false;
   int tc = t0, L = first;  // this chunk: tokens tc .. tc + L - 1
   for (int c = 0; c < nchunks && ok; ++c, tc += L, L = min(kC, t1 - tc)) {
     const uint32_t par = c & 1;
 
-    uint16_t* const ZS = zs_buf(c & 1);  // this chunk's z rows (TMA issued one chunk ahead)
 
     // this chunk's gate vectors (written before the loop or during the previous chunk)
     const float* gv = gates + (c & 1) * 256;
@@ -386,107 +448,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     const float* glv = gv + 128;
     const float* bv = gv + 192;
 
-    // ---- conv + SiLU from the bulk-copied raw rows, 8 tokens at a time; q, k
-    // written channel-major to shared memory, v to tensor memory. Every token
-    // row of the staging area is valid to read (rows past T arrive as zeros), so
-    // the loop runs branch-free and masks outputs past the chunk end.
+    // ---- conv + SiLU of q and k from the TMA-staged raw rows, written
+    // channel-major to shared memory (v was done during the previous chunk).
+    // Every token row of the staging area is valid to read (rows past T arrive
+    // as zeros), so the loop runs branch-free and masks outputs past the chunk end.
     if (!wait_mma(&bars[4], par)) { ok = false; break; }
-    if (tid == kTmaThread) store_pending();  // the previous chunk's Ogate rows
+    if (tid == kTmaThread) {
+      store_pending();  // the previous chunk's Ogate rows
+      if (want_gate && c > 0) {
+        bulk_wait_read_all();  // ... have been read out of ZS: this chunk's z rows may land
+        issue_z(tc);
+      }
+      if (c + 1 < nchunks) issue_v(tc + L);  // XV is free: the v rows of the next chunk
+    }
     {
-      // kind 0 q, 1 k, 2 v; tokens kT0 .. kT0 + kNT of channel d, window w3 running on
-      auto conv_seg = [&](auto kind_c, auto t0_c, auto nt_c, const float4 w, float (&w3)[3]) {
-        constexpr int kKind = decltype(kind_c)::value, kT0 = decltype(t0_c)::value, kNT = decltype(nt_c)::value;
-        const uint16_t* xs = XS + kKind * kC * kHeadDim + d;
-        float yv[kKind == 2 ? kNT : 1];
-#pragma unroll
-        for (int gi = 0; gi < kNT / 8; ++gi) {
-          const int grp = kT0 / 8 + gi;
-          float ya[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int t = grp * 8 + e;
-            const float x = bf16_to_f32(xs[t * kHeadDim]);
-            float pre = w.x * x;
-            pre = fmaf(w.y, w3[2], pre);
-            pre = fmaf(w.z, w3[1], pre);
-            pre = fmaf(w.w, w3[0], pre);
-            ya[e] = t < L ? silu_ftz(pre) : 0.f;
-            w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
-          }
-          if constexpr (kKind == 2) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) yv[gi * 8 + e] = ya[e];
-          } else {
-            {  // raw q or k, bf16: row d of KQ, tokens (q ? 64 : 0) + 8 grp ...
-              uint4 pk;
-              pk.x = pack_bf16(ya[0], ya[1]);
-              pk.y = pack_bf16(ya[2], ya[3]);
-              pk.z = pack_bf16(ya[4], ya[5]);
-              pk.w = pack_bf16(ya[6], ya[7]);
-              const int col = (kKind == 0 ? 64 : 0) + grp * 8;
-              *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(d, col * 2, 256)) = pk;
-            }
-            if constexpr (kKind == 1) {
-              uint4 pk;
-              const int t = grp * 8;
-              pk.x = pack_bf16(ya[0] * egv[t + 0], ya[1] * egv[t + 1]);
-              pk.y = pack_bf16(ya[2] * egv[t + 2], ya[3] * egv[t + 3]);
-              pk.z = pack_bf16(ya[4] * egv[t + 4], ya[5] * egv[t + 5]);
-              pk.w = pack_bf16(ya[6] * egv[t + 6], ya[7] * egv[t + 7]);
-              *reinterpret_cast<uint4*>(KGb + umma::tile_off(d, t * 2, 128)) = pk;
-              *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4, 256)) =
-                  make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
-              *reinterpret_cast<float4*>(KTb + umma::tile_off(d, t * 4 + 16, 256)) =
-                  make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
-            }
-          }
-        }
-        if constexpr (kKind == 2) {  // v row d = this thread's lane, columns kT0 ..
-          if constexpr (kNT == 32) umma::st32_nowait(tm + lane_base + kT_V + kT0, yv);
-          else umma::st16_nowait(tm + lane_base + kT_V + kT0, yv);
-        }
-      };
-      using I0 = std::integral_constant<int, 0>;
-      using I1 = std::integral_constant<int, 1>;
-      using I2 = std::integral_constant<int, 2>;
-      using I16 = std::integral_constant<int, 16>;
-      using I32 = std::integral_constant<int, 32>;
-      using I48 = std::integral_constant<int, 48>;
-      if (cset < 3) {
-        // the window carried to the next chunk: raw rows L-3 .. L-1, reaching
-        // back into the previous window when the chunk is shorter than 3
-        const uint16_t* xs = XS + cset * kC * kHeadDim + d;
-        const uint16_t nw[3] = {L >= 3 ? xs[(L - 3) * kHeadDim] : (L == 2 ? hw[2] : hw[1]),
-                                L >= 2 ? xs[(L - 2) * kHeadDim] : hw[2], xs[(L - 1) * kHeadDim]};
-        float w3[3] = {bf16_to_f32(hw[0]), bf16_to_f32(hw[1]), bf16_to_f32(hw[2])};
-        if (cset == 0) {
-          conv_seg(I0{}, I0{}, I32{}, wq, w3);
-          conv_seg(I0{}, I32{}, I16{}, wq, w3);
-        } else if (cset == 1) {
-          conv_seg(I1{}, I0{}, I32{}, wk, w3);
-          conv_seg(I1{}, I32{}, I16{}, wk, w3);
-        } else {
-          conv_seg(I2{}, I0{}, I32{}, wv, w3);
-          conv_seg(I2{}, I32{}, I16{}, wv, w3);
-        }
-        hw[0] = nw[0]; hw[1] = nw[1]; hw[2] = nw[2];
+      const uint16_t* xs = XS + (isq ? 0 : kC) * kHeadDim + dq;
+      uint16_t nw[3];
+      if (own_qk) next_window(xs, hqk, nw, L);
+      float w3[3];
+      if (own_qk) {
+        w3[0] = bf16_to_f32(hqk[0]); w3[1] = bf16_to_f32(hqk[1]); w3[2] = bf16_to_f32(hqk[2]);
       } else {
-        auto win45 = [&](const uint16_t* x, float (&w3)[3]) {  // raw rows 45-47
-          w3[0] = bf16_to_f32(x[45 * kHeadDim]);
-          w3[1] = bf16_to_f32(x[46 * kHeadDim]);
-          w3[2] = bf16_to_f32(x[47 * kHeadDim]);
-        };
-        float w3[3], w4[3], w5[3];
-        const uint16_t* xq = XS + d;
-        win45(xq, w3);
-        conv_seg(I0{}, I48{}, I16{}, wq, w3);
-        win45(xq + kC * kHeadDim, w4);
-        conv_seg(I1{}, I48{}, I16{}, wk, w4);
-        win45(xq + 2 * kC * kHeadDim, w5);
-        conv_seg(I2{}, I48{}, I16{}, wv, w5);
+        w3[0] = bf16_to_f32(xs[29 * kHeadDim]); w3[1] = bf16_to_f32(xs[30 * kHeadDim]);
+        w3[2] = bf16_to_f32(xs[31 * kHeadDim]);
+      }
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi) {
+        const int tb = 32 * qhalf + 8 * gi;
+        float ya[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int t = tb + e;
+          const float x = bf16_to_f32(xs[t * kHeadDim]);
+          float pre = wqk.x * x;
+          pre = fmaf(wqk.y, w3[2], pre);
+          pre = fmaf(wqk.z, w3[1], pre);
+          pre = fmaf(wqk.w, w3[0], pre);
+          ya[e] = t < L ? silu_ftz(pre) : 0.f;
+          w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
+        }
+        // raw q or k, bf16: row dq of KQ, tokens (q ? 64 : 0) + tb ..
+        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(dq, ((isq ? kC : 0) + tb) * 2, 256)) =
+            make_uint4(pack_bf16(ya[0], ya[1]), pack_bf16(ya[2], ya[3]), pack_bf16(ya[4], ya[5]), pack_bf16(ya[6], ya[7]));
+        if (!isq) {
+          // k e^g (bf16) and raw k (tf32)
+          *reinterpret_cast<uint4*>(KGb + umma::tile_off(dq, tb * 2, 128)) =
+              make_uint4(pack_bf16(ya[0] * egv[tb + 0], ya[1] * egv[tb + 1]), pack_bf16(ya[2] * egv[tb + 2], ya[3] * egv[tb + 3]),
+                         pack_bf16(ya[4] * egv[tb + 4], ya[5] * egv[tb + 5]), pack_bf16(ya[6] * egv[tb + 6], ya[7] * egv[tb + 7]));
+          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4, 256)) =
+              make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
+          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4 + 16, 256)) =
+              make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+        }
+      }
+      if (own_qk) {
+        hqk[0] = nw[0]; hqk[1] = nw[1]; hqk[2] = nw[2];
       }
     }
-    umma::wait_st();
     sync_for_mma();
 
     // ---- [K;Q][K;Q]^T (bf16): D1 lanes 0-63 = K rows, 64-127 = Q rows; columns
@@ -754,19 +772,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         make_gates(gates + ((c + 1) & 1) * 256, ln);
         if (c + 2 < nchunks) load_ab(tn + ln, min(kC, t1 - tn - ln));
       }
+      // the next chunk's v into tensor memory (this chunk's was read by Y above)
+      if (c + 1 < nchunks) {
+        if (!mbar_wait_bounded(&bars[6], (c + 1) & 1)) part_ok = false;
+        if (part_ok) v_conv(min(kC, t1 - tc - L));
+      }
     }
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
     if (__syncthreads_or(part_ok ? 0 : 1)) { ok = false; break; }
     umma::fence_after_sync();
     // the scratch area is free again (A and T consumed): raw rows of the next chunk
-    if (tid == kTmaThread && c + 1 < nchunks) {
-      issue_x(tc + L);
-      if (want_gate) {
-        bulk_wait_read_all();  // the Ogate store of the previous chunk has read that buffer
-        issue_z(tc + L, (c + 1) & 1);
-      }
-    }
+    if (tid == kTmaThread && c + 1 < nchunks) issue_x(tc + L);
     // ---- E^T = Y Tb^T (tf32)
     if (tid == 0) {
 #pragma unroll
@@ -837,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     }
     // one barrier: the RMS partials are published and (when gating) the z rows have landed
     if (want_gate) {
-      if (!wait_mma(&bars[5 + (c & 1)], (c >> 1) & 1)) { ok = false; break; }
+      if (!wait_mma(&bars[5], par)) { ok = false; break; }
     } else {
       __syncthreads();
     }
@@ -873,7 +890,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (tid == kTmaThread && want_gate) {
       st_tc = tc;
       st_len = L;
-      st_buf = c & 1;
     }
     // ---- align mode: after an absolute multiple of the block, the state (tensor
     // memory, updated by this chunk's MMAs) and the conv windows go to a snapshot slot
@@ -891,9 +907,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(sd + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-          if (cset < 3 && (cset == 2 || g == 0)) {
-            uint16_t* hp = p.conv_hist + ((size_t)ss * p.CH + gown) * 3;
-            hp[0] = hw[0]; hp[1] = hw[1]; hp[2] = hw[2];
+          if (own_v) {  // hv has already moved past the next chunk when there is one
+            const uint16_t* w = c + 1 < nchunks ? hv_end : hv;
+            uint16_t* hp = p.conv_hist + ((size_t)ss * p.CH + gvc) * 3;
+            hp[0] = w[0]; hp[1] = w[1]; hp[2] = w[2];
+          }
+          if (own_qk && g == 0) {
+            uint16_t* hp = p.conv_hist + ((size_t)ss * p.CH + gqk) * 3;
+            hp[0] = hqk[0]; hp[1] = hqk[1]; hp[2] = hqk[2];
           }
         }
       }
@@ -913,14 +934,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
     // history: q and k channels by the group's first CTA, v channels by the head's own
-    if (cset < 3 && (cset == 2 || g == 0)) {
-      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gown) * 3;
-      hp[0] = hw[0]; hp[1] = hw[1]; hp[2] = hw[2];
+    if (own_v) {  // v history: the head's own CTA
+      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gvc) * 3;
+      hp[0] = hv[0]; hp[1] = hv[1]; hp[2] = hv[2];
+    }
+    if (own_qk && g == 0) {  // q and k history: the group's first CTA
+      uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gqk) * 3;
+      hp[0] = hqk[0]; hp[1] = hqk[1]; hp[2] = hqk[2];
     }
   } else {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
     // give MMAs still in flight a second bounded chance before the memory is freed
-    for (int b = 0; b < 7; ++b) mbar_wait_bounded(&bars[b], 0);
+    for (int b = 0; b < 7; ++b) mbar_wait_bounded(&bars[b], 0);  // (bounded; phases may not match)
   }
   if (tid == kTmaThread) bulk_wait_all();  // Ogate rows stored
   umma::fence_before_sync();
