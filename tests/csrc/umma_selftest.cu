@@ -97,7 +97,25 @@ __global__ void __launch_bounds__(128) selftest_kernel(const Args p) {
   if (warp == 0) umma::tmem_dealloc(tmem, 256);
 }
 
+// A wait that can never succeed (nothing arrives on the barrier): the bounded
+// wait gives up after its time limit and the kernel reports a timeout in the
+// device error word, leaving the context usable.
+__global__ void bounded_wait_kernel(int32_t* dev_err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!mbar_wait_bounded(&bar, 0) && threadIdx.x == 0) report(dev_err, GDN_DEVERR_TIMEOUT);
+}
+
 }  // namespace
+
+extern "C" int bounded_wait_selftest(int32_t* dev_err, void* stream) {
+  bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_err);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" int umma_selftest(const float* A, const float* B, float* D, int* err, int M, int N, int K, int kind,
                              int a_mn, int b_mn, int b_cols, void* stream) {
