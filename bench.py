@@ -534,6 +534,78 @@ def measure_out_proj(b, dev, stream) -> dict:
             "hbm_peak_gbs": hbm_peak, **res}
 
 
+def measure_in_proj(b, dev, stream, geom, D) -> dict:
+    """The in_proj rows (hidden 5120 -> QKV0 10240, Z 6144, a|b 96 fp32; three cuBLASLt GEMMs) at the
+    decode batch (weight-streaming: two weight sets in rotation, 338 MB, so no step finds its weights in
+    L2) and at the prefill batch's token count (tensor-bound)."""
+    import torch
+    Dh = 5120
+    CH, NZ, NAB = geom.channels, geom.num_v_heads * geom.head_v_dim, 2 * geom.num_v_heads
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device=dev)
+    sets = [[(torch.randn((n, Dh), generator=g, device=dev) / Dh ** 0.5).to(torch.bfloat16) for n in (CH, NZ, NAB)]
+            for _ in range(2)]
+    res = {}
+    p_bf16, _, kind = load_bf16_peak()
+    hbm_peak, _ = load_peaks()
+    for name, T, steps in (("decode", NUM_REQ, 40), ("prefill", 71068, 5)):
+        u = torch.randn((T, Dh), generator=g, device=dev).to(torch.bfloat16)
+        qkv0 = torch.empty((T, CH), dtype=torch.bfloat16, device=dev)
+        z = torch.empty((T, NZ), dtype=torch.bfloat16, device=dev)
+        ab = torch.empty((T, NAB), dtype=torch.float32, device=dev)
+        it = [0]
+
+        def run():
+            wq, wz, wab = sets[it[0] % 2]
+            b.gdn_in_proj(D, u, wq, wz, qkv0, z, w_ab=wab, ab=ab, workspace=ws, stream=stream)
+            it[0] += 1
+
+        ms = timed(run, steps, 4, stream)
+        flops = 2.0 * T * Dh * (CH + NZ + NAB)
+        # weights once, the hidden rows once per GEMM, the outputs once
+        nbytes = (CH + NZ + NAB) * Dh * 2 + 3 * T * Dh * 2 + T * (CH + NZ) * 2 + T * NAB * 4
+        res[name] = {"tokens": T, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                     "tensor_frac": flops / (ms / 1e3) / 1e12 / p_bf16,
+                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+        del u, qkv0, z, ab
+    return {"workload": "QKV0 = U Wqkv^T, Z = U Wz^T, [a|b] = U Wab^T, 5120 -> 10240 / 6144 / 96, bf16 in, "
+                        "bf16 / bf16 / fp32 out, fp32 accumulation",
+            "kernel": "cuBLASLt (gdn_in_proj)", "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
+            "hbm_peak_gbs": hbm_peak, **res}
+
+
+def measure_rmsnorm(b, dev, stream) -> dict:
+    """The layer's input RMSNorm fused with the residual add (hidden 5120, bf16) at the decode batch and
+    at the prefill batch's token count: reads x and the residual, writes the residual and U."""
+    import torch
+    Dh = 5120
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    gamma = torch.rand(Dh, generator=g, device=dev) + 0.5
+    hbm_peak, _ = load_peaks()
+    res = {}
+    for name, T, steps in (("decode", NUM_REQ, 40), ("prefill", 71068, 10)):
+        # several independent buffer sets in rotation so that the decode batch's 10 MB does not stay in L2
+        nset = max(1, (1 << 30) // (T * Dh * 2 * 3))
+        sets = [[torch.randn((T, Dh), generator=g, device=dev).to(torch.bfloat16) for _ in range(3)]
+                for _ in range(nset)]
+        it = [0]
+
+        def run():
+            x, r, u = sets[it[0] % nset]
+            b.gdn_rmsnorm(x, gamma, 1e-6, u, residual=r, stream=stream)
+            it[0] += 1
+
+        ms = timed(run, steps, 4, stream)
+        nbytes = 4 * T * Dh * 2 + Dh * 4
+        res[name] = {"tokens": T, "ms": ms, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+        del sets
+    return {"workload": "residual <- x + residual; U = RMSNorm(residual) * gamma, hidden 5120, bf16",
+            "kernel": "rmsnorm_kernel (gdn_rmsnorm)", "hbm_peak_gbs": hbm_peak, **res}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -676,6 +748,9 @@ def run_gpu(args):
         extra["conv"] = measure_conv(b, dev, stream)
         torch.cuda.empty_cache()
         extra["out_proj"] = measure_out_proj(b, dev, stream)
+        extra["in_proj"] = measure_in_proj(b, dev, stream, geom, D)
+        torch.cuda.empty_cache()
+        extra["rmsnorm"] = measure_rmsnorm(b, dev, stream)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",

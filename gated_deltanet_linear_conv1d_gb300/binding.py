@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
         "gdn_spec_commit": [D, P, P, P, P, P, i32, i32, i32, P, P],
         "gdn_gated_rmsnorm": [P, P, P, f32, P, i32, i32, i32, P],
         "gdn_out_proj": [P, P, P, P, i32, i32, i32, P, sz, P],
+        "gdn_in_proj": [D, P, i32, P, P, P, P, P, P, i32, P, sz, P],
+        "gdn_rmsnorm": [P, P, P, f32, P, i32, i32, P],
         "gdn_read_device_error": [P, ctypes.POINTER(i32), i32, P],
     }
     for name, args in sigs.items():
@@ -275,6 +277,32 @@ def gdn_out_proj(ogate, w, out, residual=None, workspace=None, stream=None):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.gdn_out_proj(_ptr(ogate), _ptr(w), _ptr(residual), _ptr(out), T, K, N, _ptr(workspace), ws_bytes,
                              _stream(stream)), "gdn_out_proj")
+
+
+def gdn_rmsnorm(x, gamma, eps, out, residual=None, stream=None):
+    """out = RMSNorm(x) * gamma, or with residual: residual <- bf16(x + residual), out = RMSNorm(residual) * gamma."""
+    T, Dh = x.shape
+    _need(x, "x", torch.bfloat16, (T, Dh))
+    _need(gamma, "gamma", torch.float32, (Dh,))
+    _need(out, "out", torch.bfloat16, (T, Dh))
+    _need(residual, "residual", torch.bfloat16, (T, Dh), optional=True)
+    _check(_lib.gdn_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(out), T, Dh, _stream(stream)),
+           "gdn_rmsnorm")
+
+
+def gdn_in_proj(dims, hidden, w_qkv, w_z, qkv0, z, w_ab=None, ab=None, workspace=None, stream=None):
+    """QKV0 = hidden W_qkv^T, Z = hidden W_z^T and, when given, [a | b] = hidden W_ab^T (fp32)."""
+    T, Dh = hidden.shape
+    _need(hidden, "hidden", torch.bfloat16, (T, Dh))
+    _need(w_qkv, "w_qkv", torch.bfloat16, (dims.channels, Dh))
+    _need(w_z, "w_z", torch.bfloat16, (dims.num_v_heads * dims.head_v_dim, Dh))
+    _need(qkv0, "qkv0", torch.bfloat16, (T, dims.channels))
+    _need(z, "z", torch.bfloat16, (T, dims.num_v_heads * dims.head_v_dim))
+    _need(w_ab, "w_ab", torch.bfloat16, (2 * dims.num_v_heads, Dh), optional=True)
+    _need(ab, "ab", torch.float32, (T, 2 * dims.num_v_heads), optional=True)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_in_proj(ctypes.byref(dims), _ptr(hidden), Dh, _ptr(w_qkv), _ptr(w_z), _ptr(w_ab), _ptr(qkv0),
+                            _ptr(z), _ptr(ab), T, _ptr(workspace), ws_bytes, _stream(stream)), "gdn_in_proj")
 
 
 def gdn_spec_verify(dims, qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma, eps,

@@ -288,9 +288,38 @@ gdn_status gdn_out_proj(const uint16_t* ogate, const uint16_t* w, const uint16_t
     return GDN_ERR_INVALID_ARG;
   if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return GDN_ERR_INVALID_ARG;
   bool unsupported = false;
-  const cudaError_t e = launch_out_proj(ogate, w, residual, out, num_tokens, in_features, out_features,
-                                        workspace_bytes ? workspace : nullptr, workspace_bytes,
-                                        static_cast<cudaStream_t>(stream), &unsupported);
+  const cudaError_t e = launch_linear(ogate, w, residual, out, false, num_tokens, in_features, out_features,
+                                      workspace_bytes ? workspace : nullptr, workspace_bytes,
+                                      static_cast<cudaStream_t>(stream), &unsupported);
+  if (unsupported) return GDN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+gdn_status gdn_in_proj(const gdn_dims* d, const uint16_t* hidden, int32_t hidden_size, const uint16_t* w_qkv,
+                       const uint16_t* w_z, const uint16_t* w_ab, uint16_t* qkv0, uint16_t* z, float* ab,
+                       int32_t num_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (num_tokens < 0 || hidden_size <= 0) return GDN_ERR_INVALID_ARG;
+  const int CH = channels(d), NZ = d->num_v_heads * d->head_v_dim, NAB = 2 * d->num_v_heads;
+  if (hidden_size % 8 != 0 || NAB % 4 != 0) return GDN_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return GDN_OK;
+  if (!hidden || !w_qkv || !qkv0 || !w_z || !z || (!w_ab != !ab)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_qkv, 16) || !aligned(qkv0, 16) || !aligned(w_z, 16) || !aligned(z, 16) ||
+      (w_ab && (!aligned(w_ab, 16) || !aligned(ab, 16))))
+    return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return GDN_ERR_INVALID_ARG;
+  void* ws = workspace_bytes ? workspace : nullptr;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool unsupported = false;
+  cudaError_t e = launch_linear(hidden, w_qkv, nullptr, qkv0, false, num_tokens, hidden_size, CH, ws,
+                                workspace_bytes, s, &unsupported);
+  if (e == cudaSuccess)
+    e = launch_linear(hidden, w_z, nullptr, z, false, num_tokens, hidden_size, NZ, ws, workspace_bytes, s,
+                      &unsupported);
+  if (e == cudaSuccess && w_ab)
+    e = launch_linear(hidden, w_ab, nullptr, ab, true, num_tokens, hidden_size, NAB, ws, workspace_bytes, s,
+                      &unsupported);
   if (unsupported) return GDN_ERR_UNSUPPORTED;
   return from_cuda(e);
 }
@@ -307,6 +336,19 @@ gdn_status gdn_gated_rmsnorm(const uint16_t* o, const uint16_t* z, const float* 
   if (!aligned(o, 8) || !aligned(z, 8) || !aligned(out, 8) || !aligned(gamma, 16)) return GDN_ERR_INVALID_ARG;
   NormArgs a{o, z, gamma, out, eps, (int)rows, head_dim};
   return from_cuda(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_rmsnorm(const uint16_t* x, uint16_t* residual, const float* gamma, float eps, uint16_t* out,
+                       int32_t num_tokens, int32_t hidden_size, void* stream) {
+  if (num_tokens < 0 || hidden_size <= 0) return GDN_ERR_INVALID_ARG;
+  if (hidden_size % 8 != 0 || hidden_size > 8192) return GDN_ERR_UNSUPPORTED;
+  if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return GDN_OK;
+  if (!x || !gamma || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
+    return GDN_ERR_INVALID_ARG;
+  RmsArgs a{x, residual, gamma, out, eps, (int)num_tokens, (int)hidden_size};
+  return from_cuda(launch_rmsnorm(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -84,6 +84,16 @@ struct NormArgs {
   int D;
 };
 
+struct RmsArgs {
+  const uint16_t* x;
+  uint16_t* residual;  // NULL: no residual add
+  const float* gamma;
+  uint16_t* out;
+  float eps;
+  int rows;
+  int D;
+};
+
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (function, device).
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
@@ -103,11 +113,12 @@ constexpr int kStaticPrefillMaxSeqs = 65536;
 // device with cudaGetSymbolAddress and cached.
 cudaError_t static_prefill_order(int32_t** out);
 
-// out[T][N] = ogate[T][K] w[N][K]^T (+ residual[T][N]) through cuBLASLt; sets
+// out[T][N] = x[T][K] w[N][K]^T (+ residual[T][N]) through cuBLASLt, bf16
+// operands, fp32 accumulation, out (and residual) bf16 or fp32; sets
 // *unsupported when the library offers no algorithm for the shape.
-cudaError_t launch_out_proj(const uint16_t* ogate, const uint16_t* w, const uint16_t* residual, uint16_t* out,
-                            int T, int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream,
-                            bool* unsupported);
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, const void* residual, void* out, bool out_f32, int T,
+                          int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream, bool* unsupported);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream);
+cudaError_t launch_rmsnorm(const RmsArgs& a, cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,10 +1,12 @@
-// outproj.cu - gdn_out_proj: the output projection that follows the mixer
-// core (page "Qwen3.8-27B: from model structure to vLLM inference data flow",
-// section 01 GDN operator table, the Wo row: [T,6144] -> [T,5120], then the
-// residual add). The gated RMSNorm is already fused into the mixer kernels'
-// epilogues, so what is left is a plain bf16 GEMM with fp32 accumulation and
-// the residual folded into its epilogue (D = A B + C); it is issued through
-// cuBLASLt.
+// outproj.cu - the two projections around the mixer core (page "Qwen3.8-27B:
+// from model structure to vLLM inference data flow", section 01 GDN operator
+// table): gdn_in_proj, the rows in front of the conv ([T,5120] -> QKV0
+// [T,10240], Z [T,6144] and the a, b projections [T,48] each), and
+// gdn_out_proj, the Wo row ([T,6144] -> [T,5120]) with the residual add. The
+// conv is fused into the mixer kernels that read QKV0 and the gated RMSNorm into
+// the ones that write Ogate, so what is left on either side is a plain GEMM:
+// bf16 operands, fp32 accumulation, the residual folded into the epilogue
+// (D = A B + C), issued through cuBLASLt.
 //
 // Row-major out[T][N] = ogate[T][K] W^T (+ residual[T][N]) with W [N][K] (the
 // nn.Linear layout) is, column-major, out^T (N x T) = op(W) (N x K) ogate^T (K x T)
@@ -30,7 +32,7 @@ struct Plan {
 struct LtCache {
   std::mutex mu;
   std::map<int, cublasLtHandle_t> handles;                                  // per device
-  std::map<std::tuple<int, int, int, int, size_t>, Plan> plans;             // (device, T, K, N, workspace)
+  std::map<std::tuple<int, int, int, int, size_t, int>, Plan> plans;        // (device, T, K, N, workspace, D type)
 };
 
 LtCache& cache() {
@@ -39,7 +41,8 @@ LtCache& cache() {
 }
 
 // Builds (once per shape) the descriptors and the heuristic's first algorithm.
-cublasStatus_t get_plan(int dev, int T, int K, int N, size_t ws_bytes, cublasLtHandle_t* h_out, Plan* out) {
+cublasStatus_t get_plan(int dev, int T, int K, int N, size_t ws_bytes, cudaDataType_t cd_type, cublasLtHandle_t* h_out,
+                        Plan* out) {
   LtCache& lc = cache();
   std::lock_guard<std::mutex> lock(lc.mu);
   cublasStatus_t st = CUBLAS_STATUS_SUCCESS;
@@ -50,7 +53,7 @@ cublasStatus_t get_plan(int dev, int T, int K, int N, size_t ws_bytes, cublasLtH
     hit = lc.handles.emplace(dev, h).first;
   }
   *h_out = hit->second;
-  const auto key = std::make_tuple(dev, T, K, N, ws_bytes);
+  const auto key = std::make_tuple(dev, T, K, N, ws_bytes, (int)cd_type);
   auto pit = lc.plans.find(key);
   if (pit != lc.plans.end()) {
     *out = pit->second;
@@ -73,7 +76,7 @@ cublasStatus_t get_plan(int dev, int T, int K, int N, size_t ws_bytes, cublasLtH
     return fail(st);
   if ((st = cublasLtMatrixLayoutCreate(&p.a, CUDA_R_16BF, K, N, K)) != CUBLAS_STATUS_SUCCESS ||
       (st = cublasLtMatrixLayoutCreate(&p.b, CUDA_R_16BF, K, T, K)) != CUBLAS_STATUS_SUCCESS ||
-      (st = cublasLtMatrixLayoutCreate(&p.c, CUDA_R_16BF, N, T, N)) != CUBLAS_STATUS_SUCCESS)
+      (st = cublasLtMatrixLayoutCreate(&p.c, cd_type, N, T, N)) != CUBLAS_STATUS_SUCCESS)
     return fail(st);
   if ((st = cublasLtMatmulPreferenceCreate(&pref)) != CUBLAS_STATUS_SUCCESS) return fail(st);
   if ((st = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
@@ -93,23 +96,22 @@ cublasStatus_t get_plan(int dev, int T, int K, int N, size_t ws_bytes, cublasLtH
 
 }  // namespace
 
-cudaError_t launch_out_proj(const uint16_t* ogate, const uint16_t* w, const uint16_t* residual, uint16_t* out,
-                            int T, int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream,
-                            bool* unsupported) {
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, const void* residual, void* out, bool out_f32, int T,
+                          int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream, bool* unsupported) {
   *unsupported = false;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   cublasLtHandle_t h = nullptr;
   Plan p;
-  cublasStatus_t st = get_plan(dev, T, K, N, ws_bytes, &h, &p);
+  cublasStatus_t st = get_plan(dev, T, K, N, ws_bytes, out_f32 ? CUDA_R_32F : CUDA_R_16BF, &h, &p);
   if (st == CUBLAS_STATUS_NOT_SUPPORTED) {
     *unsupported = true;
     return cudaErrorNotSupported;
   }
   if (st != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
   const float alpha = 1.f, beta = residual ? 1.f : 0.f;
-  st = cublasLtMatmul(h, p.op, &alpha, w, p.a, ogate, p.b, &beta, residual ? residual : out, p.c, out, p.c, &p.algo,
+  st = cublasLtMatmul(h, p.op, &alpha, w, p.a, x, p.b, &beta, residual ? residual : out, p.c, out, p.c, &p.algo,
                       workspace, ws_bytes, stream);
   return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
 }

@@ -284,6 +284,47 @@ gdn_status gdn_gated_rmsnorm(const uint16_t *o, const uint16_t *z, const float *
                              int32_t head_dim, void *stream);
 
 /*
+ * gdn_rmsnorm - the layer's input RMSNorm U = X / sqrt(mean(X^2) + eps) (.) gamma
+ * over the hidden size, optionally fused with the residual add in front of it.
+ * Page "Qwen3.8-27B: from model structure to vLLM inference data flow", section
+ * 01 operator table, the U row (and the N = RMSNorm(Y) row, same form); page
+ * "DeepSeek-V3 inference pipeline walk-through" section 4.2 for the fused
+ * add-and-norm.
+ *
+ *   x         [T][D] bf16, D = hidden_size (a multiple of 8, at most 8192)
+ *   residual  [T][D] bf16 or NULL. When given, residual <- bf16(x + residual)
+ *             (rounded once, in place) and the norm is taken of that sum.
+ *   gamma     [D] fp32;  eps > 0 and finite
+ *   out       [T][D] bf16; may be x itself (in place)
+ * Pointers 16-byte aligned. num_tokens 0 is a no-op.
+ */
+gdn_status gdn_rmsnorm(const uint16_t *x, uint16_t *residual, const float *gamma, float eps, uint16_t *out,
+                       int32_t num_tokens, int32_t hidden_size, void *stream);
+
+/*
+ * gdn_in_proj - the input projections in front of the mixer core: QKV0 = U
+ * W_qkv^T, Z = U W_z^T and (optionally) the raw a, b projections [a | b] = U
+ * W_ab^T, bf16 operands, fp32 accumulation. Page: section 01 GDN operator
+ * table, the in_proj rows ([T,5120] -> QKV0 [T,10240], Z [T,6144], a and b
+ * [T,48]). The 4-tap conv that the table puts right after is fused into the
+ * mixer entry points that read QKV0; the map from a, b to alpha, beta is not
+ * on the pages, so a, b come out raw (fp32).
+ *
+ *   hidden  [T][D] bf16, D = hidden_size (a multiple of 8)
+ *   w_qkv   [CH][D] bf16;  qkv0 [T][CH] bf16 out      (the nn.Linear weight layout)
+ *   w_z     [Hv*dv][D] bf16;  z [T][Hv*dv] bf16 out
+ *   w_ab    [2*Hv][D] bf16 or NULL;  ab [T][2*Hv] fp32 out or NULL (both or neither;
+ *           a in columns 0 .. Hv-1, b in Hv .. 2Hv-1)
+ *   workspace, workspace_bytes: as gdn_out_proj (shared by the three GEMMs,
+ *           which run one after another on the stream)
+ * Pointers 16-byte aligned.
+ */
+gdn_status gdn_in_proj(const gdn_dims *dims, const uint16_t *hidden, int32_t hidden_size,
+                       const uint16_t *w_qkv, const uint16_t *w_z, const uint16_t *w_ab, uint16_t *qkv0,
+                       uint16_t *z, float *ab, int32_t num_tokens, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/*
  * gdn_out_proj - the output projection after the mixer core and the residual
  * add: out = ogate W^T (+ residual), bf16 operands, fp32 accumulation, bf16
  * out (round to nearest even). Page: section 01 GDN operator table, the Wo row

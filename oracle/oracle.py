@@ -229,6 +229,30 @@ def out_proj(ogate_bits, w_bits, residual_bits=None):
     return out
 
 
+def rmsnorm(x_bits, gamma, eps, residual_bits=None):
+    """The layer's input norm U = X / sqrt(mean(X^2 over the hidden size) + eps) * gamma in fp64 (page
+    "Qwen3.8-27B: from model structure to vLLM inference data flow", section 01 operator table, the U
+    row). With a residual, the residual stream is first X + residual, stored as bf16 the way a separate
+    add would store it, and the norm is taken of that stored sum (page "DeepSeek-V3 inference pipeline
+    walk-through" section 4.2: the fused add-and-norm equals the add followed by the norm).
+    Returns (U [T, D] fp64, the new residual as bf16 bits or None)."""
+    x = _bf16(x_bits)
+    new_res = None
+    if residual_bits is not None:
+        new_res = _round_bf16(x + _bf16(residual_bits))
+        x = _bf16(new_res)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + float(eps)) * np.asarray(gamma, dtype=np.float64), new_res
+
+
+def _round_bf16(x) -> np.ndarray:
+    """fp64 values to bf16 bits, round to nearest, ties to even, straight from fp64 (one rounding):
+    x = m 2^e with 1/2 <= |m| < 1, keep 8 significant bits of m (np.round breaks ties to even)."""
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    r = np.ldexp(np.round(np.ldexp(m, 8)), e - 8)
+    return (r.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
 def _bf16(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) to fp64 values."""
     b = np.ascontiguousarray(bits, dtype=np.uint16)

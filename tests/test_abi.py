@@ -86,3 +86,31 @@ def test_arguments_are_rejected_before_launch(b):
     assert lib.gdn_conv_update(ctypes.byref(d), p, p, p, p, p, None, 0, 0, p, None, None) == 0
     host = ctypes.c_int32(0)
     assert lib.gdn_read_device_error(None, ctypes.byref(host), 0, None) == 1
+
+
+def test_in_proj_rejects_bad_arguments_on_the_host(b):
+    """Shape and pointer checks of gdn_in_proj happen before any launch (no GPU needed)."""
+    lib = b._lib
+    D = b.make_dims(synth.FULL_HEADS, 1)
+    P = ctypes.c_void_p
+    fake = P(256)  # never dereferenced: every call below is rejected or returns before a launch
+    # hidden size not a multiple of 8
+    assert lib.gdn_in_proj(ctypes.byref(D), fake, 5121, fake, fake, None, fake, fake, None, 4, None, 0,
+                           None) == b.GDN_ERR_UNSUPPORTED
+    # w_ab without ab
+    assert lib.gdn_in_proj(ctypes.byref(D), fake, 5120, fake, fake, fake, fake, fake, None, 4, None, 0,
+                           None) == b.GDN_ERR_INVALID_ARG
+    # no tokens: nothing to do
+    assert lib.gdn_in_proj(ctypes.byref(D), None, 5120, None, None, None, None, None, None, 0, None, 0,
+                           None) == b.GDN_OK
+
+
+def test_rmsnorm_rejects_bad_arguments_on_the_host(b):
+    lib = b._lib
+    p, odd = ctypes.c_void_p(256), ctypes.c_void_p(264)  # never dereferenced
+    assert lib.gdn_rmsnorm(p, None, p, 1e-6, p, 4, 5124, None) == b.GDN_ERR_UNSUPPORTED  # not a multiple of 8
+    assert lib.gdn_rmsnorm(p, None, p, 1e-6, p, 4, 8200, None) == b.GDN_ERR_UNSUPPORTED  # above 8192
+    assert lib.gdn_rmsnorm(p, None, p, float("nan"), p, 4, 5120, None) == b.GDN_ERR_INVALID_ARG
+    assert lib.gdn_rmsnorm(p, odd, p, 1e-6, p, 4, 5120, None) == b.GDN_ERR_INVALID_ARG  # residual not 16 B aligned
+    assert lib.gdn_rmsnorm(None, None, p, 1e-6, p, 4, 5120, None) == b.GDN_ERR_INVALID_ARG
+    assert lib.gdn_rmsnorm(None, None, None, 1e-6, None, 0, 5120, None) == b.GDN_OK

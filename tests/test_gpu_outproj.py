@@ -55,3 +55,34 @@ def test_out_proj_without_workspace_and_empty(b):
     U.check_out(U.host_f64_from_bf16(out), oracle.out_proj(a, w), "out")
     empty = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
     b.gdn_out_proj(torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda"), U.dev_bf16(w), empty)
+
+
+def _in_proj_case(dims, T, Dh, seed):
+    rng = np.random.default_rng(seed)
+    u = U.synth.bf16_bits(rng.normal(size=(T, Dh)).astype(np.float32))
+    ws = [U.synth.bf16_bits((rng.normal(size=(n, Dh)) / np.sqrt(Dh)).astype(np.float32))
+          for n in (dims.channels, dims.num_v_heads * dims.head_v_dim, 2 * dims.num_v_heads)]
+    return u, ws
+
+
+@pytest.mark.parametrize("heads,T,Dh,with_ab", [("small", 1, 64, True), ("small", 67, 200, False),
+                                                ("full", 256, 5120, True)])
+def test_in_proj_matches_oracle(b, heads, T, Dh, with_ab):
+    """QKV0, Z and [a | b] = U W^T for each of the three in_proj weights; the full case is the layer's
+    hidden size 5120 at the decode batch (5120 -> 10240 / 6144 / 96)."""
+    dims = U.synth.FULL_HEADS if heads == "full" else U.synth.Dims(1, 2, 128, 128, 4)
+    u, (w_qkv, w_z, w_ab) = _in_proj_case(dims, T, Dh, 95 + T)
+    D = b.make_dims(dims, 1)
+    qkv0 = torch.zeros((T, dims.channels), dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros((T, dims.num_v_heads * dims.head_v_dim), dtype=torch.bfloat16, device="cuda")
+    ab = torch.zeros((T, 2 * dims.num_v_heads), dtype=torch.float32, device="cuda") if with_ab else None
+    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    b.gdn_in_proj(D, U.dev_bf16(u), U.dev_bf16(w_qkv), U.dev_bf16(w_z), qkv0, z,
+                  w_ab=U.dev_bf16(w_ab) if with_ab else None, ab=ab, workspace=ws)
+    U.check_out(U.host_f64_from_bf16(qkv0), oracle.out_proj(u, w_qkv), "qkv0")
+    U.check_out(U.host_f64_from_bf16(z), oracle.out_proj(u, w_z), "z")
+    if with_ab:
+        got = ab.cpu().numpy().astype(np.float64)
+        ref = oracle.out_proj(u, w_ab)
+        # fp32 output: only the accumulation order differs from the fp64 sum
+        assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max()), "ab"

@@ -420,3 +420,42 @@ def test_out_proj_one_hot_rows_select_input_columns():
     w[np.arange(N), cols] = 1.0
     got = oracle.out_proj(_bits(a), _bits(w))
     np.testing.assert_array_equal(got, synth.bf16_to_f32(_bits(a)).astype(np.float64)[:, cols])
+
+
+# ---------------------------------------------------------------- input RMSNorm (U row), fused residual add
+
+def test_rmsnorm_hand_values():
+    """[3, 4, 0, 0]: mean of squares 25/4, rms 2.5, so U = [1.2, 1.6, 0, 0] * gamma; a constant row
+    c = 1 with eps = 3 gives 1 / sqrt(1 + 3) = 0.5 (eps sits inside the root, added to the mean)."""
+    u, res = oracle.rmsnorm(_bits([[3.0, 4.0, 0.0, 0.0]]), np.array([1.0, 2.0, 1.0, 1.0]), 0.0)
+    np.testing.assert_allclose(u, [[1.2, 3.2, 0.0, 0.0]], rtol=1e-15)
+    assert res is None
+    u, _ = oracle.rmsnorm(_bits(np.ones((2, 8))), np.ones(8), 3.0)
+    np.testing.assert_array_equal(u, np.full((2, 8), 0.5))
+
+
+def test_rmsnorm_residual_sum_rounds_once_to_nearest_even():
+    """Sums worked by hand on the bf16 grid (8 significant bits: spacing 2^-7 above 1, 2^-8 below):
+    1 + 2^-8 is a tie and goes to 1 (even); 1 + 3*2^-8 is a tie between 1 + 2^-7 and 1 + 2^-6 and goes
+    to 1 + 2^-6 (even); 1 - 2^-9 is a tie between 1 - 2^-8 and 1 and goes to 1; 1 + 2^-7 is exact."""
+    x = np.array([[1.0, 1.0, 1.0, 1.0 + 2.0 ** -7]])
+    r = np.array([[2.0 ** -8, 3 * 2.0 ** -8, -2.0 ** -9, 0.0]])
+    _, res = oracle.rmsnorm(_bits(x), np.ones(4), 1e-6, _bits(r))
+    got = synth.bf16_to_f32(res).astype(np.float64)
+    np.testing.assert_array_equal(got, [[1.0, 1.0 + 2.0 ** -6, 1.0, 1.0 + 2.0 ** -7]])
+    # the norm is taken of the stored (rounded) sum, not of the exact one
+    u, _ = oracle.rmsnorm(_bits(x), np.ones(4), 1e-6, _bits(r))
+    s = got[0]
+    np.testing.assert_allclose(u[0], s / np.sqrt(np.mean(s * s) + 1e-6), rtol=1e-15)
+
+
+def test_rmsnorm_scale_invariance_and_unit_rms():
+    """With eps = 0, U does not change when a row is scaled by a power of two, and U / gamma has mean
+    square exactly 1 per row."""
+    rng = np.random.default_rng(72)
+    x = _bits(rng.normal(size=(6, 40)))
+    g = rng.uniform(0.5, 2.0, size=40)
+    u, _ = oracle.rmsnorm(x, g, 0.0)
+    u4, _ = oracle.rmsnorm(_bits(4.0 * synth.bf16_to_f32(x)), g, 0.0)
+    np.testing.assert_allclose(u4, u, rtol=1e-14)
+    np.testing.assert_allclose(np.mean((u / g) ** 2, axis=1), 1.0, rtol=1e-13)
