@@ -456,8 +456,23 @@ def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
                             wp["alpha"], wp["beta"], wp["z"], wp["gamma"], 1e-6, ogate=pog, workspace=pws,
                             dev_err=err, stream=stream)
 
+    side = torch.cuda.Stream(device=dev)
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+
+    def mixed_two_streams():
+        # the prefill on a second stream, so its CTAs can take the SMs the verify leaves idle and vice versa
+        fork.record(stream)
+        side.wait_event(fork)
+        spec_only()
+        b.gdn_chunk_prefill(Dp, wp["qkv0"], wp["conv_w"], wp["conv_hist"], wp["state"], pqsl, pslots,
+                            wp["alpha"], wp["beta"], wp["z"], wp["gamma"], 1e-6, ogate=pog, workspace=pws,
+                            dev_err=err, stream=side)
+        join.record(side)
+        stream.wait_event(join)
+
     ms_spec = timed(spec_only, steps, warmup, stream)
     ms_mixed = timed(mixed, steps, warmup, stream)
+    ms_two = timed(mixed_two_streams, steps, warmup, stream)
     if b.gdn_read_device_error(err) != 0:
         raise RuntimeError("device error flagged during the speculative-verify measurement")
     state = geom.num_v_heads * geom.head_v_dim * geom.head_k_dim * 4
@@ -469,7 +484,9 @@ def measure_spec_mixed(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
                         "checkpoint per position, commit by copy at accepted U{0..3}; B: prefill 8 x 2048 tokens",
             "spec_value": N * P / (ms_spec / 1e3), "unit": "verified tokens/s", "spec_ms": ms_spec,
             "spec_hbm_gbs": spec_bytes / (ms_spec / 1e3) / 1e9, "spec_hbm_frac": spec_bytes / (ms_spec / 1e3) / 1e9 / hbm_peak,
-            "mixed_ms": ms_mixed, "mixed_tokens_per_s": (N * P + int(lengths.sum())) / (ms_mixed / 1e3)}
+            "mixed_ms": ms_mixed, "mixed_tokens_per_s": (N * P + int(lengths.sum())) / (ms_mixed / 1e3),
+            "mixed_two_streams_ms": ms_two,
+            "mixed_two_streams_tokens_per_s": (N * P + int(lengths.sum())) / (ms_two / 1e3)}
 
 
 def measure_conv(b, dev, stream, steps: int = 10, warmup: int = 3) -> dict:
@@ -572,6 +589,68 @@ def measure_in_proj(b, dev, stream, geom, D) -> dict:
     return {"workload": "QKV0 = U Wqkv^T, Z = U Wz^T, [a|b] = U Wab^T, 5120 -> 10240 / 6144 / 96, bf16 in, "
                         "bf16 / bf16 / fp32 out, fp32 accumulation",
             "kernel": "cuBLASLt (gdn_in_proj)", "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
+            "hbm_peak_gbs": hbm_peak, **res}
+
+
+def measure_fp8_proj(b, dev, stream) -> dict:
+    """The projections with FP8 E4M3 block-scaled weights (one scale per 128 x 128 block) and activations
+    quantised per token and 128-wide group: Wo (6144 -> 5120) and the QKV + Z rows of in_proj
+    (5120 -> 10240 + 6144), each as activation quantisation + the tcgen05 GEMM, at the decode batch
+    (weight sets in rotation past L2) and at the prefill batch's token count."""
+    import torch
+    p_bf16, _, kind = load_bf16_peak()
+    p_fp8 = 2.0 * p_bf16  # nominal dense fp8 rate is twice bf16 on this part
+    hbm_peak, _ = load_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(8)
+    res = {}
+    for proj, K, Ns in (("wo", 6144, (5120,)), ("in_proj", 5120, (10240, 6144))):
+        wbytes = sum(Ns) * K
+        nsets = max(2, -(-(192 << 20) // wbytes))
+        sets = []
+        for _ in range(nsets):
+            one = []
+            for N in Ns:
+                w = (torch.randn((N, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+                w8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
+                ws = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
+                b.gdn_fp8_quant_weight(w, w8, ws, stream=stream)
+                one.append((w8, ws))
+                del w
+            sets.append(one)
+        for name, T, steps in (("decode", NUM_REQ, 40), ("prefill", 71068, 5)):
+            x = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+            x8 = torch.empty((T, K), dtype=torch.uint8, device=dev)
+            xs = torch.empty((T, K // 128), dtype=torch.float32, device=dev)
+            outs = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for N in Ns]
+            wsps = [torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device=dev)
+                    for N in Ns]
+            it = [0]
+
+            def gemms():
+                for (w8, ws), out, wsp in zip(sets[it[0] % nsets], outs, wsps):
+                    b.gdn_fp8_linear(x8, xs, w8, ws, out, workspace=wsp, stream=stream)
+                it[0] += 1
+
+            def run():
+                b.gdn_fp8_quant_act(x, x8, xs, stream=stream)
+                gemms()
+
+            ms = timed(run, steps, 4, stream)
+            ms_gemm = timed(gemms, steps, 4, stream)
+            flops = 2.0 * T * K * sum(Ns)
+            nbytes = wbytes + T * K * len(Ns) + T * sum(Ns) * 2
+            res[f"{proj}_{name}"] = {"tokens": T, "ms": ms, "gemm_ms": ms_gemm,
+                                     "gemm_tflops": flops / (ms_gemm / 1e3) / 1e12,
+                                     "gemm_tensor_frac_of_fp8": flops / (ms_gemm / 1e3) / 1e12 / p_fp8,
+                                     "gemm_hbm_frac": nbytes / (ms_gemm / 1e3) / 1e9 / hbm_peak}
+            del x, x8, xs, outs, wsps
+        del sets
+        torch.cuda.empty_cache()
+    return {"workload": "E4M3 weights, one fp32 scale per 128x128 block; activations quantised per token and "
+                        "128-wide group (gdn_fp8_quant_act) then gdn_fp8_linear; ms = quantise + GEMM(s)",
+            "kernel": "fp8_gemm_kernel (tcgen05 kind::f8f6f4, per-block promotion in registers)",
+            "peak_fp8_tflops": p_fp8, "peak_kind": f"2 x {kind} bf16 burst (nominal fp8/bf16 ratio)",
             "hbm_peak_gbs": hbm_peak, **res}
 
 
@@ -751,6 +830,8 @@ def run_gpu(args):
         extra["in_proj"] = measure_in_proj(b, dev, stream, geom, D)
         torch.cuda.empty_cache()
         extra["rmsnorm"] = measure_rmsnorm(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["fp8_proj"] = measure_fp8_proj(b, dev, stream)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",

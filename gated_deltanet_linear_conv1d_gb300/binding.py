@@ -68,6 +68,9 @@ def _load() -> ctypes.CDLL:
         "gdn_out_proj": [P, P, P, P, i32, i32, i32, P, sz, P],
         "gdn_in_proj": [D, P, i32, P, P, P, P, P, P, i32, P, sz, P],
         "gdn_rmsnorm": [P, P, P, f32, P, i32, i32, P],
+        "gdn_fp8_quant_act": [P, P, P, i32, i32, P],
+        "gdn_fp8_quant_weight": [P, P, P, i32, i32, P],
+        "gdn_fp8_linear": [P, P, P, P, P, P, i32, i32, i32, P, sz, P, P],
         "gdn_read_device_error": [P, ctypes.POINTER(i32), i32, P],
     }
     for name, args in sigs.items():
@@ -81,6 +84,8 @@ def _load() -> ctypes.CDLL:
     lib.gdn_prefill_workspace_bytes.restype = sz
     lib.gdn_out_proj_workspace_bytes.argtypes = []
     lib.gdn_out_proj_workspace_bytes.restype = sz
+    lib.gdn_fp8_linear_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.gdn_fp8_linear_workspace_bytes.restype = sz
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_status_string.restype = ctypes.c_char_p
     return lib
@@ -288,6 +293,46 @@ def gdn_rmsnorm(x, gamma, eps, out, residual=None, stream=None):
     _need(residual, "residual", torch.bfloat16, (T, Dh), optional=True)
     _check(_lib.gdn_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(out), T, Dh, _stream(stream)),
            "gdn_rmsnorm")
+
+
+def gdn_fp8_quant_act(x, x8, x_scale, stream=None):
+    """x [T, K] bf16 -> x8 [T, K] e4m3 (uint8 storage) and x_scale [T, K/128] fp32."""
+    T, K = x.shape
+    _need(x, "x", torch.bfloat16, (T, K))
+    _need(x8, "x8", torch.uint8, (T, K))
+    _need(x_scale, "x_scale", torch.float32, (T, K // 128))
+    _check(_lib.gdn_fp8_quant_act(_ptr(x), _ptr(x8), _ptr(x_scale), T, K, _stream(stream)), "gdn_fp8_quant_act")
+
+
+def gdn_fp8_quant_weight(w, w8, w_scale, stream=None):
+    """w [N, K] bf16 -> w8 [N, K] e4m3 (uint8 storage) and w_scale [ceil(N/128), K/128] fp32."""
+    N, K = w.shape
+    _need(w, "w", torch.bfloat16, (N, K))
+    _need(w8, "w8", torch.uint8, (N, K))
+    _need(w_scale, "w_scale", torch.float32, ((N + 127) // 128, K // 128))
+    _check(_lib.gdn_fp8_quant_weight(_ptr(w), _ptr(w8), _ptr(w_scale), N, K, _stream(stream)),
+           "gdn_fp8_quant_weight")
+
+
+def gdn_fp8_linear_workspace_bytes(num_tokens: int, k: int, n: int) -> int:
+    return int(_lib.gdn_fp8_linear_workspace_bytes(int(num_tokens), int(k), int(n)))
+
+
+def gdn_fp8_linear(x8, x_scale, w8, w_scale, out, residual=None, workspace=None, dev_err=None, stream=None):
+    """out [T, N] = dequant(x8) dequant(w8)^T (+ residual), block-scaled FP8 operands, bf16 out.
+    workspace: zero-filled before its first use (each call resets its tickets)."""
+    T, K = x8.shape
+    N = w8.shape[0]
+    _need(x8, "x8", torch.uint8, (T, K))
+    _need(w8, "w8", torch.uint8, (N, K))
+    _need(x_scale, "x_scale", torch.float32, (T, K // 128))
+    _need(w_scale, "w_scale", torch.float32, ((N + 127) // 128, K // 128))
+    _need(out, "out", torch.bfloat16, (T, N))
+    _need(residual, "residual", torch.bfloat16, (T, N), optional=True)
+    _need(dev_err, "dev_err", torch.int32, (1,), optional=True)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_fp8_linear(_ptr(x8), _ptr(x_scale), _ptr(w8), _ptr(w_scale), _ptr(residual), _ptr(out), T, K, N,
+                               _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)), "gdn_fp8_linear")
 
 
 def gdn_in_proj(dims, hidden, w_qkv, w_z, qkv0, z, w_ab=None, ab=None, workspace=None, stream=None):

@@ -351,4 +351,46 @@ gdn_status gdn_rmsnorm(const uint16_t* x, uint16_t* residual, const float* gamma
   return from_cuda(launch_rmsnorm(a, static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_fp8_quant_act(const uint16_t* x, uint8_t* x8, float* x_scale, int32_t num_tokens, int32_t k,
+                             void* stream) {
+  if (num_tokens < 0 || k <= 0) return GDN_ERR_INVALID_ARG;
+  if (k % 128 != 0) return GDN_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return GDN_OK;
+  if (!x || !x8 || !x_scale) return GDN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(x_scale, 16)) return GDN_ERR_INVALID_ARG;
+  QuantActArgs a{x, x8, x_scale, k / 128, 1, (int)num_tokens, (int)k};  // scales [T][K/128]
+  return from_cuda(launch_quant_act(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_fp8_quant_weight(const uint16_t* w, uint8_t* w8, float* w_scale, int32_t n, int32_t k, void* stream) {
+  if (n < 0 || k <= 0) return GDN_ERR_INVALID_ARG;
+  if (k % 128 != 0) return GDN_ERR_UNSUPPORTED;
+  if (n == 0) return GDN_OK;
+  if (!w || !w8 || !w_scale) return GDN_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(w8, 16) || !aligned(w_scale, 16)) return GDN_ERR_INVALID_ARG;
+  QuantWeightArgs a{w, w8, w_scale, k / 128, 1, (int)n, (int)k};  // scales [ceil(N/128)][K/128]
+  return from_cuda(launch_quant_weight(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t gdn_fp8_linear_workspace_bytes(int32_t num_tokens, int32_t k, int32_t n) {
+  if (num_tokens <= 0 || n <= 0 || k <= 0 || k % 128 != 0) return 0;
+  return fp8_gemm_workspace_bytes(num_tokens, n, k);
+}
+
+gdn_status gdn_fp8_linear(const uint8_t* x8, const float* x_scale, const uint8_t* w8, const float* w_scale,
+                          const uint16_t* residual, uint16_t* out, int32_t num_tokens, int32_t k, int32_t n,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (num_tokens < 0 || k <= 0 || n <= 0) return GDN_ERR_INVALID_ARG;
+  if (k % 128 != 0 || n % 16 != 0) return GDN_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return GDN_OK;
+  if (!x8 || !x_scale || !w8 || !w_scale || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned(x8, 16) || !aligned(x_scale, 16) || !aligned(w8, 16) || !aligned(w_scale, 16) || !aligned(out, 16) ||
+      (residual && !aligned(residual, 16)))
+    return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return GDN_ERR_INVALID_ARG;
+  Fp8Operands o{x8, x_scale, w8, w_scale, residual, out, (int)num_tokens, (int)k, (int)n};
+  return from_cuda(launch_fp8_gemm(o, workspace_bytes ? workspace : nullptr, workspace_bytes, dev_err,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -1,0 +1,417 @@
+// fp8_gemm.cu - gdn_fp8_linear: out[T][N] = dequant(X8) dequant(W8)^T (+ residual)
+// with DeepSeek-style block scales (page "Qwen3.8-27B: from model structure to
+// vLLM inference data flow", section 04, precision and cache: FP8 E4M3 linear
+// weights with one scale per 128 x 128 weight block, activations quantised
+// dynamically; here one scale per token and 128-wide group of K).
+//
+//   out[t][n] = sum_kb xs[t][kb] * ws[n/128][kb] * sum_{k in block kb} X8[t][k] W8[n][k]
+//
+// Because the scales change every 128 elements of K, the tensor cores compute
+// one 128 x 128 x 128 block product at a time into tensor memory (four
+// kind::f8f6f4 MMAs of K = 32, exact E4M3 products, fp32 sums) and eight
+// "promotion" warps fold each block product into fp32 registers with its scale
+// product. Four tensor-memory buffers let the MMAs run up to three blocks ahead
+// of the folding.
+//
+// Output tiles are 128 tokens x 128 outputs. With at least two waves of tiles a
+// persistent CTA takes whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... and
+// stores bf16 rows directly. With fewer tiles (the decode batch) the K blocks of
+// all tiles, laid end to end, are cut into gridDim.x equal contiguous ranges
+// (stream-K), so every SM does the same work; a CTA stores the fp32 partial of a
+// tile it covers only in part into its own workspace slice (plain coalesced
+// stores), and the CTA that finishes a tile's last piece (an atomic ticket, no
+// waiting) adds the other pieces, stores the bf16 tile and resets the ticket.
+//
+// Warp roles (320 threads): warp 0 lane 0 issues the TMA copies into a 4-stage
+// ring (X8 and W8 tiles, 128 B x 128 rows each, 128-byte swizzle), warp 1
+// allocates tensor memory and its lane 0 issues the MMAs, warps 2-9 promote and
+// store: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (its 32 tokens) and
+// columns 64 ((w - 2) / 4) .. +63 (its half of the 128 outputs).
+#include <cuda.h>
+
+#include "device.cuh"
+#include "launch.h"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 128;  // kBK: one scale block of K (bytes = elements)
+constexpr int kStages = 4;
+constexpr int kPromoWarps = 8;
+constexpr int kThreads = 32 * (2 + kPromoWarps);
+constexpr int kTileBytes = kBM * kBK;            // 16 KB per operand tile
+constexpr int kStageBytes = 2 * kTileBytes;      // X tile, then W tile
+constexpr int kBarOff = kStages * kStageBytes;   // barriers after the ring
+constexpr int kSmemBytes = kBarOff + 256 + 1024; // + barriers + alignment slack
+constexpr int kTmemBufs = 4;
+constexpr int kTmemCols = kTmemBufs * kBN;       // four partial-product buffers (all 512 columns)
+constexpr int kCols = kBN / 2;                   // output columns per promotion thread
+constexpr int kScaleAhead = 4;                   // block scales are loaded this many K blocks ahead
+constexpr int kPromo = 32 * kPromoWarps;         // promotion threads
+
+// f8f6f4, E4M3 x E4M3, fp32 accumulator, both K-major, M = 128, N = 128
+constexpr uint32_t kIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kBN);
+
+__device__ __forceinline__ void promo_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Columns n .. n+7 of one output row: v (+ residual) rounded to bf16, one 16-byte store.
+__device__ __forceinline__ void store_row8(uint16_t* out_row, const uint16_t* res_row, int n, int N, const float (&v)[8]) {
+  if (n >= N) return;
+  float f[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] = v[e];
+  if (res_row) {
+    const uint4 r = *reinterpret_cast<const uint4*>(res_row + n);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[2 * e] += bf16_to_f32(rw[e] & 0xffff);
+      f[2 * e + 1] += bf16_to_f32(rw[e] >> 16);
+    }
+  }
+  uint32_t w4[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) w4[e] = (uint32_t)f32_to_bf16(f[2 * e]) | ((uint32_t)f32_to_bf16(f[2 * e + 1]) << 16);
+  *reinterpret_cast<uint4*>(out_row + n) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+}
+
+__device__ __forceinline__ void arrive_one(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs p,
+                                                                const __grid_constant__ CUtensorMap tmx,
+                                                                const __grid_constant__ CUtensorMap tmw) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // [kStages] TMA -> MMA
+  uint64_t* empty = full + kStages;                                // [kStages] MMA -> TMA
+  uint64_t* tfull = empty + kStages;                               // [kTmemBufs] MMA -> promotion
+  uint64_t* tempty = tfull + kTmemBufs;                            // [kTmemBufs] promotion -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kTmemBufs);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);              // [0] abort, [1] last-split ticket
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kTmemBufs; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kPromoWarps);  // one arrival per promotion warp
+    }
+    flags[0] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) umma::tmem_alloc(tmem_slot, kTmemCols);
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tm = *tmem_slot;
+  volatile int* abort_flag = flags;
+
+  // ---- the pieces this CTA computes: (tile t, K blocks kb0 .. kb1-1)
+  const long long G = gridDim.x;
+  const long long r0 = p.stream_k ? (long long)blockIdx.x * p.total / G : blockIdx.x;
+  const long long r1 = p.stream_k ? (long long)(blockIdx.x + 1) * p.total / G : p.tiles;
+  auto next_piece = [&](long long& cur, int& t, int& kb0, int& kb1) -> bool {
+    if (p.stream_k) {
+      if (cur >= r1) return false;
+      t = (int)(cur / p.KB);
+      kb0 = (int)(cur - (long long)t * p.KB);
+      kb1 = (int)min((long long)p.KB, kb0 + (r1 - cur));
+      cur += kb1 - kb0;
+    } else {
+      if (cur >= r1) return false;
+      t = (int)cur;
+      kb0 = 0;
+      kb1 = p.KB;
+      cur += G;
+    }
+    return true;
+  };
+
+  if (warp == 0) {
+    // ---- TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+      uint32_t gk = 0;
+      bool ok = true;
+      long long cur = r0;
+      int t, kb0, kb1;
+      while (ok && next_piece(cur, t, kb0, kb1)) {
+        const int m_t = t / p.nt, n_t = t % p.nt;
+        for (int kb = kb0; kb < kb1; ++kb, ++gk) {
+          const int s = gk % kStages;
+          if (gk >= (uint32_t)kStages && !mbar_wait_bounded(&empty[s], ((gk / kStages) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (*abort_flag) { ok = false; break; }
+          unsigned char* st = smem + s * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(st, &tmx, kb * kBK, m_t * kBM, &full[s]);
+          tma_load_2d(st + kTileBytes, &tmw, kb * kBK, n_t * kBN, &full[s]);
+        }
+      }
+      if (!ok) {
+        report(p.dev_err, GDN_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        // copies still in flight land before the CTA leaves: wait (bounded) for the last ones issued
+        for (uint32_t j = (gk > (uint32_t)kStages ? gk - kStages : 0); j < gk; ++j)
+          mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      uint32_t gk = 0;
+      bool ok = true;
+      long long cur = r0;
+      int t, kb0, kb1;
+      while (ok && next_piece(cur, t, kb0, kb1)) {
+        for (int kb = kb0; kb < kb1; ++kb, ++gk) {
+          const int s = gk % kStages;
+          const uint32_t b = gk % kTmemBufs, use = gk / kTmemBufs;
+          if (!mbar_wait_bounded(&full[s], (gk / kStages) & 1) ||
+              (gk >= (uint32_t)kTmemBufs && !mbar_wait_bounded(&tempty[b], (use - 1) & 1)) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          umma::fence_after_sync();
+          const uint32_t sx = smem_u32(smem + s * kStageBytes), sw = sx + kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            umma::mma<umma::kKindF8>(tm + b * kBN, umma::smem_desc_sw128(sx + kk * 32),
+                                     umma::smem_desc_sw128(sw + kk * 32), kIdesc, kk > 0);
+          umma::commit(&empty[s]);
+          umma::commit(&tfull[b]);
+        }
+      }
+      if (!ok) {
+        report(p.dev_err, GDN_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // the MMAs issued last have finished before tensor memory is released
+      if (gk > 0) mbar_wait_bounded(&tfull[(gk - 1) % kTmemBufs], ((gk - 1) / kTmemBufs) & 1);
+    }
+  } else {
+    // ---- promotion and store (warps 2-9). These warps never leave the item loop
+    // early, so the named barriers of the split-K store stay matched; once a wait
+    // has timed out (abort flag) they only skip the work.
+    const int q = warp & 3;                 // tensor-memory lane quarter
+    const int half = (warp - 2) >> 2;       // which 64 of the tile's 128 columns
+    const uint32_t lane_base = ((uint32_t)(32 * q) << 16) + half * kCols;
+    uint32_t gk = 0;
+    long long cur = r0;
+    int t, kb0, kb1;
+    const int my_first_tile = p.stream_k ? (int)(r0 / p.KB) : -1;
+    while (next_piece(cur, t, kb0, kb1)) {
+      const int m_t = t / p.nt, n_t = t % p.nt;
+      const int row = m_t * kBM + 32 * q + lane;  // this thread's token
+      const bool live = row < p.T;
+      const float* xs_row = p.xs + (size_t)(live ? row : 0) * p.KB;
+      const float* ws_row = p.ws + (size_t)n_t * p.KB;
+      float acc[kCols];
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
+      // the block scales, loaded kScaleAhead blocks before they are used so that
+      // their latency stays off the folding loop
+      float sx[kScaleAhead], sw[kScaleAhead];
+#pragma unroll
+      for (int i = 0; i < kScaleAhead; ++i) {
+        const int kb = min(kb0 + i, kb1 - 1);
+        sx[i] = live ? __ldg(xs_row + kb) : 0.f;
+        sw[i] = __ldg(ws_row + kb);
+      }
+      for (int kb = kb0; kb < kb1; ++kb, ++gk) {
+        const uint32_t b = gk % kTmemBufs, use = gk / kTmemBufs;
+        const float scale = sx[0] * sw[0];
+#pragma unroll
+        for (int i = 0; i + 1 < kScaleAhead; ++i) {
+          sx[i] = sx[i + 1];
+          sw[i] = sw[i + 1];
+        }
+        {
+          const int kn = min(kb + kScaleAhead, kb1 - 1);
+          sx[kScaleAhead - 1] = live ? __ldg(xs_row + kn) : 0.f;
+          sw[kScaleAhead - 1] = __ldg(ws_row + kn);
+        }
+        if (*abort_flag) continue;
+        if (!mbar_wait_bounded(&tfull[b], use & 1)) {
+          report(p.dev_err, GDN_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          continue;
+        }
+        umma::fence_after_sync();
+        {
+          uint32_t v0[32], v1[32];
+          umma::ld32_nowait(tm + lane_base + b * kBN, v0);
+          umma::ld32_nowait(tm + lane_base + b * kBN + 32, v1);
+          umma::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            acc[i] = fmaf(scale, __uint_as_float(v0[i]), acc[i]);
+            acc[32 + i] = fmaf(scale, __uint_as_float(v1[i]), acc[32 + i]);
+          }
+        }
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_one(&tempty[b]);
+      }
+      const bool aborted = *abort_flag != 0;
+
+      // ---- store: bf16 rows directly, or through the split-K workspace
+      const int n0 = n_t * kBN + half * kCols;
+      uint16_t* out_row = p.out + (size_t)row * p.N;
+      const uint16_t* res_row = p.residual ? p.residual + (size_t)row * p.N : nullptr;
+      if (kb0 == 0 && kb1 == p.KB) {  // the whole tile
+        if (live && !aborted) {
+#pragma unroll
+          for (int j = 0; j < kCols / 8; ++j) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = acc[8 * j + e];
+            store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
+          }
+        }
+      } else {
+        // a piece of the tile: partial slice (CTA, 0 for its first tile / 1 for its
+        // last), float4 j of promotion thread i at [j][i], so that a warp's 32
+        // lanes store 512 contiguous bytes
+        const int pid = tid - 64;  // promotion thread index 0 .. kPromo-1
+        auto slice = [&](long long cta, int slot) {
+          return reinterpret_cast<float4*>(p.partial) + ((size_t)cta * 2 + slot) * (kCols / 4) * kPromo + pid;
+        };
+        auto owner = [&](long long L) { return ((L + 1) * G - 1) / p.total; };  // the CTA whose range holds L
+        if (!aborted) {
+          float4* dst = slice(blockIdx.x, t == my_first_tile ? 0 : 1);
+#pragma unroll
+          for (int j = 0; j < kCols / 4; ++j)
+            dst[(size_t)j * kPromo] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+        }
+        __threadfence();
+        promo_sync();
+        const long long tl = (long long)t * p.KB;
+        const long long c_first = owner(tl), c_last = owner(tl + p.KB - 1);
+        if (tid == 2 * 32)
+          flags[1] = aborted ? 0 : (atomicAdd(p.tile_cnt + t, 1) == (int)(c_last - c_first));
+        promo_sync();
+        if (flags[1] != 0) {  // this CTA finished the tile's last piece: add the others
+          __threadfence();
+          for (long long c2 = c_first; c2 <= c_last; ++c2) {
+            if (c2 == blockIdx.x) continue;
+            const int first_t = (int)((c2 * p.total / G) / p.KB);
+            const float4* src = slice(c2, t == first_t ? 0 : 1);
+#pragma unroll
+            for (int j = 0; j < kCols / 4; ++j) {
+              const float4 v = __ldcg(src + (size_t)j * kPromo);
+              acc[4 * j] += v.x; acc[4 * j + 1] += v.y; acc[4 * j + 2] += v.z; acc[4 * j + 3] += v.w;
+            }
+          }
+          if (live) {
+#pragma unroll
+            for (int j = 0; j < kCols / 8; ++j) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = acc[8 * j + e];
+              store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
+            }
+          }
+          if (tid == 2 * 32) p.tile_cnt[t] = 0;
+        }
+        promo_sync();  // flags[1] is rewritten by the next piece
+      }
+    }
+  }
+
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  if (warp == 1) umma::tmem_dealloc(tm, kTmemCols);
+}
+
+bool encode_u8(CUtensorMap* m, const void* base, int rows, int cols) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint32_t box[2] = {kBK, 128};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+// Stream-K (equal K-block ranges) when the tiles make fewer than two waves.
+struct Plan8 {
+  bool stream_k;
+  long long tiles, total;
+  int grid;
+};
+
+Plan8 plan_fp8(int T, int N, int K, int sms) {
+  Plan8 pl;
+  pl.tiles = (long long)((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  pl.total = pl.tiles * (K / kBK);
+  pl.stream_k = pl.tiles < 2LL * sms && pl.total > pl.tiles;
+  const long long work = pl.stream_k ? pl.total : pl.tiles;
+  pl.grid = (int)(work < sms ? work : sms);
+  return pl;
+}
+
+size_t fp8_gemm_workspace_bytes(int T, int N, int K) {
+  const Plan8 pl = plan_fp8(T, N, K, num_sms());
+  if (!pl.stream_k) return 0;
+  return (size_t)pl.grid * 2 * kBM * kBN * 4 + ((size_t)pl.tiles * 4 + 255) / 256 * 256;
+}
+
+cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                            cudaStream_t stream) {
+  if (o.T == 0) return cudaSuccess;
+  CUtensorMap tmx{}, tmw{};
+  if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K)) return cudaErrorInvalidValue;
+  Fp8GemmArgs a{};
+  a.xs = o.xs;
+  a.ws = o.ws;
+  a.residual = o.residual;
+  a.out = o.out;
+  a.dev_err = dev_err;
+  a.T = o.T;
+  a.N = o.N;
+  a.KB = o.K / kBK;
+  a.mt = (o.T + kBM - 1) / kBM;
+  a.nt = (o.N + kBN - 1) / kBN;
+  const int sms = num_sms();
+  Plan8 pl = plan_fp8(o.T, o.N, o.K, sms);
+  if (pl.stream_k && (!workspace || ws_bytes < fp8_gemm_workspace_bytes(o.T, o.N, o.K))) {
+    pl.stream_k = false;  // no room for the partial tiles: whole tiles only
+    pl.grid = (int)(pl.tiles < sms ? pl.tiles : sms);
+  }
+  a.stream_k = pl.stream_k ? 1 : 0;
+  a.tiles = pl.tiles;
+  a.total = pl.total;
+  if (pl.stream_k) {
+    a.partial = static_cast<float*>(workspace);
+    a.tile_cnt = reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) + (size_t)pl.grid * 2 * kBM * kBN * 4);
+  }
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_kernel), kSmemBytes);
+  if (err != cudaSuccess) return err;
+  fp8_gemm_kernel<<<pl.grid, kThreads, kSmemBytes, stream>>>(a, tmx, tmw);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

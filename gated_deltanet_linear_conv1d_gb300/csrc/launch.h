@@ -2,6 +2,8 @@
 // (api.cu) and the kernel files. Internal to libgdn.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -94,6 +96,50 @@ struct RmsArgs {
   int D;
 };
 
+struct QuantActArgs {
+  const uint16_t* x;  // [T][K] bf16
+  uint8_t* x8;        // [T][K] e4m3
+  float* scale;       // scale of (token t, group g) at t * scale_t + g * scale_g
+  long long scale_t, scale_g;
+  int T, K;
+};
+
+struct QuantWeightArgs {
+  const uint16_t* w;  // [N][K] bf16
+  uint8_t* w8;        // [N][K] e4m3
+  float* scale;       // scale of block (nb, kb) at nb * scale_n + kb * scale_k
+  long long scale_n, scale_k;
+  int N, K;
+};
+
+// Block-scaled FP8 GEMM: out[T][N] = dequant(x8) dequant(w8)^T (+ residual).
+struct Fp8Operands {
+  const uint8_t* x8;         // [T][K] e4m3
+  const float* xs;           // [T][K/128]
+  const uint8_t* w8;         // [N][K] e4m3
+  const float* ws;           // [ceil(N/128)][K/128]
+  const uint16_t* residual;  // [T][N] bf16 or nullptr
+  uint16_t* out;             // [T][N] bf16
+  int T, K, N;
+};
+
+struct Fp8GemmArgs {
+  const float* xs;
+  const float* ws;
+  const uint16_t* residual;
+  uint16_t* out;
+  float* partial;  // stream-K partial tiles [grid][2][128 x 128 fp32], or nullptr
+  int* tile_cnt;   // stream-K tickets [tiles] (zero on entry, left zero), or nullptr
+  int32_t* dev_err;
+  int T, N, KB;
+  int mt, nt;
+  int stream_k;          // 1: equal K-block ranges per CTA; 0: whole tiles, strided
+  long long tiles, total;  // output tiles; tiles x K blocks
+};
+
+// The driver's tensor-map encoder (resolved once).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (function, device).
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
@@ -120,5 +166,13 @@ cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, const void* resi
                           int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream, bool* unsupported);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream);
 cudaError_t launch_rmsnorm(const RmsArgs& a, cudaStream_t stream);
+cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream);
+cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream);
+// Workspace bytes for the split-K partial tiles of a [T][N] output with K inputs
+// (0 when the shape is not split on this device).
+size_t fp8_gemm_workspace_bytes(int T, int N, int K);
+// Launches the block-scaled FP8 GEMM; without enough workspace it runs one K split.
+cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                            cudaStream_t stream);
 
 }  // namespace gdn

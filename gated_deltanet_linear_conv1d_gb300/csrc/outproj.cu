@@ -40,19 +40,26 @@ LtCache& cache() {
   return *c;
 }
 
+// The device's library handle (created on first use; caller holds lc.mu).
+cublasStatus_t handle_locked(LtCache& lc, int dev, cublasLtHandle_t* h_out) {
+  auto hit = lc.handles.find(dev);
+  if (hit == lc.handles.end()) {
+    cublasLtHandle_t h = nullptr;
+    const cublasStatus_t st = cublasLtCreate(&h);
+    if (st != CUBLAS_STATUS_SUCCESS) return st;
+    hit = lc.handles.emplace(dev, h).first;
+  }
+  *h_out = hit->second;
+  return CUBLAS_STATUS_SUCCESS;
+}
+
 // Builds (once per shape) the descriptors and the heuristic's first algorithm.
 cublasStatus_t get_plan(int dev, int T, int K, int N, size_t ws_bytes, cudaDataType_t cd_type, cublasLtHandle_t* h_out,
                         Plan* out) {
   LtCache& lc = cache();
   std::lock_guard<std::mutex> lock(lc.mu);
-  cublasStatus_t st = CUBLAS_STATUS_SUCCESS;
-  auto hit = lc.handles.find(dev);
-  if (hit == lc.handles.end()) {
-    cublasLtHandle_t h = nullptr;
-    if ((st = cublasLtCreate(&h)) != CUBLAS_STATUS_SUCCESS) return st;
-    hit = lc.handles.emplace(dev, h).first;
-  }
-  *h_out = hit->second;
+  cublasStatus_t st = handle_locked(lc, dev, h_out);
+  if (st != CUBLAS_STATUS_SUCCESS) return st;
   const auto key = std::make_tuple(dev, T, K, N, ws_bytes, (int)cd_type);
   auto pit = lc.plans.find(key);
   if (pit != lc.plans.end()) {

@@ -39,9 +39,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t row_bytes
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) | (1ull << 46);
 }
 
+// Descriptor of a K-major tile written by TMA with 128-byte swizzling: rows of
+// 128 bytes, 8-row groups 1024 bytes apart (SBO), the tile 1024-byte aligned.
+// A step along K inside the 128-byte row advances the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
 // ---- instruction descriptors -------------------------------------------------
 
-enum : uint32_t { kBF16 = 1, kTF32 = 2 };
+// Operand type codes of the instruction descriptor: kind::f16 takes kBF16,
+// kind::tf32 takes kTF32, kind::f8f6f4 takes kE4M3 (E4M3 is code 0 there).
+enum : uint32_t { kE4M3 = 0, kBF16 = 1, kTF32 = 2 };
+// MMA kinds for the issue wrapper.
+enum : uint32_t { kKindF16 = 1, kKindTF32 = 2, kKindF8 = 3 };
 
 // kind::f16 (bf16 operands) or kind::tf32, fp32 accumulator, dense.
 __host__ __device__ constexpr uint32_t idesc(uint32_t ab_type, bool a_mn_major, bool b_mn_major, int M, int N) {
@@ -80,7 +92,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 template <uint32_t kKind>
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc_v,
                                     uint32_t accumulate) {
-  if constexpr (kKind == kTF32) {
+  if constexpr (kKind == kKindF8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc_v), "r"(accumulate)
+        : "memory");
+  } else if constexpr (kKind == kTF32) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -119,6 +137,23 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 32 consecutive columns of this thread's lane, raw bits, without waiting:
+// the registers hold the values only after the next wait_ld().
+__device__ __forceinline__ void ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive columns of this thread's lane.
 __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {

@@ -185,3 +185,12 @@ def spec_workload(dims: Dims, num_requests: int, num_pos: int = 4, seed: int = 4
     w.update(slot_pool(rng, dims, Rs))
     w["accepted"] = rng.integers(0, num_pos, size=num_requests).astype(np.int32)
     return w
+
+
+def fp8_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Random E4M3 bit patterns (uint8) with magnitudes from 0.25 up to 3.75: sign bit random,
+    exponent field 5..8, mantissa field 0..7. These are stored codes, not a quantisation of anything."""
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << 7
+    e = rng.integers(5, 9, size=shape, dtype=np.uint8) << 3
+    m = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    return (sign | e | m).astype(np.uint8)

@@ -325,6 +325,47 @@ gdn_status gdn_in_proj(const gdn_dims *dims, const uint16_t *hidden, int32_t hid
                        void *stream);
 
 /*
+ * FP8 block-scaled projections. Page "Qwen3.8-27B: from model structure to vLLM
+ * inference data flow", section 04 (precision and cache): the checkpoint's
+ * linear weights are FP8 E4M3 with one scale per 128 x 128 weight block and the
+ * activations are quantised to FP8 dynamically. A scale s dequantises its
+ * block: value = E4M3(code) * s. Both quantisers set s = max(amax, 1e-12) / 448
+ * (amax = the block's largest |x|, 448 = the largest finite E4M3 value) and
+ * code = E4M3(x / s) rounded to nearest even with saturation; the divisions
+ * are IEEE-rounded fp32, so the codes are reproducible bit for bit.
+ *
+ * gdn_fp8_quant_act - x [T][K] bf16 -> x8 [T][K] e4m3 and x_scale, one scale per
+ *   token and 128-wide group of K, stored [T][K/128] (group fastest). K a
+ *   multiple of 128; pointers 16-byte aligned.
+ * gdn_fp8_quant_weight - w [N][K] bf16 -> w8 [N][K] e4m3 and w_scale, one scale
+ *   per 128 x 128 block, stored [ceil(N/128)][K/128] (K block fastest); a last
+ *   partial row block takes the largest |w| of its rows. K a multiple of 128;
+ *   pointers 16-byte aligned.
+ * gdn_fp8_linear - out [T][N] = dequant(x8) dequant(w8)^T (+ residual [T][N]),
+ *   bf16 out; in place on the residual is allowed. x_scale [T][K/128] and
+ *   w_scale [ceil(N/128)][K/128] as the two quantisers write them. The tensor
+ *   cores form each 128-wide block product of K exactly (E4M3 products, fp32
+ *   sums) and fp32 registers take the scaled sum over blocks. K a multiple of
+ *   128, N a multiple of 16.
+ *   workspace: when K is split across CTAs, one fp32 partial tile per split
+ *   and a ticket per output tile, gdn_fp8_linear_workspace_bytes(T, K, N) bytes
+ *   (0: this shape is not split on the current GPU), 256-byte aligned and
+ *   ZERO-FILLED before its first use: the tickets must start at zero, and every
+ *   call that completes resets them, so the workspace is reusable without
+ *   clearing (after a call that reports a device error, clear it again). NULL or
+ *   too small: K is not split. Calls sharing one workspace must not overlap.
+ *   dev_err: GDN_DEVERR_TIMEOUT if a bounded wait inside the kernel ran out.
+ */
+gdn_status gdn_fp8_quant_act(const uint16_t *x, uint8_t *x8, float *x_scale, int32_t num_tokens, int32_t k,
+                             void *stream);
+gdn_status gdn_fp8_quant_weight(const uint16_t *w, uint8_t *w8, float *w_scale, int32_t n, int32_t k,
+                                void *stream);
+size_t gdn_fp8_linear_workspace_bytes(int32_t num_tokens, int32_t k, int32_t n);
+gdn_status gdn_fp8_linear(const uint8_t *x8, const float *x_scale, const uint8_t *w8, const float *w_scale,
+                          const uint16_t *residual, uint16_t *out, int32_t num_tokens, int32_t k, int32_t n,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
  * gdn_out_proj - the output projection after the mixer core and the residual
  * add: out = ogate W^T (+ residual), bf16 operands, fp32 accumulation, bf16
  * out (round to nearest even). Page: section 01 GDN operator table, the Wo row

@@ -245,6 +245,87 @@ def rmsnorm(x_bits, gamma, eps, residual_bits=None):
     return x / np.sqrt(ms + float(eps)) * np.asarray(gamma, dtype=np.float64), new_res
 
 
+# ---------------------------------------------------------------- FP8 E4M3 block-scaled projections
+# Page "Qwen3.8-27B: from model structure to vLLM inference data flow", section 04 (precision and
+# cache): the linear weights are FP8 E4M3 with one scale per 128 x 128 block and activations are
+# quantised dynamically. E4M3 here is the OCP FP8 format: 1 sign bit, 4 exponent bits with bias 7,
+# 3 mantissa bits, subnormals at exponent 0, no infinities, S.1111.111 the only NaN, 448 the largest
+# finite value.
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """E4M3 codes (uint8) to their values, straight from the bit fields."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_from_f32(v) -> np.ndarray:
+    """fp32 values to E4M3 codes: round to nearest, ties to even mantissa, magnitudes above 448
+    saturate to 448 (the value keeps its sign, zero included)."""
+    x = np.asarray(v, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))       # a = f 2^ex, 1/2 <= f < 1: binade 2^(ex-1)
+    e = np.clip(ex - 1, -6, 8)                      # below 2^-6 the spacing stays 2^-9 (subnormals)
+    q = np.ldexp(1.0, e - 3)                        # spacing of the binade: 3 mantissa bits
+    r = np.minimum(np.round(a / q) * q, 448.0)      # a / q is exact; np.round ties to even
+    _, rex = np.frexp(np.where(r > 0, r, 1.0))
+    normal = r >= 2.0 ** -6
+    E = np.where(normal, rex - 1 + 7, 0)
+    M = np.where(normal, r / np.ldexp(1.0, rex - 1) - 1.0, r / 2.0 ** -9)
+    M = np.where(normal, M * 8.0, M)
+    code = (E.astype(np.int64) << 3) | np.round(M).astype(np.int64)
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+
+
+def _fp8_block_scale(amax) -> np.ndarray:
+    """Block scale s = max(amax, 1e-12) / 448 as an IEEE fp32 division."""
+    return (np.maximum(np.asarray(amax, np.float32), np.float32(1e-12)) / np.float32(448.0)).astype(np.float32)
+
+
+def fp8_quant_act(x_bits):
+    """Dynamic activation quantisation: one scale per token and 128-wide group of K. x [T, K] bf16
+    bits -> (codes [T, K] uint8, scales [T, K/128] fp32); code = E4M3(x / s), the division in fp32."""
+    x = _bf16(x_bits).astype(np.float32)
+    T, K = x.shape
+    g = x.reshape(T, K // 128, 128)
+    s = _fp8_block_scale(np.abs(g).max(axis=2))
+    codes = e4m3_from_f32((g / s[:, :, None]).astype(np.float32))
+    return codes.reshape(T, K), s
+
+
+def fp8_quant_weight(w_bits):
+    """Weight quantisation with one scale per 128 x 128 block (a last partial row block takes the
+    largest magnitude of the rows it has). w [N, K] bf16 bits -> (codes [N, K], scales [ceil(N/128), K/128])."""
+    w = _bf16(w_bits).astype(np.float32)
+    N, K = w.shape
+    NB, KB = (N + 127) // 128, K // 128
+    codes = np.zeros((N, K), np.uint8)
+    s = np.zeros((NB, KB), np.float32)
+    for nb in range(NB):
+        for kb in range(KB):
+            blk = w[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+            s[nb, kb] = _fp8_block_scale(np.abs(blk).max())
+            codes[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128] = e4m3_from_f32((blk / s[nb, kb]).astype(np.float32))
+    return codes, s
+
+
+def fp8_linear(x8, x_scale, w8, w_scale, residual_bits=None):
+    """out = dequant(X) dequant(W)^T (+ residual) in fp64, dequant(X)[t, k] = E4M3(x8[t, k]) x_scale[t, k/128]
+    and dequant(W)[n, k] = E4M3(w8[n, k]) w_scale[n/128, k/128]."""
+    x = e4m3_to_f64(x8) * np.repeat(np.asarray(x_scale, np.float64), 128, axis=1)
+    ws = np.repeat(np.repeat(np.asarray(w_scale, np.float64), 128, axis=0), 128, axis=1)
+    w = e4m3_to_f64(w8) * ws[:w8.shape[0]]
+    out = x @ w.T
+    if residual_bits is not None:
+        out = out + _bf16(residual_bits)
+    return out
+
+
 def _round_bf16(x) -> np.ndarray:
     """fp64 values to bf16 bits, round to nearest, ties to even, straight from fp64 (one rounding):
     x = m 2^e with 1/2 <= |m| < 1, keep 8 significant bits of m (np.round breaks ties to even)."""

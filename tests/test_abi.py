@@ -114,3 +114,18 @@ def test_rmsnorm_rejects_bad_arguments_on_the_host(b):
     assert lib.gdn_rmsnorm(p, odd, p, 1e-6, p, 4, 5120, None) == b.GDN_ERR_INVALID_ARG  # residual not 16 B aligned
     assert lib.gdn_rmsnorm(None, None, p, 1e-6, p, 4, 5120, None) == b.GDN_ERR_INVALID_ARG
     assert lib.gdn_rmsnorm(None, None, None, 1e-6, None, 0, 5120, None) == b.GDN_OK
+
+
+def test_fp8_entry_points_reject_bad_arguments_on_the_host(b):
+    lib = b._lib
+    p, odd = ctypes.c_void_p(256), ctypes.c_void_p(264)  # never dereferenced
+    assert lib.gdn_fp8_quant_act(p, p, p, 4, 200, None) == b.GDN_ERR_UNSUPPORTED   # K not a multiple of 128
+    assert lib.gdn_fp8_quant_act(p, odd, p, 4, 256, None) == b.GDN_ERR_INVALID_ARG  # misaligned codes
+    assert lib.gdn_fp8_quant_act(None, None, None, 0, 256, None) == b.GDN_OK       # no tokens
+    assert lib.gdn_fp8_quant_weight(p, p, p, 16, 100, None) == b.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_fp8_quant_weight(p, p, None, 16, 128, None) == b.GDN_ERR_INVALID_ARG
+    assert lib.gdn_fp8_linear(p, p, p, p, None, p, 4, 128, 24, None, 0, None, None) == b.GDN_ERR_UNSUPPORTED  # N % 16
+    assert lib.gdn_fp8_linear(p, p, p, p, None, p, 4, 130, 32, None, 0, None, None) == b.GDN_ERR_UNSUPPORTED  # K % 128
+    assert lib.gdn_fp8_linear(p, p, p, p, odd, p, 4, 128, 32, None, 0, None, None) == b.GDN_ERR_INVALID_ARG
+    assert lib.gdn_fp8_linear(None, None, None, None, None, None, 0, 128, 32, None, 0, None, None) == b.GDN_OK
+    assert lib.gdn_fp8_linear_workspace_bytes(256, 100, 5120) == 0  # K not a multiple of 128

@@ -1,0 +1,126 @@
+"""Block-scaled FP8 projections (the checkpoint format of section 04 of the Qwen3.8-27B page:
+E4M3 weights with one scale per 128 x 128 block, activations quantised per token and 128-wide
+group) against the fp64 oracle: the quantisers bit for bit (codes and scales), the tcgen05 GEMM
+element by element over ragged shapes, the split-K path at the layer's decode shapes, reuse of
+the workspace without clearing, and quantise-then-multiply end to end."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from tests import gdnutil as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def b():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from gated_deltanet_linear_conv1d_gb300 import build
+    build.build()
+    from gated_deltanet_linear_conv1d_gb300 import binding
+    return binding
+
+
+def _dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.uint8)).cuda()
+
+
+@pytest.mark.parametrize("T,K", [(1, 128), (37, 384), (256, 6144), (1000, 5120)])
+def test_quant_act_bit_exact(b, T, K):
+    rng = np.random.default_rng(200 + T)
+    x = rng.normal(size=(T, K)).astype(np.float32) * rng.uniform(0.01, 30.0, size=(T, 1)).astype(np.float32)
+    x[0, :128] = 0.0  # an all-zero group
+    xb = U.synth.bf16_bits(x)
+    x8 = torch.zeros((T, K), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((T, K // 128), dtype=torch.float32, device="cuda")
+    b.gdn_fp8_quant_act(U.dev_bf16(xb), x8, xs)
+    codes, s = oracle.fp8_quant_act(xb)
+    np.testing.assert_array_equal(xs.cpu().numpy(), s)
+    np.testing.assert_array_equal(x8.cpu().numpy(), codes)
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (200, 256), (5120, 6144)])
+def test_quant_weight_bit_exact(b, N, K):
+    rng = np.random.default_rng(300 + N)
+    w = (rng.normal(size=(N, K)) / np.sqrt(K)).astype(np.float32)
+    wb = U.synth.bf16_bits(w)
+    w8 = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(((N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    b.gdn_fp8_quant_weight(U.dev_bf16(wb), w8, ws)
+    codes, s = oracle.fp8_quant_weight(wb)
+    np.testing.assert_array_equal(ws.cpu().numpy(), s)
+    np.testing.assert_array_equal(w8.cpu().numpy(), codes)
+
+
+def _operands(T, K, N, seed):
+    rng = np.random.default_rng(seed)
+    x8 = U.synth.fp8_codes(rng, (T, K))
+    w8 = U.synth.fp8_codes(rng, (N, K))
+    xs = rng.uniform(0.002, 0.02, size=(T, K // 128)).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-3, size=((N + 127) // 128, K // 128)).astype(np.float32)
+    r = U.synth.bf16_bits(rng.normal(size=(T, N)).astype(np.float32))
+    return x8, xs, w8, ws, r
+
+
+@pytest.mark.parametrize("T,K,N,res,with_ws", [
+    (1, 128, 16, False, True),        # one tile, one K block
+    (130, 256, 144, True, True),      # ragged m and n tiles
+    (300, 1024, 384, False, False),   # no workspace: one K split
+    (256, 6144, 5120, True, True),    # Wo at the decode batch: split K
+    (256, 5120, 10240, False, True),  # the QKV projection at the decode batch: split K
+    (2000, 768, 256, True, True),     # many m tiles
+])
+def test_fp8_linear_matches_oracle(b, T, K, N, res, with_ws):
+    x8, xs, w8, ws, r = _operands(T, K, N, 400 + T + N)
+    out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda") if with_ws else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.gdn_fp8_linear(_dev_u8(x8), U.dev(xs), _dev_u8(w8), U.dev(ws), out, residual=U.dev_bf16(r) if res else None,
+                     workspace=wsp, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    ref = oracle.fp8_linear(x8, xs, w8, ws, r if res else None)
+    U.check_out(U.host_f64_from_bf16(out), ref, "out")
+
+
+def test_fp8_linear_repeat_and_in_place(b):
+    """Two calls on one workspace give the same result; out may be the residual itself."""
+    T, K, N = 256, 6144, 5120
+    x8, xs, w8, ws, r = _operands(T, K, N, 450)
+    wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda")
+    args = (_dev_u8(x8), U.dev(xs), _dev_u8(w8), U.dev(ws))
+    out1 = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    b.gdn_fp8_linear(*args, out1, workspace=wsp)
+    b.gdn_fp8_linear(*args, out2, workspace=wsp)
+    ref = oracle.fp8_linear(x8, xs, w8, ws)
+    U.check_out(U.host_f64_from_bf16(out1), ref, "first call")
+    U.check_out(U.host_f64_from_bf16(out2), ref, "second call")
+    hidden = U.dev_bf16(r)
+    b.gdn_fp8_linear(*args, hidden, residual=hidden, workspace=wsp)
+    U.check_out(U.host_f64_from_bf16(hidden), oracle.fp8_linear(x8, xs, w8, ws, r), "in place")
+
+
+def test_quantise_then_multiply_end_to_end(b):
+    """bf16 Ogate and Wo quantised on the GPU, multiplied on the GPU, against the oracle doing the
+    same steps; and the FP8 result stays within the quantisation error of the bf16 product."""
+    T, K, N = 128, 6144, 1024
+    rng = np.random.default_rng(460)
+    xb = U.synth.bf16_bits(rng.normal(size=(T, K)).astype(np.float32))
+    wb = U.synth.bf16_bits((rng.normal(size=(N, K)) / np.sqrt(K)).astype(np.float32))
+    x8 = torch.zeros((T, K), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((T, K // 128), dtype=torch.float32, device="cuda")
+    w8 = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros((N // 128, K // 128), dtype=torch.float32, device="cuda")
+    b.gdn_fp8_quant_act(U.dev_bf16(xb), x8, xs)
+    b.gdn_fp8_quant_weight(U.dev_bf16(wb), w8, ws)
+    out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda")
+    b.gdn_fp8_linear(x8, xs, w8, ws, out, workspace=wsp)
+    cx, sx = oracle.fp8_quant_act(xb)
+    cw, sw = oracle.fp8_quant_weight(wb)
+    ref = oracle.fp8_linear(cx, sx, cw, sw)
+    U.check_out(U.host_f64_from_bf16(out), ref, "fp8 path")
+    exact = oracle.out_proj(xb, wb)
+    assert U.rel_l2(ref, exact) < 0.06  # E4M3 keeps 3 mantissa bits: a few percent of quantisation error

@@ -459,3 +459,74 @@ def test_rmsnorm_scale_invariance_and_unit_rms():
     u4, _ = oracle.rmsnorm(_bits(4.0 * synth.bf16_to_f32(x)), g, 0.0)
     np.testing.assert_allclose(u4, u, rtol=1e-14)
     np.testing.assert_allclose(np.mean((u / g) ** 2, axis=1), 1.0, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- FP8 E4M3 block-scaled projections
+
+def test_e4m3_codes_decode_to_the_format_values():
+    """OCP E4M3: exponent bias 7, 3 mantissa bits, subnormal step 2^-9, largest finite 448,
+    S.1111.111 the only NaN, sign-magnitude (0x80 is -0)."""
+    got = oracle.e4m3_to_f64([0x00, 0x01, 0x07, 0x08, 0x38, 0x3C, 0x40, 0x7E, 0xB8, 0x80])
+    np.testing.assert_array_equal(got, [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 1.5, 2.0, 448.0, -1.0, 0.0])
+    assert np.signbit(got[-1])
+    assert np.isnan(oracle.e4m3_to_f64([0x7F, 0xFF])).all()
+    # 254 finite codes, all distinct values apart from +-0
+    v = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    fin = v[~np.isnan(v)]
+    assert fin.size == 254 and np.unique(fin).size == 253
+
+
+def test_e4m3_encoding_rounds_to_nearest_even_and_saturates():
+    """Every finite code survives decode -> encode; ties worked by hand go to the even mantissa:
+    1 + 1/16 -> 1 (0x38), 1 + 3/16 -> 1.25 (0x3A), 2^-10 -> 0, 3 * 2^-10 -> 2^-8 (0x02);
+    magnitudes past 448 saturate (0x7E / 0xFE)."""
+    codes = np.arange(256, dtype=np.uint8)
+    v = oracle.e4m3_to_f64(codes)
+    fin = ~np.isnan(v)
+    np.testing.assert_array_equal(oracle.e4m3_from_f32(v[fin].astype(np.float32)), codes[fin])
+    got = oracle.e4m3_from_f32(np.array([1 + 1 / 16, 1 + 3 / 16, 2.0 ** -10, 3 * 2.0 ** -10, 500.0, -1e6, 447.0],
+                                        np.float32))
+    np.testing.assert_array_equal(got, np.array([0x38, 0x3A, 0x00, 0x02, 0x7E, 0xFE, 0x7E], np.uint8))
+
+
+def test_fp8_quantisers_scale_and_error_bound():
+    """A group whose largest magnitude is 448 gets scale 1 and the plain codes; an all-zero group gets
+    codes 0 and scale fp32(1e-12)/448; every code is within half a step of x / s (3 mantissa bits:
+    relative 2^-4, absolute 2^-10 in the subnormal range); the weight blocks follow the same rule."""
+    rng = np.random.default_rng(73)
+    x = rng.normal(size=(3, 384)).astype(np.float32)
+    x[0, :128] = np.clip(x[0, :128] * 100.0, -440.0, 440.0)
+    x[0, 5] = -448.0
+    x[1, 128:256] = 0.0
+    xb = _bits(x)
+    codes, s = oracle.fp8_quant_act(xb)
+    xv = synth.bf16_to_f32(xb).astype(np.float64)
+    assert s[0, 0] == np.float32(1.0)
+    np.testing.assert_array_equal(codes[0, :128], oracle.e4m3_from_f32(xv[0, :128].astype(np.float32)))
+    assert np.all(codes[1, 128:256] == 0) and s[1, 1] == np.float32(np.float32(1e-12) / np.float32(448.0))
+    deq = oracle.e4m3_to_f64(codes) * np.repeat(s.astype(np.float64), 128, axis=1)
+    ratio = xv / np.repeat(s.astype(np.float64), 128, axis=1)
+    assert np.all(np.abs(ratio) <= 448.0 * (1 + 1e-6))
+    assert np.all(np.abs(deq - xv) <= np.repeat(s.astype(np.float64), 128, axis=1) *
+                  (2.0 ** -4 * np.abs(ratio) + 2.0 ** -10) + 1e-30)
+    w = rng.normal(size=(200, 256)).astype(np.float32)
+    wc, ws = oracle.fp8_quant_weight(_bits(w))
+    assert ws.shape == (2, 2)
+    wv = synth.bf16_to_f32(_bits(w)).astype(np.float64)
+    for nb in range(2):
+        for kb in range(2):
+            blk = wv[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+            assert ws[nb, kb] == np.float32(np.float32(np.abs(blk).max()) / np.float32(448.0))
+
+
+def test_fp8_linear_hand_example():
+    """K = 256 (two scale blocks), one token, one output: codes 1.0 and 0.5, block scales chosen by
+    hand: out = 128 * (1 * 0.5) * (2 * 3) + 128 * (1 * 0.5) * (4 * 0.25) = 384 + 64 = 448."""
+    x8 = np.full((1, 256), 0x38, np.uint8)
+    w8 = np.full((16, 256), 0x30, np.uint8)  # 0.5
+    xs = np.array([[2.0, 4.0]], np.float32)
+    ws = np.array([[3.0, 0.25]], np.float32)
+    out = oracle.fp8_linear(x8, xs, w8, ws)
+    np.testing.assert_array_equal(out, np.full((1, 16), 448.0))
+    r = np.full((1, 16), -48.0)
+    np.testing.assert_array_equal(oracle.fp8_linear(x8, xs, w8, ws, _bits(r)), np.full((1, 16), 400.0))
