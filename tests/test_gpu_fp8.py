@@ -124,3 +124,19 @@ def test_quantise_then_multiply_end_to_end(b):
     U.check_out(U.host_f64_from_bf16(out), ref, "fp8 path")
     exact = oracle.out_proj(xb, wb)
     assert U.rel_l2(ref, exact) < 0.06  # E4M3 keeps 3 mantissa bits: a few percent of quantisation error
+
+
+@pytest.mark.parametrize("T,K,N,res", [(1, 6144, 5120, True), (16, 256, 144, False), (100, 5120, 6144, True),
+                                       (256, 5120, 96 * 2, False), (257, 1024, 256, False)])
+def test_fp8_linear_decode_batches(b, T, K, N, res):
+    """Decode-sized token counts (one to three m tiles, stream-K over the K blocks): a single token,
+    ragged tiles, the a|b width, and a ragged third m tile; the workspace is reused without clearing."""
+    x8, xs, w8, ws, r = _operands(T, K, N, 470 + T + N)
+    out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace without clearing it
+        b.gdn_fp8_linear(_dev_u8(x8), U.dev(xs), _dev_u8(w8), U.dev(ws), out,
+                         residual=U.dev_bf16(r) if res else None, workspace=wsp, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    U.check_out(U.host_f64_from_bf16(out), oracle.fp8_linear(x8, xs, w8, ws, r if res else None), "out")
