@@ -14,10 +14,13 @@
 // Design. The path is bound by HBM bandwidth: nearly all of its bytes are the
 // fp32 state read and written back. The kernel keeps the state stream
 // continuous:
-//  - one CTA per SM, each owning a contiguous range of work units; a unit is
-//    (request n, key head j) with its G = Hv/Hk value heads, so the unit owns
+//  - one CTA per SM, claiming work units from a device-wide counter (one unit
+//    ahead, so the claim's latency stays off the stream) until none is left,
+//    so SMs that stream faster take more units and all finish together; a unit
+//    is (request n, key head j) with its G = Hv/Hk value heads, so the unit owns
 //    the conv channels of q_j, k_j and its value heads outright (the in-place
-//    history update needs no cross-CTA ordering);
+//    history update needs no cross-CTA ordering). The counter is one of a small
+//    static array, chosen per stream, and the last CTA to finish resets it;
 //  - a producer warp streams the unit's 2G half-tiles of state (64 rows x 128
 //    fp32 = 32 KiB each) through a ring of shared-memory stages with bulk (TMA)
 //    copies completing on mbarriers, running ahead of the consumers; it also
@@ -35,6 +38,9 @@
 //    rate.
 // Every wait is bounded: a stalled copy sets GDN_DEVERR_TIMEOUT and the CTA
 // leaves instead of hanging.
+#include <mutex>
+#include <unordered_map>
+
 #include "device.cuh"
 #include "launch.h"
 
@@ -53,6 +59,8 @@ constexpr uint32_t kHalfBytes = kHalfFloats * 4;           // 32 KiB
 constexpr int kRowsPerWarp = kHalfRows / kConsumerWarps;   // 4: lanes 8r..8r+7 share row r
 constexpr float kInvSqrtDk = 0.08838834764831845f;         // 1/sqrt(128)
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kSchedSlots = 64;  // unit counters, one per stream in use
+constexpr int kIdRing = 4;       // claimed unit ids in flight (two iterations ahead)
 
 // Dynamic shared-memory layout for group size G and P positions (byte offsets,
 // 16-byte aligned). The stage ring takes what the rest leaves, up to 6 stages.
@@ -70,7 +78,7 @@ struct Layout {
     o = rest;        rest += G * P * kHeadDim * 4;          // [G][P][128] fp32
     red = rest;      rest += (P * 16 + G * P * 4) * 4;      // [P][16] norm and [G*P][4] RMS partial sums
     ab = rest;       rest += kMaxGroup * kMaxPos * 4 * 4 + kMaxPos * 4;  // [G][P][4] alpha, beta; [P] output slots
-    bars = rest;     rest += (2 * kMaxStages + 4) * 8 + 16; // mbarriers + abort flag
+    bars = rest;     rest += (2 * kMaxStages + 8) * 8 + 32; // mbarriers + abort flag + claimed unit ids
     stages = (kSmemLimit - rest) / (int)kHalfBytes;
     if (stages > kMaxStages) stages = kMaxStages;
     const int off = stages * (int)kHalfBytes;
@@ -109,10 +117,13 @@ __device__ __forceinline__ bool unit_slots_ok(const StepArgs& p, int n) {
   return true;
 }
 
+// Unit counters: [slot][0] = next unit to claim, [slot][1] = CTAs finished.
+// Both are zero between launches (the last CTA of a launch resets them).
+__device__ int g_unit_counter[kSchedSlots * 2];
+
 // kOne: exactly one position (decode), so the per-position vectors are loaded once per unit.
 template <bool kOne>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, const int units_per_cta,
-                                                             const int extra) {
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, const int units, const int sched) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int G = p.G, P = kOne ? 1 : p.P;
   const Layout L(G, P);
@@ -131,15 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
   uint64_t* empty = full + kMaxStages;
   uint64_t* in_full = empty + kMaxStages;
   uint64_t* in_empty = in_full + 2;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(in_empty + 2);
+  uint64_t* id_full = in_empty + 2;  // [kIdRing] a claimed unit id is in uid[i % kIdRing]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(id_full + kIdRing);
+  volatile int* uid = reinterpret_cast<volatile int*>(id_full + kIdRing) + 1;  // [kIdRing], -1: none left
+  int* counter = g_unit_counter + 2 * sched;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nseg = 2 + G;
   const int xrow_len = nseg * kHeadDim;  // bf16 per position in the x buffer
-  // contiguous range of units: the first `extra` CTAs take one more
-  const int c = blockIdx.x;
-  const int u0 = c * units_per_cta + min(c, extra);
-  const int nunits = units_per_cta + (c < extra ? 1 : 0);
   const bool want_z = p.ogate != nullptr;  // z may be NULL when only o is written
 
   if (tid == 0) {
@@ -151,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
       mbar_init(&in_full[b], 1);
       mbar_init(&in_empty[b], 1);
     }
+    for (int r = 0; r < kIdRing; ++r) mbar_init(&id_full[r], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -161,9 +172,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
     if (lane != 0) return;
     const uint64_t pol = l2_policy_evict_first();
     int t = 0, kin = 0;
-    for (int i = 0; i < nunits && !*abort_flag; ++i) {
-      const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
-      if (!unit_slots_ok(p, n)) continue;  // the consumers skip the same unit
+    for (int i = 0; !*abort_flag; ++i) {
+      // the unit the consumers claimed for their i-th iteration
+      if (!mbar_wait_bounded(&id_full[i % kIdRing], (i / kIdRing) & 1)) { *abort_flag = 1; break; }
+      const int u = uid[i % kIdRing];
+      if (u < 0) break;
+      const int n = u / p.Hk, j = u % p.Hk;
+      if (!unit_slots_ok(p, n)) {  // the consumers skip the same unit: an empty hand-over
+        const int b = kin & 1;
+        if (!mbar_wait_bounded(&in_empty[b], ((kin >> 1) & 1) ^ 1)) { *abort_flag = 1; break; }
+        mbar_arrive(&in_full[b]);
+        ++kin;
+        continue;
+      }
       const int slot = p.slot_idx[n];
       const int b = kin & 1;
       if (!mbar_wait_bounded(&in_empty[b], ((kin >> 1) & 1) ^ 1)) { *abort_flag = 1; break; }
@@ -217,11 +238,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
   int* out_slot = reinterpret_cast<int*>(ab + kMaxGroup * kMaxPos * 4);  // [P] slot written after position q
   bool dead = false;
   int t = 0, kin = 0;
-  // the next unit's slot and (threads < G*P) its alpha, beta are loaded one unit ahead
+  // Units are claimed two iterations ahead by consumer thread 0 (uid[i %
+  // kIdRing] for iteration i, announced to the producer on id_full), so both
+  // the producer and the consumers find the next unit's id already there; the
+  // next unit's slot and (threads < G*P) its alpha, beta are loaded one unit
+  // ahead.
+  auto claim = [&](int i) {
+    if (ctid == 0) {
+      const int u = atomicAdd(counter, 1);
+      uid[i % kIdRing] = u < units ? u : -1;
+      mbar_arrive(&id_full[i % kIdRing]);
+    }
+  };
   int slot_nx = -1, oslot_nx = -1;
   float a_nx = 0.f, b_nx = 0.f;
-  auto prefetch = [&](int i) {
-    const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
+  auto prefetch = [&](int u) {
+    const int n = u / p.Hk, j = u % p.Hk;
     slot_nx = p.slot_idx[n];
     if (p.spec_slot && ctid < P) oslot_nx = p.spec_slot[n * P + ctid];
     if (ctid < G * P) {
@@ -230,27 +262,39 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
       b_nx = p.beta[ai];
     }
   };
-  if (nunits > 0) prefetch(0);
-  for (int i = 0; i < nunits; ++i) {
-    const int u = u0 + i, n = u / p.Hk, j = u % p.Hk;
+  claim(0);
+  claim(1);
+  consumer_sync();
+  int u_nx = uid[0];
+  if (u_nx >= 0) prefetch(u_nx);
+  for (int i = 0; u_nx >= 0; ++i) {
+    const int u = u_nx, n = u / p.Hk, j = u % p.Hk;
     const int slot = slot_nx, oslot_cur = oslot_nx;
     const float a_cur = a_nx, b_cur = b_nx;
-    if (i + 1 < nunits) prefetch(i + 1);
-    if (slot < 0 || slot >= p.Rs || (p.spec_slot && !unit_slots_ok(p, n))) {
-      if (ctid == 0 && slot >= 0) report(p.dev_err, GDN_DEVERR_SLOT);
-      continue;
-    }
+    u_nx = uid[(i + 1) % kIdRing];  // claimed in the previous iteration, visible since its barriers
+    if (u_nx >= 0) prefetch(u_nx);
+    claim(i + 2);
     const int b = kin & 1;
-    if (ctid < G * P) {
-      ab[ctid * 4 + 0] = a_cur;  // [g][q] with g = ctid / P, q = ctid % P
-      ab[ctid * 4 + 1] = b_cur;
+    const bool skip = slot < 0 || slot >= p.Rs || (p.spec_slot && !unit_slots_ok(p, n));
+    if (!skip) {
+      if (ctid < G * P) {
+        ab[ctid * 4 + 0] = a_cur;  // [g][q] with g = ctid / P, q = ctid % P
+        ab[ctid * 4 + 1] = b_cur;
+      }
+      if (ctid < P) out_slot[ctid] = p.spec_slot ? oslot_cur : slot;
     }
-    if (ctid < P) out_slot[ctid] = p.spec_slot ? oslot_cur : slot;
     dead = dead || *abort_flag;
     if (!dead && !mbar_wait_bounded(&in_full[b], (kin >> 1) & 1)) {
       dead = true;
       *abort_flag = 1;
       report(p.dev_err, GDN_DEVERR_TIMEOUT);
+    }
+    if (skip) {  // a bad or padding slot: the producer handed over nothing
+      if (ctid == 0 && slot >= 0) report(p.dev_err, GDN_DEVERR_SLOT);
+      consumer_sync();
+      if (ctid == 0) mbar_arrive(&in_empty[b]);
+      ++kin;
+      continue;
     }
     // ---- conv + SiLU of the unit's channels for every position; the history
     // after each position goes to its checkpoint slot (verify), or the final
@@ -432,6 +476,32 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs p, c
     if (ctid == 0) mbar_arrive(&in_empty[b]);
     ++kin;
   }
+  // the last CTA to finish leaves the counter at zero for the next launch
+  consumer_sync();
+  if (ctid == 0) {
+    __threadfence();
+    if (atomicAdd(counter + 1, 1) == (int)gridDim.x - 1) {
+      counter[0] = 0;
+      counter[1] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// Counter slot of a stream: streams get slots in order of first use (wrapping
+// after kSchedSlots streams), so launches on one stream share a slot (they run
+// one after the other) and launches on different streams use different slots.
+int sched_slot(cudaStream_t stream) {
+  static std::mutex mu;
+  static std::unordered_map<cudaStream_t, int> slots;
+  static int next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = slots.find(stream);
+  if (it != slots.end()) return it->second;
+  const int s = next;
+  next = (next + 1) % kSchedSlots;
+  slots.emplace(stream, s);
+  return s;
 }
 
 int sm_count() {
@@ -461,9 +531,9 @@ cudaError_t launch_stream(const StepArgs& a, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = units < sms ? units : sms;
-  const int per = units / grid, extra = units % grid;
-  if (one) stream_kernel<true><<<grid, kThreads, L.total, stream>>>(a, per, extra);
-  else stream_kernel<false><<<grid, kThreads, L.total, stream>>>(a, per, extra);
+  const int sched = sched_slot(stream);
+  if (one) stream_kernel<true><<<grid, kThreads, L.total, stream>>>(a, units, sched);
+  else stream_kernel<false><<<grid, kThreads, L.total, stream>>>(a, units, sched);
   return cudaGetLastError();
 }
 

@@ -131,6 +131,14 @@ gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *x, const float 
  *   alpha, beta [N][Hv] fp32;  z [N][Hv][dv] bf16;  gamma [dv] fp32;  eps >= 0
  *   o         [N][Hv][dv] bf16 out, or NULL
  *   ogate     [N][Hv*dv] bf16 out, or NULL (at least one of o, ogate)
+ *
+ * Scheduling: the kernel's CTAs claim (request, key head) units from a device
+ * counter that the library keeps per stream (a static array of 64, given to
+ * streams in order of first use and reused round-robin after that). Calls on
+ * one stream run one after another; calls that run at the same time must be
+ * on streams holding different counters, i.e. at most 64 streams in use. A
+ * captured graph keeps the counter of the stream it was captured on. The same
+ * holds for gdn_spec_verify.
  */
 gdn_status gdn_decode_step(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
                            uint16_t *conv_hist, float *state, const int32_t *slot_idx,
