@@ -16,6 +16,11 @@
 // computed). Every other thread starts a request at token t0 + 3 or later,
 // where the window is made of raw inputs only, so the history of a slot is read
 // and written by one thread and the in-place update needs no ordering.
+//
+// Written plainly the kernel is bound by instruction issue, not by HBM (ncu:
+// 77 % issue-active at 56 % of DRAM bandwidth), so the window is kept as floats
+// (one unpack per new input), SiLU takes one tanh.approx instead of an
+// exponential and a division, and pairs are packed with one bf16x2 conversion.
 #include "device.cuh"
 #include "launch.h"
 
@@ -29,8 +34,20 @@ constexpr int kBatch = 8;      // token rows loaded together by a thread
 __device__ __forceinline__ float lo_f(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float hi_f(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Two floats to a bf16 pair (round to nearest even), a in the low half.
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-  return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// SiLU(x) = x sigmoid(x) = (x/2)(1 + tanh(x/2)): one tanh.approx instead of an
+// exponential and a division (the result is rounded to bf16 next).
+__device__ __forceinline__ float silu_tanh(float x) {
+  const float h = 0.5f * x;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
 }
 
 // Largest n in [0, N) with qsl[n] <= t (offsets assumed non-decreasing; stays in
@@ -49,13 +66,13 @@ struct Quad {
   uint32_t a, b;
 };
 
-__device__ __forceinline__ uint32_t conv_pair(uint32_t xv, uint32_t w2, uint32_t w1, uint32_t w0, const float4& wl,
-                                              const float4& wh) {
-  float pl = wl.x * lo_f(xv), ph = wh.x * hi_f(xv);
-  pl = fmaf(wl.y, lo_f(w2), pl); ph = fmaf(wh.y, hi_f(w2), ph);
-  pl = fmaf(wl.z, lo_f(w1), pl); ph = fmaf(wh.z, hi_f(w1), ph);
-  pl = fmaf(wl.w, lo_f(w0), pl); ph = fmaf(wh.w, hi_f(w0), ph);
-  return pack2(silu(pl), silu(ph));
+// One channel: window f0 (oldest) .. f2 (newest) plus the new input x.
+__device__ __forceinline__ float conv1(float x, float f2, float f1, float f0, const float4& w) {
+  float pre = w.x * x;
+  pre = fmaf(w.y, f2, pre);
+  pre = fmaf(w.z, f1, pre);
+  pre = fmaf(w.w, f0, pre);
+  return silu_tanh(pre);
 }
 
 // History of two channels (lo, hi) as three words [l0 l1] [l2 h0] [h1 h2] <->
@@ -120,6 +137,16 @@ __global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p, int se
         a0 = v0.x; a1 = v1.x; a2 = v2.x;
         b0 = v0.y; b1 = v1.y; b2 = v2.y;
       }
+      // the windows as floats, channel e of the four at f[e][0 (oldest) .. 2]
+      float f[4][3];
+      {
+        const uint32_t wa[3] = {a0, a1, a2}, wb[3] = {b0, b1, b2};
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          f[0][k] = lo_f(wa[k]); f[1][k] = hi_f(wa[k]);
+          f[2][k] = lo_f(wb[k]); f[3][k] = hi_f(wb[k]);
+        }
+      }
       // kBatch tokens at a time: all loads first, so they are in flight together
       for (int tb = start; tb < end; tb += kBatch) {
         const int nt = min(kBatch, end - tb);
@@ -129,14 +156,24 @@ __global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p, int se
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
           if (i < nt) {
-            uint2 o;
-            o.x = conv_pair(xv[i].x, a2, a1, a0, w[0], w[1]);
-            o.y = conv_pair(xv[i].y, b2, b1, b0, w[2], w[3]);
-            y[(size_t)(tb + i) * ld] = o;
-            a0 = a1; a1 = a2; a2 = xv[i].x;
-            b0 = b1; b1 = b2; b2 = xv[i].y;
+            const float xn[4] = {lo_f(xv[i].x), hi_f(xv[i].x), lo_f(xv[i].y), hi_f(xv[i].y)};
+            float r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              r[e] = conv1(xn[e], f[e][2], f[e][1], f[e][0], w[e]);
+              f[e][0] = f[e][1]; f[e][1] = f[e][2]; f[e][2] = xn[e];
+            }
+            y[(size_t)(tb + i) * ld] = make_uint2(pack2(r[0], r[1]), pack2(r[2], r[3]));
           }
         }
+      }
+      // packed windows back from the floats (exact: they hold bf16 values)
+      if (owner) {
+        auto bits = [](float v) { return __float_as_uint(v) >> 16; };
+        a0 = bits(f[0][0]) | (bits(f[1][0]) << 16); a1 = bits(f[0][1]) | (bits(f[1][1]) << 16);
+        a2 = bits(f[0][2]) | (bits(f[1][2]) << 16);
+        b0 = bits(f[2][0]) | (bits(f[3][0]) << 16); b1 = bits(f[2][1]) | (bits(f[3][1]) << 16);
+        b2 = bits(f[2][2]) | (bits(f[3][2]) << 16);
       }
       if (owner) {
         if (end < t1) {  // longer than computed here (so at least 4 tokens)

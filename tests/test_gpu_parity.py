@@ -143,6 +143,29 @@ def test_decode_padding_and_bad_slot(b):
     torch.cuda.synchronize()
 
 
+def test_decode_on_two_streams_at_once(b):
+    """Two decode steps on different streams run at the same time (separate pools and inputs); each
+    stream's launches claim units from their own counter, so both match the oracle."""
+    ws_ = [synth.decode_workload(synth.FULL_HEADS, 64, 128, seed=47 + k) for k in range(2)]
+    ds = [U.to_device(w) for w in ws_]
+    ogs = [torch.zeros((64, 6144), dtype=torch.bfloat16, device="cuda") for _ in ws_]
+    err = _dev_err()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(3):  # repeated so the two streams' launches overlap; each repeat redoes the step
+        if rep:
+            ds = [U.to_device(w) for w in ws_]
+            torch.cuda.synchronize()
+        for w, d, og, st in zip(ws_, ds, ogs, streams):
+            D = b.make_dims(w["dims"], w["num_slots"])
+            b.gdn_decode_step(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"], d["alpha"],
+                              d["beta"], d["z"], d["gamma"], w["eps"], ogate=og, dev_err=err, stream=st)
+        torch.cuda.synchronize()
+    assert b.gdn_read_device_error(err) == 0
+    for w, d, og in zip(ws_, ds, ogs):
+        _check_decode(w, d, None, og)
+
+
 def test_decode_is_deterministic(b):
     w = synth.decode_workload(synth.FULL_HEADS, 16, seed=46)
     d1, _, og1 = _run_decode(b, w, want_o=False)
