@@ -3,6 +3,7 @@
     python -m gated_deltanet_linear_conv1d_gb300.profile_case decode  --requests 64 --slots 128 --launches 3
     python -m gated_deltanet_linear_conv1d_gb300.profile_case prefill --lengths 2048x8 --launches 2
     python -m gated_deltanet_linear_conv1d_gb300.profile_case spec    --requests 64 --launches 2
+    python -m gated_deltanet_linear_conv1d_gb300.profile_case fp8     --requests 4096 --k 6144 --n 5120
 
 Each launch is preceded by the same warm-up launches (--warmup) and followed
 by a device synchronisation; nothing else runs on the GPU besides the input
@@ -43,12 +44,14 @@ def _lengths(spec: str) -> list[int]:
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["decode", "prefill", "spec", "conv", "rmsnorm"])
+    ap.add_argument("case", choices=["decode", "prefill", "spec", "conv", "rmsnorm", "fp8"])
     ap.add_argument("--heads", choices=["full", "rank"], default="full")
     ap.add_argument("--requests", type=int, default=64)
     ap.add_argument("--slots", type=int, default=0)
     ap.add_argument("--lengths", default="2048x8", help="prefill lengths, e.g. 2048x8 or 16,300,8192")
     ap.add_argument("--loguniform", type=int, default=0, help="prefill: N log-uniform lengths in [16, 8192]")
+    ap.add_argument("--k", type=int, default=6144, help="fp8: input features")
+    ap.add_argument("--n", type=int, default=5120, help="fp8: output features")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     args = ap.parse_args(argv)
@@ -95,6 +98,19 @@ def main(argv=None):
             b.gdn_spec_verify(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"],
                               d["spec_slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og,
                               dev_err=err)
+    elif args.case == "fp8":
+        # out [T, N] = dequant(x8) dequant(w8)^T with block scales: random E4M3 codes and scales
+        rng = np.random.default_rng(6)
+        T, K, N = args.requests, args.k, args.n
+        x8 = torch.from_numpy(synth.fp8_codes(rng, (T, K))).to(dev)
+        w8 = torch.from_numpy(synth.fp8_codes(rng, (N, K))).to(dev)
+        xs = torch.from_numpy(rng.uniform(0.002, 0.02, size=(T, K // 128)).astype(np.float32)).to(dev)
+        ws = torch.from_numpy(rng.uniform(1e-4, 1e-3, size=((N + 127) // 128, K // 128)).astype(np.float32)).to(dev)
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device=dev)
+
+        def run():
+            b.gdn_fp8_linear(x8, xs, w8, ws, out, workspace=wsp, dev_err=err)
     else:
         rng = np.random.default_rng(5)
         T = args.requests
@@ -117,7 +133,7 @@ def main(argv=None):
         if it >= args.warmup:
             times.append(e0.elapsed_time(e1))
     flag = b.gdn_read_device_error(err)
-    tokens = {"decode": args.requests, "spec": args.requests * 4}.get(args.case)
+    tokens = {"decode": args.requests, "spec": args.requests * 4, "fp8": args.requests}.get(args.case)
     if args.case in ("prefill", "conv"):
         tokens = T
     ms = sum(times) / max(1, len(times))
