@@ -75,10 +75,14 @@ size_t gdn_conv_hist_bytes(const gdn_dims* d) {
   return (size_t)channels(d) * (d->conv_kernel - 1) * sizeof(uint16_t);
 }
 
+// Prefill scratch: the schedule (requests, longest first) and one ticket per (request, key head).
+size_t prefill_order_bytes(int32_t num_seqs) { return ((size_t)num_seqs * sizeof(int32_t) + 255) / 256 * 256; }
+
 size_t gdn_prefill_workspace_bytes(const gdn_dims* d, int32_t num_seqs, int32_t num_tokens) {
   (void)num_tokens;
   if (check_dims(d) != GDN_OK || num_seqs <= 0) return 0;
-  return ((size_t)num_seqs * sizeof(int32_t) + 255) / 256 * 256;  // the schedule: requests, longest first
+  return prefill_order_bytes(num_seqs) +
+         ((size_t)num_seqs * d->num_k_heads * sizeof(int32_t) + 255) / 256 * 256;
 }
 
 const char* gdn_status_string(gdn_status s) {
@@ -209,7 +213,9 @@ gdn_status gdn_chunk_prefill(const gdn_dims* d, const uint16_t* qkv0, const floa
     return GDN_ERR_INVALID_ARG;
   PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
                 dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
-                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace), nullptr, nullptr, 0, 0};
+                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace),
+                reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + prefill_order_bytes(num_seqs)),
+                nullptr, nullptr, 0, 0};
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -241,8 +247,9 @@ gdn_status gdn_chunk_prefill_align(const gdn_dims* d, const uint16_t* qkv0, cons
     return GDN_ERR_INVALID_ARG;
   PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
                 dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
-                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace), prefix_len,
-                max_snaps > 0 ? snap_slot : nullptr, block_tokens, max_snaps};
+                d->num_slots, num_seqs, num_tokens, static_cast<int32_t*>(workspace),
+                reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + prefill_order_bytes(num_seqs)),
+                prefix_len, max_snaps > 0 ? snap_slot : nullptr, block_tokens, max_snaps};
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -255,7 +262,9 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
   gdn_status st = check_dims(d);
   if (st != GDN_OK) return st;
   if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
-  if (num_seqs > gdn::kStaticPrefillMaxSeqs) return GDN_ERR_INVALID_ARG;  // beyond the fixed schedule array
+  if (num_seqs > gdn::kStaticPrefillMaxSeqs ||
+      (long long)num_seqs * d->num_k_heads > gdn::kStaticPrefillMaxTickets)
+    return GDN_ERR_INVALID_ARG;  // beyond the fixed schedule arrays
   if (num_seqs == 0) return num_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
   if (!conv_w || !conv_hist || !state || !qsl || !slot_idx) return GDN_ERR_INVALID_ARG;
   if (num_tokens == 0) return GDN_OK;  // every request is empty: nothing is read or written
@@ -268,10 +277,11 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
   if ((o && !aligned(o, 8)) || (ogate && (!aligned(ogate, 16) || !aligned(z, 16) || !aligned(gamma, 16))))
     return GDN_ERR_INVALID_ARG;
   int32_t* order = nullptr;
-  if (gdn::static_prefill_order(&order) != cudaSuccess) return GDN_ERR_CUDA;
+  int32_t* tickets = nullptr;
+  if (gdn::static_prefill_order(&order, &tickets) != cudaSuccess) return GDN_ERR_CUDA;
   PrefillArgs a{qkv0, conv_w, conv_hist, state, qsl, slot_idx, has_init, alpha, beta, z, gamma, eps, o, ogate,
                 dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
-                d->num_slots, num_seqs, num_tokens, order, nullptr, nullptr, 0, 0};
+                d->num_slots, num_seqs, num_tokens, order, tickets, nullptr, nullptr, 0, 0};
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -67,7 +67,8 @@ struct PrefillArgs {
   uint16_t* ogate;            // or nullptr
   int32_t* dev_err;
   int Hk, Hv, G, CH, Rs, N, T;
-  int32_t* order;             // [N] scratch: requests, longest first (filled by launch_prefill), or nullptr
+  int32_t* order;             // [N] scratch: requests, longest first (filled by launch_prefill)
+  int32_t* tickets;           // [N][Hk] scratch: CTAs of (request, key head) finished (zeroed by launch_prefill)
   // align mode (all nullptr / 0 otherwise): pos0[n] tokens already in request n's slot; chunks end on
   // absolute multiples of 64, and after every absolute multiple of snap_block the state and history go
   // to snap_slot[n][j] (j-th such boundary of this call; -1 skips)
@@ -155,9 +156,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // Largest request count the allocation-free prefill accepts: the size of its
 // file-scope schedule array (one int32 per request, 256 KiB).
 constexpr int kStaticPrefillMaxSeqs = 65536;
+constexpr int kStaticPrefillMaxTickets = 1 << 20;  // requests x key heads
 // Device address of that array on the current device, looked up once per
 // device with cudaGetSymbolAddress and cached.
-cudaError_t static_prefill_order(int32_t** out);
+cudaError_t static_prefill_order(int32_t** order, int32_t** tickets);
 
 // out[T][N] = x[T][K] w[N][K]^T (+ residual[T][N]) through cuBLASLt, bf16
 // operands, fp32 accumulation, out (and residual) bf16 or fp32; sets

@@ -15,9 +15,11 @@
 // products' readouts, so the tensor cores take the raw conv outputs.
 //
 // One CTA per (value head h, request n), 512 threads (16 warps, four per
-// tensor-memory lane quarter, splitting the columns of every readout); the G
-// CTAs of a key head form a cluster (only to order the in-place conv-history
-// update). The fp32 state lives in tensor memory (128 lanes x 128 columns) for
+// tensor-memory lane quarter, splitting the columns of every readout). The G
+// CTAs of a key head all read the key head's old q/k conv history; the last of
+// them to finish (an atomic ticket per (request, key head)) writes the new one,
+// so the in-place update needs no co-scheduling (a cluster of 3 would leave 14
+// of the 152 SMs idle at this kernel's footprint). The fp32 state lives in tensor memory (128 lanes x 128 columns) for
 // the whole request. The raw QKV0 rows and the z rows of the next chunk are
 // fetched by TMA while the current chunk runs. Per chunk:
 //   conv + SiLU (CUDA cores, thread = channel x token range) -> raw q, k (bf16,
@@ -34,7 +36,6 @@
 // The two products that feed the carried state (E and the state update) take
 // tf32 operands; the others take bf16 (measured against the fp64 oracle:
 // state error ~6e-4, output error ~3e-3 relative L2).
-#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,7 +46,6 @@
 #include "launch.h"
 #include "umma.cuh"
 
-namespace cg = cooperative_groups;
 
 namespace gdn {
 
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const int quarter = warp & 3, part = warp >> 2;
   const int row = 32 * quarter + lane;  // tensor-memory lane read by this thread
 
-  // ---- request checks (uniform over the cluster: same request)
+  // ---- request checks (uniform over the request's CTAs)
   const int slot = p.slot_idx[n];
   if (slot < 0) return;
   const int t0 = p.qsl[n], t1 = p.qsl[n + 1];
@@ -294,8 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   for (int it = tid; it < kC * kC / 4; it += kThreads)
     reinterpret_cast<float4*>(TBb)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
   umma::fence_before_sync();
-  // All CTAs of the key-head group have read the old history from here on.
-  cg::this_cluster().sync();
+  __syncthreads();
   umma::fence_after_sync();
   const uint32_t tm = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
@@ -938,7 +937,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gvc) * 3;
       hp[0] = hv[0]; hp[1] = hv[1]; hp[2] = hv[2];
     }
-    if (own_qk && g == 0) {  // q and k history: the group's first CTA
+    // q and k history (the same in every CTA of the group): by the group's last
+    // CTA to get here, when all of them have read the old one
+    volatile int* last_of_group = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    if (tid == 0) {
+      __threadfence();
+      *last_of_group = atomicAdd(p.tickets + (size_t)n * p.Hk + j, 1) == p.G - 1;
+    }
+    __syncthreads();
+    if (*last_of_group && own_qk) {
       uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gqk) * 3;
       hp[0] = hqk[0]; hp[1] = hqk[1]; hp[2] = hqk[2];
     }
@@ -971,7 +978,8 @@ bool encode_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* d
 // first and the short ones fill in behind them. One CTA: a counting sort.
 constexpr int kOrderThreads = 1024, kOrderBuckets = 2 * kOrderThreads;
 
-__global__ void __launch_bounds__(kOrderThreads) prefill_order_kernel(const int32_t* qsl, int N, int32_t* order) {
+__global__ void __launch_bounds__(kOrderThreads) prefill_order_kernel(const int32_t* qsl, int N, int32_t* order,
+                                                                      int32_t* tickets, int n_tickets) {
   __shared__ int cnt[kOrderBuckets];
   __shared__ int wsum[kOrderThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -980,6 +988,7 @@ __global__ void __launch_bounds__(kOrderThreads) prefill_order_kernel(const int3
     return len <= 0 ? 0 : min((len + kC - 1) / kC, kOrderBuckets - 1);
   };
   for (int b = tid; b < kOrderBuckets; b += kOrderThreads) cnt[b] = 0;
+  for (int i = tid; i < n_tickets; i += kOrderThreads) tickets[i] = 0;  // the prefill's group tickets
   __syncthreads();
   for (int n = tid; n < N; n += kOrderThreads) atomicAdd(&cnt[key(n)], 1);
   __syncthreads();
@@ -1032,26 +1041,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // the library a workspace because they cannot allocate device memory at the
 // call site (a host whose device memory is all reserved up front by its own
 // pool, with no allocation hook). Fixed size, one per device; it needs no
-// clearing (the order kernel writes all N entries before the prefill reads
-// them), and two such calls in flight at once on one device race on it.
+// clearing (the order kernel writes all N entries and zeroes the N x Hk
+// tickets before the prefill reads them), and two such calls in flight at once
+// on one device race on it.
 static __device__ __align__(256) int32_t g_static_prefill_order[kStaticPrefillMaxSeqs];
+static __device__ __align__(256) int32_t g_static_prefill_tickets[kStaticPrefillMaxTickets];
 
-cudaError_t static_prefill_order(int32_t** out) {
+cudaError_t static_prefill_order(int32_t** order, int32_t** tickets) {
   constexpr int kMaxDevices = 64;
   static std::mutex mu;
-  static int32_t* cache[kMaxDevices] = {};
+  static int32_t* cache[kMaxDevices][2] = {};
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* ptr = nullptr;
-    err = cudaGetSymbolAddress(&ptr, g_static_prefill_order);
-    if (err != cudaSuccess) return err;
-    cache[dev] = static_cast<int32_t*>(ptr);
+  if (!cache[dev][0]) {
+    void* po = nullptr;
+    void* pt = nullptr;
+    if ((err = cudaGetSymbolAddress(&po, g_static_prefill_order)) != cudaSuccess) return err;
+    if ((err = cudaGetSymbolAddress(&pt, g_static_prefill_tickets)) != cudaSuccess) return err;
+    cache[dev][0] = static_cast<int32_t*>(po);
+    cache[dev][1] = static_cast<int32_t*>(pt);
   }
-  *out = cache[dev];
+  *order = cache[dev][0];
+  *tickets = cache[dev][1];
   return cudaSuccess;
 }
 
@@ -1073,23 +1087,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   }
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(&prefill_tc_kernel), kSmemBytes);
   if (err != cudaSuccess) return err;
-  if (a.order) {
-    prefill_order_kernel<<<1, kOrderThreads, 0, stream>>>(a.qsl, a.N, a.order);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hv, a.N, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.G;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, a, tmx, tmz, tmo);
+  if (!a.order || !a.tickets) return cudaErrorInvalidValue;
+  prefill_order_kernel<<<1, kOrderThreads, 0, stream>>>(a.qsl, a.N, a.order, a.tickets, a.N * a.Hk);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  prefill_tc_kernel<<<dim3(a.Hv, a.N, 1), kThreads, kSmemBytes, stream>>>(a, tmx, tmz, tmo);
+  return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -166,8 +166,10 @@ gdn_status gdn_decode_step(const gdn_dims *dims, const uint16_t *qkv0, const flo
  *             gdn_prefill_workspace_bytes(dims, N, T) bytes, 256-byte aligned.
  *             Contents need not be zeroed and are clobbered: the call writes
  *             there the order in which the (request, head) chains are started,
- *             longest request first. Two calls in flight at once need two
- *             workspaces.
+ *             longest request first, and one ticket per (request, key head)
+ *             counting its value-head chains that have finished (the last one
+ *             writes the key head's new q/k conv history). Two calls in flight
+ *             at once need two workspaces.
  */
 gdn_status gdn_chunk_prefill(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
                              uint16_t *conv_hist, float *state, const int32_t *query_start_loc,
@@ -221,13 +223,14 @@ gdn_status gdn_chunk_prefill_align(const gdn_dims *dims, const uint16_t *qkv0, c
  * convenience of this library, and computes exactly what gdn_chunk_prefill
  * computes.
  *
- * Its schedule scratch is a fixed file-scope device array of 65536 int32
- * (256 KiB) per device: num_seqs above that is rejected with
- * GDN_ERR_INVALID_ARG. The library allocates nothing; the first call on each
- * device looks up the array's address (cudaGetSymbolAddress) and caches it, so
+ * Its scratch is two fixed file-scope device arrays per device: the schedule,
+ * 65536 int32 (256 KiB), and the (request, key head) tickets, 2^20 int32
+ * (4 MiB): num_seqs above 65536, or num_seqs x num_k_heads above 2^20, is
+ * rejected with GDN_ERR_INVALID_ARG. The library allocates nothing; the first call on each
+ * device looks up the arrays' addresses (cudaGetSymbolAddress) and caches them, so
  * make that first call before any stream capture. The scratch needs no
  * clearing. Calls that overlap in time on one device (two streams, or two
- * threads) race on the one array: serialise them.
+ * threads) race on the arrays: serialise them.
  *
  * Arguments, layouts, errors: as gdn_chunk_prefill, without workspace and
  * workspace_bytes.
@@ -407,7 +410,8 @@ size_t gdn_state_bytes(const gdn_dims *dims);
 size_t gdn_conv_hist_bytes(const gdn_dims *dims);
 
 /* Device scratch gdn_chunk_prefill needs for N requests and T packed tokens:
- * N int32 rounded up to 256 bytes (0 for invalid dims or N <= 0). */
+ * N int32 rounded up to 256 bytes, then N x num_k_heads int32 rounded up to 256
+ * bytes (0 for invalid dims or N <= 0). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t num_seqs, int32_t num_tokens);
 
 /* Static, human-readable name of a status code. */

@@ -37,11 +37,12 @@ def test_size_queries_match_the_page(b):
     assert b.gdn_state_bytes(b.GdnDims(0, 0, 0, 0, 0, 0)) == 0
 
 
-def test_prefill_workspace_holds_one_int_per_request(b):
+def test_prefill_workspace_holds_the_schedule_and_the_tickets(b):
     d = b.make_dims(synth.FULL_HEADS, 512)
-    assert b.gdn_prefill_workspace_bytes(d, 64, 71068) == 256
-    assert b.gdn_prefill_workspace_bytes(d, 65, 100) == 512
-    assert b.gdn_prefill_workspace_bytes(d, 1000, 1000) == 4096
+    # schedule (N int32, 256-byte rounded) + tickets (N x 16 key heads int32, 256-byte rounded)
+    assert b.gdn_prefill_workspace_bytes(d, 64, 71068) == 256 + 4096
+    assert b.gdn_prefill_workspace_bytes(d, 65, 100) == 512 + 4352
+    assert b.gdn_prefill_workspace_bytes(d, 1000, 1000) == 4096 + 64000
     assert b.gdn_prefill_workspace_bytes(d, 0, 0) == 0
     assert b.gdn_prefill_workspace_bytes(b.GdnDims(0, 0, 0, 0, 0, 0), 64, 64) == 0
 
