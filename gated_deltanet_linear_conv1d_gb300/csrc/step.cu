@@ -278,14 +278,33 @@ __global__ void __launch_bounds__(256) commit_kernel(const CommitArgs p) {
     return;
   }
   if (x < p.Hv) {
+    // 64 KiB: 16 float4 per thread, loaded four at a time before they are stored
     const float4* s = reinterpret_cast<const float4*>(p.state + ((size_t)src * p.Hv + x) * kTile);
     float4* d = reinterpret_cast<float4*>(p.state + ((size_t)slot * p.Hv + x) * kTile);
-    for (int i = threadIdx.x; i < kTile / 4; i += blockDim.x) d[i] = s[i];
+    for (int i0 = threadIdx.x; i0 < kTile / 4; i0 += 4 * blockDim.x) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < kTile / 4) v[u] = s[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < kTile / 4) d[i] = v[u];
+      }
+    }
   } else {
     const size_t nb = (size_t)p.CH * (kTaps - 1);  // uint16 per slot
     const uint16_t* s = p.conv_hist + (size_t)src * nb;
     uint16_t* d = p.conv_hist + (size_t)slot * nb;
-    for (size_t i = threadIdx.x; i < nb; i += blockDim.x) d[i] = s[i];
+    if (((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) & 15) == 0 && nb % 8 == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(s);
+      uint4* d4 = reinterpret_cast<uint4*>(d);
+      for (size_t i = threadIdx.x; i < nb / 8; i += blockDim.x) d4[i] = s4[i];
+    } else {
+      for (size_t i = threadIdx.x; i < nb; i += blockDim.x) d[i] = s[i];
+    }
   }
 }
 
