@@ -17,7 +17,7 @@
 // One CTA per (value head h, request n), 512 threads (16 warps, four per
 // tensor-memory lane quarter, splitting the columns of every readout). The G
 // CTAs of a key head all read the key head's old q/k conv history; the last of
-// them to finish (an atomic ticket per (request, key head)) writes the new one,
+// them to start (an atomic ticket per (request, key head)) writes the new one,
 // so the in-place update needs no co-scheduling (a cluster of 3 would leave 14
 // of the 152 SMs idle at this kernel's footprint). The fp32 state lives in tensor memory (128 lanes x 128 columns) for
 // the whole request. The raw QKV0 rows and the z rows of the next chunk are
@@ -298,6 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   umma::fence_after_sync();
   const uint32_t tm = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+  // This CTA has read the key head's old q/k history (before the barrier above):
+  // take its ticket. The group's last CTA to get here writes the new history
+  // at its end, when every CTA of the group has read the old one.
+  volatile int* last_of_group = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  if (tid == 0) {
+    __threadfence();
+    *last_of_group = atomicAdd(p.tickets + (size_t)n * p.Hk + j, 1) == p.G - 1;
+  }
 
   // ---- initial state into tensor memory: thread (row, part) owns 32 columns
   {
@@ -938,13 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       hp[0] = hv[0]; hp[1] = hv[1]; hp[2] = hv[2];
     }
     // q and k history (the same in every CTA of the group): by the group's last
-    // CTA to get here, when all of them have read the old one
-    volatile int* last_of_group = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    if (tid == 0) {
-      __threadfence();
-      *last_of_group = atomicAdd(p.tickets + (size_t)n * p.Hk + j, 1) == p.G - 1;
-    }
-    __syncthreads();
+    // CTA to start (its ticket, taken after the old history was read)
     if (*last_of_group && own_qk) {
       uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gqk) * 3;
       hp[0] = hqk[0]; hp[1] = hqk[1]; hp[2] = hqk[2];

@@ -167,8 +167,9 @@ gdn_status gdn_decode_step(const gdn_dims *dims, const uint16_t *qkv0, const flo
  *             Contents need not be zeroed and are clobbered: the call writes
  *             there the order in which the (request, head) chains are started,
  *             longest request first, and one ticket per (request, key head)
- *             counting its value-head chains that have finished (the last one
- *             writes the key head's new q/k conv history). Two calls in flight
+ *             counting its value-head chains that have started (the last to
+ *             start writes the key head's new q/k conv history at its end).
+ *             Two calls in flight
  *             at once need two workspaces.
  */
 gdn_status gdn_chunk_prefill(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
