@@ -274,6 +274,21 @@ def test_prefill_ragged_batch(b, geom):
     _check_prefill(w, d, o, og, np.arange(len(lengths)))
 
 
+def test_prefill_many_short_requests(b):
+    """400 requests of 1-5 tokens at 4/12 heads (4,800 CTAs, 1,600 key-head groups): every key head's
+    new q/k history is written by the last of its group's CTAs to start, whatever order they run in;
+    the whole history pool is checked bit for bit, state and outputs on a sample of requests."""
+    rng = np.random.default_rng(52)
+    lengths = rng.integers(1, 6, size=400).tolist()
+    w = synth.prefill_workload(synth.RANK_HEADS, lengths, seed=52)
+    d, _, og = _run_prefill(b, w, want_o=False)
+    sample = np.sort(rng.choice(len(lengths), 24, replace=False))
+    _check_prefill(w, d, None, og, sample)
+    r, _ = U.oracle_compact(w, np.arange(len(lengths)))
+    slots = torch.from_numpy(w["slot_idx"].astype(np.int64)).cuda()
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][slots]), r["conv_hist"])
+
+
 def test_prefill_varlen_64_requests_sampled(b):
     """64 requests, log-uniform lengths in [16, 8192], half from zero; sampled requests checked."""
     lengths = synth.loguniform_lengths(np.random.default_rng(3), 64, 16, 8192)
