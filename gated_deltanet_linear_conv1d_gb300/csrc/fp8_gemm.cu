@@ -335,12 +335,216 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
   if (warp == 1) umma::tmem_dealloc(tm, kTmemCols);
 }
 
-bool encode_u8(CUtensorMap* m, const void* base, int rows, int cols) {
+// ---- many tiles: 128 x 256 output tiles, the fp32 sum kept in tensor memory --
+//
+// With at least two waves of tiles the kernel below takes 256 outputs per tile
+// (two weight-scale blocks), which halves the barrier hand-overs per flop. The
+// running fp32 sum of the tile lives in tensor memory (columns 0-255) rather
+// than in registers, next to two 128-column buffers for the two halves' block
+// products (256-383 and 384-511): the MMAs of one half run while the other
+// half's product is folded (read the product and the sum, multiply-add, store
+// the sum), so the tensor core and the folding warps overlap within a K block.
+constexpr int kWN = 256;
+constexpr int kWStageBytes = kTileBytes + kWN * kBK;   // 16 KB of X rows + 32 KB of W rows
+constexpr int kWBarOff = kStages * kWStageBytes;
+constexpr int kWSmemBytes = kWBarOff + 256 + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8GemmArgs p,
+                                                                     const __grid_constant__ CUtensorMap tmx,
+                                                                     const __grid_constant__ CUtensorMap tmw) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWBarOff);  // [kStages] TMA -> MMA
+  uint64_t* empty = full + kStages;                                 // [kStages] MMA -> TMA
+  uint64_t* pfull = empty + kStages;                                // [2] half's product ready
+  uint64_t* pempty = pfull + 2;                                     // [2] half's product folded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);               // [0] abort
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&pfull[h], 1);
+      mbar_init(&pempty[h], 4);  // the four promotion warps of that half
+    }
+    flags[0] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) umma::tmem_alloc(tmem_slot, 512);
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tm = *tmem_slot;
+  volatile int* abort_flag = flags;
+  const int nt = (p.N + kWN - 1) / kWN;
+  const long long tiles = (long long)p.mt * nt;
+  constexpr uint32_t kIdHalf = umma::idesc(umma::kE4M3, false, false, kBM, 128);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t gk = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m_t = (int)(t / nt), n_t = (int)(t % nt);
+        for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+          const int s = gk % kStages;
+          if ((gk >= (uint32_t)kStages && !mbar_wait_bounded(&empty[s], ((gk / kStages) - 1) & 1)) ||
+              *abort_flag) {
+            ok = false;
+            break;
+          }
+          unsigned char* st = smem + s * kWStageBytes;
+          mbar_arrive_expect_tx(&full[s], kWStageBytes);
+          tma_load_2d(st, &tmx, kb * kBK, m_t * kBM, &full[s]);
+          tma_load_2d(st + kTileBytes, &tmw, kb * kBK, n_t * kWN, &full[s]);
+        }
+      }
+      if (!ok) {
+        report(p.dev_err, GDN_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        for (uint32_t j = (gk > (uint32_t)kStages ? gk - kStages : 0); j < gk; ++j)
+          mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t gk = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+          const int s = gk % kStages;
+          if (!mbar_wait_bounded(&full[s], (gk / kStages) & 1) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          umma::fence_after_sync();
+          const uint32_t sx = smem_u32(smem + s * kWStageBytes), sw = sx + kTileBytes;
+          for (int h = 0; h < 2 && ok; ++h) {
+            if (gk >= 1 && !mbar_wait_bounded(&pempty[h], (gk - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            umma::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kBK / 32; ++kk)
+              umma::mma<umma::kKindF8>(tm + 256 + 128 * h, umma::smem_desc_sw128(sx + kk * 32),
+                                       umma::smem_desc_sw128(sw + h * 128 * kBK + kk * 32), kIdHalf, kk > 0);
+            umma::commit(&pfull[h]);
+          }
+          if (!ok) break;
+          umma::commit(&empty[s]);
+        }
+      }
+      if (!ok) {
+        report(p.dev_err, GDN_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (gk > 0) {
+        mbar_wait_bounded(&pfull[0], (gk - 1) & 1);
+        mbar_wait_bounded(&pfull[1], (gk - 1) & 1);
+      }
+    }
+  } else {
+    // promotion: warp w folds half h = (w - 2) / 4 for tensor-memory lanes 32 (w % 4) .. +31
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const uint32_t t_acc = tm + lane_off + 128 * h, t_prod = tm + lane_off + 256 + 128 * h;
+    const int NB = (p.N + 127) / 128;
+    uint32_t gk = 0;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int m_t = (int)(t / nt), n_t = (int)(t % nt);
+      const int row = m_t * kBM + 32 * q + lane;
+      const bool live = row < p.T;
+      const int nb = min(2 * n_t + h, NB - 1);  // weight-scale block of this half
+      const float* xs_row = p.xs + (size_t)(live ? row : 0) * p.KB;
+      const float* ws_row = p.ws + (size_t)nb * p.KB;
+      float sx[kScaleAhead], sw[kScaleAhead];
+#pragma unroll
+      for (int i = 0; i < kScaleAhead; ++i) {
+        const int kb = min(i, p.KB - 1);
+        sx[i] = live ? __ldg(xs_row + kb) : 0.f;
+        sw[i] = __ldg(ws_row + kb);
+      }
+      for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+        const float scale = sx[0] * sw[0];
+#pragma unroll
+        for (int i = 0; i + 1 < kScaleAhead; ++i) {
+          sx[i] = sx[i + 1];
+          sw[i] = sw[i + 1];
+        }
+        {
+          const int kn = min(kb + kScaleAhead, p.KB - 1);
+          sx[kScaleAhead - 1] = live ? __ldg(xs_row + kn) : 0.f;
+          sw[kScaleAhead - 1] = __ldg(ws_row + kn);
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) continue;
+        const bool got = mbar_wait_bounded(&pfull[h], gk & 1);
+        if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
+          if (lane == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          continue;
+        }
+        umma::fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          float a[32];
+          umma::ld32_nowait(t_prod + 32 * c, v);
+          if (kb > 0) {
+            uint32_t r[32];
+            umma::ld32_nowait(t_acc + 32 * c, r);
+            umma::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = fmaf(scale, __uint_as_float(v[i]), __uint_as_float(r[i]));
+          } else {
+            umma::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = scale * __uint_as_float(v[i]);
+          }
+          umma::st32(t_acc + 32 * c, a);
+        }
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_one(&pempty[h]);
+      }
+      // ---- store the tile's half: bf16 rows (+ residual). The tensor-memory
+      // reads are warp-wide (.sync.aligned): every lane reads, rows past T
+      // skip only the store.
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) continue;
+      uint16_t* out_row = p.out + (size_t)(live ? row : 0) * p.N;
+      const uint16_t* res_row = p.residual ? p.residual + (size_t)(live ? row : 0) * p.N : nullptr;
+      const int n0 = n_t * kWN + 128 * h;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float a[32];
+        umma::ld32(t_acc + 32 * c, a);
+        if (!live) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = a[8 * j + e];
+          store_row8(out_row, res_row, n0 + 32 * c + 8 * j, p.N, v);
+        }
+      }
+    }
+  }
+
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  if (warp == 1) umma::tmem_dealloc(tm, 512);
+}
+
+bool encode_u8(CUtensorMap* m, const void* base, int rows, int cols, int box_rows = 128) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols};
-  const cuuint32_t box[2] = {kBK, 128};
+  const cuuint32_t box[2] = {kBK, (cuuint32_t)box_rows};
   const cuuint32_t elem[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -382,6 +586,26 @@ size_t fp8_gemm_workspace_bytes(int T, int N, int K) {
 cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_bytes, int32_t* dev_err,
                             cudaStream_t stream) {
   if (o.T == 0) return cudaSuccess;
+  const int sms_w = num_sms();
+  const long long wide_tiles = (long long)((o.T + kBM - 1) / kBM) * ((o.N + kWN - 1) / kWN);
+  if (wide_tiles >= 2LL * sms_w) {  // many tiles: 128 x 256 tiles, the sum in tensor memory
+    CUtensorMap tmx{}, tmw{};
+    if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K, kWN)) return cudaErrorInvalidValue;
+    Fp8GemmArgs a{};
+    a.xs = o.xs;
+    a.ws = o.ws;
+    a.residual = o.residual;
+    a.out = o.out;
+    a.dev_err = dev_err;
+    a.T = o.T;
+    a.N = o.N;
+    a.KB = o.K / kBK;
+    a.mt = (o.T + kBM - 1) / kBM;
+    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes);
+    if (err != cudaSuccess) return err;
+    fp8_gemm_wide_kernel<<<sms_w, kThreads, kWSmemBytes, stream>>>(a, tmx, tmw);
+    return cudaGetLastError();
+  }
   CUtensorMap tmx{}, tmw{};
   if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K)) return cudaErrorInvalidValue;
   Fp8GemmArgs a{};

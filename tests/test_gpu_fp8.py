@@ -140,3 +140,23 @@ def test_fp8_linear_decode_batches(b, T, K, N, res):
                          residual=U.dev_bf16(r) if res else None, workspace=wsp, dev_err=err)
     assert b.gdn_read_device_error(err) == 0
     U.check_out(U.host_f64_from_bf16(out), oracle.fp8_linear(x8, xs, w8, ws, r if res else None), "out")
+
+
+@pytest.mark.parametrize("T,K,N,res", [
+    (4836, 256, 2048, True),    # 38 x 8 = 304 tiles of 128 x 256: the wide tiles, ragged last row tile
+    (4836, 384, 2176, False),   # the last column tile's second half lies past N
+    (9800, 128, 4096, True),    # one K block, eight tiles per CTA
+])
+def test_fp8_linear_wide_tiles(b, T, K, N, res):
+    """Token counts with at least two waves of 128 x 256 tiles take the wide-tile kernel (the running
+    sum in tensor memory, the two 128-column halves folded in turn): ragged rows and columns, a half
+    tile past the last column, several tiles per CTA; called twice on the same buffers."""
+    x8, xs, w8, ws, r = _operands(T, K, N, 490 + T + N)
+    out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        b.gdn_fp8_linear(_dev_u8(x8), U.dev(xs), _dev_u8(w8), U.dev(ws), out,
+                         residual=U.dev_bf16(r) if res else None, workspace=wsp, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    U.check_out(U.host_f64_from_bf16(out), oracle.fp8_linear(x8, xs, w8, ws, r if res else None), "out")
