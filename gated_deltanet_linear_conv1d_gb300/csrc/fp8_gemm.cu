@@ -335,19 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
   if (warp == 1) umma::tmem_dealloc(tm, kTmemCols);
 }
 
-// ---- many tiles: 128 x 256 output tiles, the fp32 sum kept in tensor memory --
+// ---- many tiles: 128 x 256 output tiles, one N = 256 MMA per K step --------
 //
 // With at least two waves of tiles the kernel below takes 256 outputs per tile
-// (two weight-scale blocks), which halves the barrier hand-overs per flop. The
-// running fp32 sum of the tile lives in tensor memory (columns 0-255) rather
-// than in registers, next to two 128-column buffers for the two halves' block
-// products (256-383 and 384-511): the MMAs of one half run while the other
-// half's product is folded (read the product and the sum, multiply-add, store
-// the sum), so the tensor core and the folding warps overlap within a K block.
+// (two weight-scale blocks): each K step is one N = 256 MMA (its cost is about
+// 1.6 times an N = 128 one for twice the work) and each K block's product lands
+// in one of two 256-column tensor-memory buffers, so the folding of block kb
+// overlaps the MMAs of block kb + 1. The fp32 running sum of the tile stays in
+// registers: promotion warp w holds the 128 columns of half (w - 2) / 4 for the
+// 32 rows of its tensor-memory lane quarter.
 constexpr int kWN = 256;
 constexpr int kWStageBytes = kTileBytes + kWN * kBK;   // 16 KB of X rows + 32 KB of W rows
 constexpr int kWBarOff = kStages * kWStageBytes;
 constexpr int kWSmemBytes = kWBarOff + 256 + 1024;
+constexpr int kWScaleAhead = 2;  // fewer registers than the narrow kernel: the sum takes 128
+constexpr uint32_t kWIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kWN);
 
 __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8GemmArgs p,
                                                                      const __grid_constant__ CUtensorMap tmx,
@@ -356,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWBarOff);  // [kStages] TMA -> MMA
   uint64_t* empty = full + kStages;                                 // [kStages] MMA -> TMA
-  uint64_t* pfull = empty + kStages;                                // [2] half's product ready
-  uint64_t* pempty = pfull + 2;                                     // [2] half's product folded
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
+  uint64_t* tfull = empty + kStages;                                // [2] K block's product ready
+  uint64_t* tempty = tfull + 2;                                     // [2] K block's product folded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);               // [0] abort
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -366,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&pfull[h], 1);
-      mbar_init(&pempty[h], 4);  // the four promotion warps of that half
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kPromoWarps);
     }
     flags[0] = 0;
     fence_mbar_init();
@@ -380,15 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
   const uint32_t tm = *tmem_slot;
   volatile int* abort_flag = flags;
   const int nt = (p.N + kWN - 1) / kWN;
-  const long long tiles = (long long)p.mt * nt;
-  constexpr uint32_t kIdHalf = umma::idesc(umma::kE4M3, false, false, kBM, 128);
+  const int tiles = p.mt * nt;  // the launcher keeps this below 2^31
 
   if (warp == 0) {
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
       uint32_t gk = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int m_t = (int)(t / nt), n_t = (int)(t % nt);
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m_t = t / nt, n_t = t % nt;
         for (int kb = 0; kb < p.KB; ++kb, ++gk) {
           const int s = gk % kStages;
           if ((gk >= (uint32_t)kStages && !mbar_wait_bounded(&empty[s], ((gk / kStages) - 1) & 1)) ||
@@ -413,122 +416,96 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
     if (lane == 0) {
       uint32_t gk = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < p.KB; ++kb, ++gk) {
           const int s = gk % kStages;
-          if (!mbar_wait_bounded(&full[s], (gk / kStages) & 1) || *abort_flag) {
+          const uint32_t b = gk & 1, use = gk >> 1;
+          if (!mbar_wait_bounded(&full[s], (gk / kStages) & 1) ||
+              (gk >= 2 && !mbar_wait_bounded(&tempty[b], (use - 1) & 1)) || *abort_flag) {
             ok = false;
             break;
           }
           umma::fence_after_sync();
           const uint32_t sx = smem_u32(smem + s * kWStageBytes), sw = sx + kTileBytes;
-          for (int h = 0; h < 2 && ok; ++h) {
-            if (gk >= 1 && !mbar_wait_bounded(&pempty[h], (gk - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            umma::fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < kBK / 32; ++kk)
-              umma::mma<umma::kKindF8>(tm + 256 + 128 * h, umma::smem_desc_sw128(sx + kk * 32),
-                                       umma::smem_desc_sw128(sw + h * 128 * kBK + kk * 32), kIdHalf, kk > 0);
-            umma::commit(&pfull[h]);
-          }
-          if (!ok) break;
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            umma::mma<umma::kKindF8>(tm + b * kWN, umma::smem_desc_sw128(sx + kk * 32),
+                                     umma::smem_desc_sw128(sw + kk * 32), kWIdesc, kk > 0);
           umma::commit(&empty[s]);
+          umma::commit(&tfull[b]);
         }
       }
       if (!ok) {
         report(p.dev_err, GDN_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
-      if (gk > 0) {
-        mbar_wait_bounded(&pfull[0], (gk - 1) & 1);
-        mbar_wait_bounded(&pfull[1], (gk - 1) & 1);
-      }
+      if (gk > 0) mbar_wait_bounded(&tfull[(gk - 1) & 1], ((gk - 1) >> 1) & 1);
     }
   } else {
-    // promotion: warp w folds half h = (w - 2) / 4 for tensor-memory lanes 32 (w % 4) .. +31
     const int q = warp & 3, h = (warp - 2) >> 2;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    const uint32_t t_acc = tm + lane_off + 128 * h, t_prod = tm + lane_off + 256 + 128 * h;
     const int NB = (p.N + 127) / 128;
     uint32_t gk = 0;
-    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-      const int m_t = (int)(t / nt), n_t = (int)(t % nt);
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int m_t = t / nt, n_t = t % nt;
       const int row = m_t * kBM + 32 * q + lane;
       const bool live = row < p.T;
       const int nb = min(2 * n_t + h, NB - 1);  // weight-scale block of this half
       const float* xs_row = p.xs + (size_t)(live ? row : 0) * p.KB;
       const float* ws_row = p.ws + (size_t)nb * p.KB;
-      float sx[kScaleAhead], sw[kScaleAhead];
+      float sx[kWScaleAhead], sw[kWScaleAhead];
 #pragma unroll
-      for (int i = 0; i < kScaleAhead; ++i) {
+      for (int i = 0; i < kWScaleAhead; ++i) {
         const int kb = min(i, p.KB - 1);
         sx[i] = live ? __ldg(xs_row + kb) : 0.f;
         sw[i] = __ldg(ws_row + kb);
       }
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
       for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+        const uint32_t b = gk & 1, use = gk >> 1;
         const float scale = sx[0] * sw[0];
 #pragma unroll
-        for (int i = 0; i + 1 < kScaleAhead; ++i) {
+        for (int i = 0; i + 1 < kWScaleAhead; ++i) {
           sx[i] = sx[i + 1];
           sw[i] = sw[i + 1];
         }
         {
-          const int kn = min(kb + kScaleAhead, p.KB - 1);
-          sx[kScaleAhead - 1] = live ? __ldg(xs_row + kn) : 0.f;
-          sw[kScaleAhead - 1] = __ldg(ws_row + kn);
+          const int kn = min(kb + kWScaleAhead, p.KB - 1);
+          sx[kWScaleAhead - 1] = live ? __ldg(xs_row + kn) : 0.f;
+          sw[kWScaleAhead - 1] = __ldg(ws_row + kn);
         }
         if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) continue;
-        const bool got = mbar_wait_bounded(&pfull[h], gk & 1);
+        const bool got = mbar_wait_bounded(&tfull[b], use & 1);
         if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
           if (lane == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
           *abort_flag = 1;
           continue;
         }
         umma::fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          float a[32];
-          umma::ld32_nowait(t_prod + 32 * c, v);
-          if (kb > 0) {
-            uint32_t r[32];
-            umma::ld32_nowait(t_acc + 32 * c, r);
-            umma::wait_ld();
+        const uint32_t tp = tm + lane_off + b * kWN + 128 * h;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = fmaf(scale, __uint_as_float(v[i]), __uint_as_float(r[i]));
-          } else {
-            umma::wait_ld();
+        for (int c = 0; c < 8; ++c) {
+          float v[16];
+          umma::ld16(tp + 16 * c, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = scale * __uint_as_float(v[i]);
-          }
-          umma::st32(t_acc + 32 * c, a);
+          for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(scale, v[i], acc[16 * c + i]);
         }
         umma::fence_before_sync();
         __syncwarp();
-        if (lane == 0) arrive_one(&pempty[h]);
+        if (lane == 0) arrive_one(&tempty[b]);
       }
-      // ---- store the tile's half: bf16 rows (+ residual). The tensor-memory
-      // reads are warp-wide (.sync.aligned): every lane reads, rows past T
-      // skip only the store.
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) continue;
-      uint16_t* out_row = p.out + (size_t)(live ? row : 0) * p.N;
-      const uint16_t* res_row = p.residual ? p.residual + (size_t)(live ? row : 0) * p.N : nullptr;
+      if (*abort_flag != 0 || !live) continue;
+      uint16_t* out_row = p.out + (size_t)row * p.N;
+      const uint16_t* res_row = p.residual ? p.residual + (size_t)row * p.N : nullptr;
       const int n0 = n_t * kWN + 128 * h;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float a[32];
-        umma::ld32(t_acc + 32 * c, a);
-        if (!live) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v[8];
+      for (int j = 0; j < 16; ++j) {
+        float v[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = a[8 * j + e];
-          store_row8(out_row, res_row, n0 + 32 * c + 8 * j, p.N, v);
-        }
+        for (int e = 0; e < 8; ++e) v[e] = acc[8 * j + e];
+        store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
       }
     }
   }
@@ -588,7 +565,7 @@ cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_byt
   if (o.T == 0) return cudaSuccess;
   const int sms_w = num_sms();
   const long long wide_tiles = (long long)((o.T + kBM - 1) / kBM) * ((o.N + kWN - 1) / kWN);
-  if (wide_tiles >= 2LL * sms_w) {  // many tiles: 128 x 256 tiles, the sum in tensor memory
+  if (wide_tiles >= 2LL * sms_w && wide_tiles < (1LL << 31)) {  // many tiles: 128 x 256 tiles
     CUtensorMap tmx{}, tmw{};
     if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K, kWN)) return cudaErrorInvalidValue;
     Fp8GemmArgs a{};
