@@ -10,7 +10,7 @@
 // divisions are IEEE-rounded, so the codes are a pure function of the inputs.
 //
 //  * quant_act_kernel: activations [T][K] bf16, one scale per token and
-//    128-element group of K; one warp per (token, group), 4 elements per lane.
+//    128-element group of K; half a warp per (token, group), 8 elements per lane.
 //  * quant_weight_kernel: weights [N][K] bf16, one scale per 128 x 128 block;
 //    one 256-thread block per weight block, 64 elements per thread.
 #include "device.cuh"
@@ -36,22 +36,53 @@ __device__ __forceinline__ uint32_t quant4(const float (&v)[4], float s) {
   return a | (b << 16);
 }
 
+// Half a warp per (token, group): lane l of the half holds elements 8l .. 8l+7
+// (one 16-byte load); each thread takes kActRounds items, loads first.
+constexpr int kActRounds = 2;
+constexpr int kActItemsPerBlock = 8 * 2 * kActRounds;
+
 __global__ void __launch_bounds__(256) quant_act_kernel(const QuantActArgs p) {
   const int groups = p.K / 128;
-  const long long item = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, group)
-  if (item >= (long long)p.T * groups) return;
-  const int t = (int)(item / groups), g = (int)(item % groups);
-  const int lane = threadIdx.x & 31;
-  const size_t off = (size_t)t * p.K + (size_t)g * 128 + lane * 4;
-  const uint2 raw = *reinterpret_cast<const uint2*>(p.x + off);
-  const float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff),
-                      bf16_to_f32(raw.y >> 16)};
-  float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  const long long items = (long long)p.T * groups;
+  const int lane = threadIdx.x & 31, sub = lane & 15;
+  const long long base = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (2 * kActRounds) + (lane >> 4);
+  uint4 raw[kActRounds];
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
-  const float s = __fdiv_rn(fmaxf(a, kMinAmax), kE4m3Max);
-  *reinterpret_cast<uint32_t*>(p.x8 + off) = quant4(v, s);
-  if (lane == 0) p.scale[(size_t)t * p.scale_t + (size_t)g * p.scale_g] = s;
+  for (int r = 0; r < kActRounds; ++r) {
+    const long long item = base + 2 * r;
+    raw[r] = make_uint4(0u, 0u, 0u, 0u);
+    if (item < items) {
+      const long long t = item / groups;
+      const int g = (int)(item - t * groups);
+      raw[r] = *reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + (size_t)g * 128 + sub * 8);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kActRounds; ++r) {
+    const long long item = base + 2 * r;
+    const uint32_t w4[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+    float v0[4], v1[4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      v0[2 * e] = bf16_to_f32(w4[e] & 0xffff);
+      v0[2 * e + 1] = bf16_to_f32(w4[e] >> 16);
+      v1[2 * e] = bf16_to_f32(w4[2 + e] & 0xffff);
+      v1[2 * e + 1] = bf16_to_f32(w4[2 + e] >> 16);
+    }
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a = fmaxf(a, fmaxf(fabsf(v0[e]), fabsf(v1[e])));
+#pragma unroll
+    for (int m = 8; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));  // within the half
+    const float s = __fdiv_rn(fmaxf(a, kMinAmax), kE4m3Max);
+    if (item < items) {
+      const long long t = item / groups;
+      const int g = (int)(item - t * groups);
+      *reinterpret_cast<uint2*>(p.x8 + (size_t)t * p.K + (size_t)g * 128 + sub * 8) =
+          make_uint2(quant4(v0, s), quant4(v1, s));
+      if (sub == 0) p.scale[(size_t)t * p.scale_t + (size_t)g * p.scale_g] = s;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(256) quant_weight_kernel(const QuantWeightArgs p) {
@@ -101,7 +132,8 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const QuantWeightArgs
 
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream) {
   const long long items = (long long)a.T * (a.K / 128);
-  quant_act_kernel<<<(unsigned)((items + 7) / 8), 256, 0, stream>>>(a);
+  if (items == 0) return cudaSuccess;
+  quant_act_kernel<<<(unsigned)((items + kActItemsPerBlock - 1) / kActItemsPerBlock), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
