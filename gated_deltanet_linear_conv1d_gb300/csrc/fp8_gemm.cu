@@ -345,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
 // registers: promotion warp w holds the 128 columns of half (w - 2) / 4 for the
 // 32 rows of its tensor-memory lane quarter.
 constexpr int kWN = 256;
+constexpr int kWStages = 4;
 constexpr int kWStageBytes = kTileBytes + kWN * kBK;   // 16 KB of X rows + 32 KB of W rows
-constexpr int kWBarOff = kStages * kWStageBytes;
+constexpr int kWBarOff = kWStages * kWStageBytes;
 constexpr int kWSmemBytes = kWBarOff + 256 + 1024;
 constexpr int kWScaleAhead = 2;  // fewer registers than the narrow kernel: the sum takes 128
 constexpr uint32_t kWIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kWN);
@@ -356,15 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
                                                                      const __grid_constant__ CUtensorMap tmw) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWBarOff);  // [kStages] TMA -> MMA
-  uint64_t* empty = full + kStages;                                 // [kStages] MMA -> TMA
-  uint64_t* tfull = empty + kStages;                                // [2] K block's product ready
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWBarOff);  // [kWStages] TMA -> MMA
+  uint64_t* empty = full + kWStages;                                // [kWStages] MMA -> TMA
+  uint64_t* tfull = empty + kWStages;                               // [2] K block's product ready
   uint64_t* tempty = tfull + 2;                                     // [2] K block's product folded
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);               // [0] abort
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kWStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -393,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int m_t = t / nt, n_t = t % nt;
         for (int kb = 0; kb < p.KB; ++kb, ++gk) {
-          const int s = gk % kStages;
-          if ((gk >= (uint32_t)kStages && !mbar_wait_bounded(&empty[s], ((gk / kStages) - 1) & 1)) ||
+          const int s = gk % kWStages;
+          if ((gk >= (uint32_t)kWStages && !mbar_wait_bounded(&empty[s], ((gk / kWStages) - 1) & 1)) ||
               *abort_flag) {
             ok = false;
             break;
@@ -408,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       if (!ok) {
         report(p.dev_err, GDN_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        for (uint32_t j = (gk > (uint32_t)kStages ? gk - kStages : 0); j < gk; ++j)
-          mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
+        for (uint32_t j = (gk > (uint32_t)kWStages ? gk - kWStages : 0); j < gk; ++j)
+          mbar_wait_bounded(&full[j % kWStages], (j / kWStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -418,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < p.KB; ++kb, ++gk) {
-          const int s = gk % kStages;
+          const int s = gk % kWStages;
           const uint32_t b = gk & 1, use = gk >> 1;
-          if (!mbar_wait_bounded(&full[s], (gk / kStages) & 1) ||
+          if (!mbar_wait_bounded(&full[s], (gk / kWStages) & 1) ||
               (gk >= 2 && !mbar_wait_bounded(&tempty[b], (use - 1) & 1)) || *abort_flag) {
             ok = false;
             break;
