@@ -146,6 +146,7 @@ def test_fp8_linear_decode_batches(b, T, K, N, res):
     (4836, 256, 2048, True),    # 38 x 8 = 304 tiles of 128 x 256: the wide tiles, ragged last row tile
     (4836, 384, 2176, False),   # the last column tile's second half lies past N
     (9800, 128, 4096, True),    # one K block, eight tiles per CTA
+    (39000, 128, 144, True),    # 305 row tiles of one ragged column tile (N = 144 < 256)
 ])
 def test_fp8_linear_wide_tiles(b, T, K, N, res):
     """Token counts with at least two waves of 128 x 256 tiles take the wide-tile kernel (the running
