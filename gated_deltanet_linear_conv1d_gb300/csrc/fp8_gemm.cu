@@ -13,9 +13,11 @@
 // product. Four tensor-memory buffers let the MMAs run up to three blocks ahead
 // of the folding.
 //
-// Output tiles are 128 tokens x 128 outputs. With at least two waves of tiles a
-// persistent CTA takes whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... and
-// stores bf16 rows directly. With fewer tiles (the decode batch) the K blocks of
+// Two schedules. With at least two waves of 128 x 256 tiles (prefill token
+// counts) fp8_gemm_wide_kernel below takes 128 tokens x 256 outputs per tile
+// (N = 256 MMAs, two 256-column buffers). Otherwise fp8_gemm_kernel takes
+// 128 x 128 tiles: with at least two waves of those a persistent CTA takes whole
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ... and stores bf16 rows directly. With fewer tiles (the decode batch) the K blocks of
 // all tiles, laid end to end, are cut into gridDim.x equal contiguous ranges
 // (stream-K), so every SM does the same work; a CTA stores the fp32 partial of a
 // tile it covers only in part into its own workspace slice (plain coalesced
