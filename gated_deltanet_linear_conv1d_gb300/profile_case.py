@@ -3,6 +3,7 @@
     python -m gated_deltanet_linear_conv1d_gb300.profile_case decode  --requests 64 --slots 128 --launches 3
     python -m gated_deltanet_linear_conv1d_gb300.profile_case prefill --lengths 2048x8 --launches 2
     python -m gated_deltanet_linear_conv1d_gb300.profile_case spec    --requests 64 --launches 2
+    python -m gated_deltanet_linear_conv1d_gb300.profile_case commit  --requests 256 --launches 3
     python -m gated_deltanet_linear_conv1d_gb300.profile_case fp8     --requests 4096 --k 6144 --n 5120
 
 Each launch is preceded by the same warm-up launches (--warmup) and followed
@@ -44,7 +45,7 @@ def _lengths(spec: str) -> list[int]:
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["decode", "prefill", "spec", "conv", "rmsnorm", "fp8"])
+    ap.add_argument("case", choices=["decode", "prefill", "spec", "commit", "conv", "rmsnorm", "fp8"])
     ap.add_argument("--heads", choices=["full", "rank"], default="full")
     ap.add_argument("--requests", type=int, default=64)
     ap.add_argument("--slots", type=int, default=0)
@@ -88,16 +89,21 @@ def main(argv=None):
                 b.gdn_chunk_prefill(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["query_start_loc"],
                                     d["slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og,
                                     has_init=d["has_init"], workspace=ws, dev_err=err)
-    elif args.case == "spec":
+    elif args.case in ("spec", "commit"):
         w = synth.spec_workload(geom, args.requests, num_pos=4, seed=4)
         d = _dev(w, dev)
         D = b.make_dims(geom, w["num_slots"])
         og = torch.empty((args.requests * 4, geom.num_v_heads * 128), dtype=torch.bfloat16, device=dev)
+        acc = torch.from_numpy(w["accepted"]).to(dev)
 
         def run():
-            b.gdn_spec_verify(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"],
-                              d["spec_slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og,
-                              dev_err=err)
+            if args.case == "commit":  # copy the accepted position's checkpoint into the live slot
+                b.gdn_spec_commit(D, acc, d["spec_slot_idx"], d["slot_idx"], d["state"], d["conv_hist"],
+                                  mode=b.GDN_COMMIT_COPY, dev_err=err)
+            else:
+                b.gdn_spec_verify(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"],
+                                  d["spec_slot_idx"], d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], ogate=og,
+                                  dev_err=err)
     elif args.case == "fp8":
         # out [T, N] = dequant(x8) dequant(w8)^T with block scales: random E4M3 codes and scales
         rng = np.random.default_rng(6)
@@ -133,7 +139,8 @@ def main(argv=None):
         if it >= args.warmup:
             times.append(e0.elapsed_time(e1))
     flag = b.gdn_read_device_error(err)
-    tokens = {"decode": args.requests, "spec": args.requests * 4, "fp8": args.requests}.get(args.case)
+    tokens = {"decode": args.requests, "spec": args.requests * 4, "commit": args.requests,
+              "fp8": args.requests}.get(args.case)
     if args.case in ("prefill", "conv"):
         tokens = T
     ms = sum(times) / max(1, len(times))
