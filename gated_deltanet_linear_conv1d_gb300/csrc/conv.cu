@@ -21,6 +21,9 @@
 // 77 % issue-active at 56 % of DRAM bandwidth), so the window is kept as floats
 // (one unpack per new input), SiLU takes one tanh.approx instead of an
 // exponential and a division, and pairs are packed with one bf16x2 conversion.
+// Then it waited on its loads: each thread now issues the next batch of rows
+// before computing the current one, and the register budget is set for six
+// 128-thread blocks per SM (five or seven moved fewer bytes per second).
 #include "device.cuh"
 #include "launch.h"
 
@@ -90,7 +93,7 @@ __device__ __forceinline__ void window_to_hist(uint32_t* hp, uint32_t w0, uint32
   hp[2] = (w1 >> 16) | (w2 & 0xffff0000u);
 }
 
-__global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p, int seg) {
+__global__ void __launch_bounds__(kThreads, 6) conv_kernel(const ConvArgs p, int seg) {
   const int c = 4 * (blockIdx.y * kThreads + threadIdx.x);  // channels c .. c + 3
   const int s0 = blockIdx.x * seg, s1 = min(s0 + seg, p.T);
 
@@ -147,12 +150,21 @@ __global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p, int se
           f[2][k] = lo_f(wb[k]); f[3][k] = hi_f(wb[k]);
         }
       }
-      // kBatch tokens at a time: all loads first, so they are in flight together
+      // kBatch tokens at a time, the next batch's loads issued before this batch is
+      // computed, so rows stay in flight while the thread computes
+      uint2 xv[kBatch];
+      {
+        const int nt = min(kBatch, end - start);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) xv[i] = i < nt ? x[(size_t)(start + i) * ld] : make_uint2(0u, 0u);
+      }
       for (int tb = start; tb < end; tb += kBatch) {
         const int nt = min(kBatch, end - tb);
-        uint2 xv[kBatch];
+        const int nt2 = min(kBatch, end - tb - kBatch);  // <= 0 after the last batch
+        uint2 xq[kBatch];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) xv[i] = i < nt ? x[(size_t)(tb + i) * ld] : make_uint2(0u, 0u);
+        for (int i = 0; i < kBatch; ++i)
+          xq[i] = i < nt2 ? x[(size_t)(tb + kBatch + i) * ld] : make_uint2(0u, 0u);
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
           if (i < nt) {
@@ -166,6 +178,8 @@ __global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p, int se
             y[(size_t)(tb + i) * ld] = make_uint2(pack2(r[0], r[1]), pack2(r[2], r[3]));
           }
         }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) xv[i] = xq[i];
       }
       // packed windows back from the floats (exact: they hold bf16 values)
       if (owner) {
