@@ -686,6 +686,36 @@ def measure_rmsnorm(b, dev, stream) -> dict:
             "kernel": "rmsnorm_kernel (gdn_rmsnorm)", "hbm_peak_gbs": hbm_peak, **res}
 
 
+def measure_gated_rmsnorm(b, dev, stream) -> dict:
+    """The gated RMSNorm on its own (Ogate = RMSNorm(o) * gamma * SiLU(z) per head, 48 heads x 128), for
+    callers that take o and z from elsewhere; the mixer kernels fuse it. Decode batch and prefill batch."""
+    import torch
+    H, Dv = 48, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    gamma = torch.rand(Dv, generator=g, device=dev) + 0.5
+    hbm_peak, _ = load_peaks()
+    res = {}
+    for name, T, steps in (("decode", NUM_REQ, 40), ("prefill", 71068, 10)):
+        nset = max(1, (1 << 30) // (T * H * Dv * 2 * 3))
+        sets = [[torch.randn((T, H, Dv), generator=g, device=dev).to(torch.bfloat16) for _ in range(2)]
+                + [torch.empty((T, H * Dv), dtype=torch.bfloat16, device=dev)] for _ in range(nset)]
+        it = [0]
+
+        def run():
+            o, z, out = sets[it[0] % nset]
+            b.gdn_gated_rmsnorm(o, z, gamma, 1e-6, out, stream=stream)
+            it[0] += 1
+
+        ms = timed(run, steps, 4, stream)
+        nbytes = 3 * T * H * Dv * 2 + Dv * 4
+        res[name] = {"tokens": T, "ms": ms, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+        del sets
+    return {"workload": "Ogate = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z), 48 heads x 128, bf16",
+            "kernel": "gated_rmsnorm_kernel (gdn_gated_rmsnorm)", "hbm_peak_gbs": hbm_peak, **res}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -829,6 +859,8 @@ def run_gpu(args):
         extra["in_proj"] = measure_in_proj(b, dev, stream, geom, D)
         torch.cuda.empty_cache()
         extra["rmsnorm"] = measure_rmsnorm(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["gated_rmsnorm"] = measure_gated_rmsnorm(b, dev, stream)
         torch.cuda.empty_cache()
         extra["fp8_proj"] = measure_fp8_proj(b, dev, stream)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

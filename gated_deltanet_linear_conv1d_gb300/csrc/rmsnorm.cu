@@ -3,9 +3,9 @@
 //
 //  * gdn_gated_rmsnorm: out = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z) per
 //    head row (gate row Ogate = RMSNorm(o) (.) SiLU(Z); section 08, the GDN
-//    output gate is SiLU after RMSNorm). One warp per row of D values; each
-//    lane holds D/32 values (4-element, 8-byte vectors). 6 bytes in and 2 out
-//    per element.
+//    output gate is SiLU after RMSNorm). One warp per row of D values, each
+//    lane holding 4-element (8-byte) groups, several rows per warp with all
+//    their loads in flight together. 6 bytes in and 2 out per element.
 //  * gdn_rmsnorm: the layer's input norm U = X / sqrt(mean(X^2) + eps) (.) gamma
 //    over the hidden size, optionally with the residual add in front of it
 //    (residual <- bf16(X + residual), U = RMSNorm(residual) (.) gamma), the
@@ -20,51 +20,63 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRowsPerBlock = kThreads / 32;
-constexpr int kMaxPerLane = 32;  // D <= 1024
+constexpr int kWarpsPerBlock = kThreads / 32;
 
+// One warp per row, R rows per warp with every load issued before any row is
+// reduced (so a warp keeps 2 R rows of o and z in flight); lane l holds the
+// 4-element groups l, l + 32, ... (U of them: D <= 128 U). The head dim of the
+// layer (128) takes U = 1, R = 4; other sizes up to 1024 take U = 8, R = 1.
+template <int U, int R>
 __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const NormArgs p) {
-  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int row0 = (blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * R;
   const int lane = threadIdx.x & 31;
-  if (row >= p.rows) return;
-  const uint16_t* o = p.o + (size_t)row * p.D;
-  const uint16_t* z = p.z + (size_t)row * p.D;
-  uint16_t* out = p.out + (size_t)row * p.D;
-  // groups of 4 consecutive elements, strided over the lanes
   const int groups = p.D / 4;
-  float ov[kMaxPerLane];
-  float ss = 0.f;
+  uint2 oraw[R][U], zraw[R][U];
 #pragma unroll
-  for (int u = 0; u < kMaxPerLane / 4; ++u) {
-    const int gi = lane + 32 * u;
-    if (gi < groups) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(o + 4 * gi);
-      ov[4 * u + 0] = bf16_to_f32(raw.x & 0xffff);
-      ov[4 * u + 1] = bf16_to_f32(raw.x >> 16);
-      ov[4 * u + 2] = bf16_to_f32(raw.y & 0xffff);
-      ov[4 * u + 3] = bf16_to_f32(raw.y >> 16);
+  for (int r = 0; r < R; ++r) {
+    const int row = row0 + r;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ss = fmaf(ov[4 * u + e], ov[4 * u + e], ss);
+    for (int u = 0; u < U; ++u) {
+      const int gi = lane + 32 * u;
+      if (row < p.rows && gi < groups) {
+        oraw[r][u] = *reinterpret_cast<const uint2*>(p.o + (size_t)row * p.D + 4 * gi);
+        zraw[r][u] = *reinterpret_cast<const uint2*>(p.z + (size_t)row * p.D + 4 * gi);
+      } else {
+        oraw[r][u] = make_uint2(0u, 0u);
+        zraw[r][u] = make_uint2(0u, 0u);
+      }
     }
   }
-  ss = warp_sum(ss);
-  const float rinv = rsqrtf(ss / (float)p.D + p.eps);
 #pragma unroll
-  for (int u = 0; u < kMaxPerLane / 4; ++u) {
-    const int gi = lane + 32 * u;
-    if (gi < groups) {
-      const uint2 zr = *reinterpret_cast<const uint2*>(z + 4 * gi);
-      const float4 gm = *reinterpret_cast<const float4*>(p.gamma + 4 * gi);
-      const float zf[4] = {bf16_to_f32(zr.x & 0xffff), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffff),
-                           bf16_to_f32(zr.y >> 16)};
-      const float gf[4] = {gm.x, gm.y, gm.z, gm.w};
-      uint16_t r[4];
+  for (int r = 0; r < R; ++r) {
+    const int row = row0 + r;
+    if (row >= p.rows) break;  // uniform over the warp
+    float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) r[e] = f32_to_bf16(ov[4 * u + e] * rinv * gf[e] * silu(zf[e]));
-      uint2 packed;
-      packed.x = (uint32_t)r[0] | ((uint32_t)r[1] << 16);
-      packed.y = (uint32_t)r[2] | ((uint32_t)r[3] << 16);
-      *reinterpret_cast<uint2*>(out + 4 * gi) = packed;
+    for (int u = 0; u < U; ++u) {
+      const float f[4] = {bf16_to_f32(oraw[r][u].x & 0xffff), bf16_to_f32(oraw[r][u].x >> 16),
+                          bf16_to_f32(oraw[r][u].y & 0xffff), bf16_to_f32(oraw[r][u].y >> 16)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = fmaf(f[e], f[e], ss);  // lanes past D hold zeros
+    }
+    ss = warp_sum(ss);
+    const float rinv = rsqrtf(ss / (float)p.D + p.eps);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gi = lane + 32 * u;
+      if (gi < groups) {
+        const float of[4] = {bf16_to_f32(oraw[r][u].x & 0xffff), bf16_to_f32(oraw[r][u].x >> 16),
+                             bf16_to_f32(oraw[r][u].y & 0xffff), bf16_to_f32(oraw[r][u].y >> 16)};
+        const float zf[4] = {bf16_to_f32(zraw[r][u].x & 0xffff), bf16_to_f32(zraw[r][u].x >> 16),
+                             bf16_to_f32(zraw[r][u].y & 0xffff), bf16_to_f32(zraw[r][u].y >> 16)};
+        const float4 gm = *reinterpret_cast<const float4*>(p.gamma + 4 * gi);
+        const float gf[4] = {gm.x, gm.y, gm.z, gm.w};
+        uint16_t q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) q[e] = f32_to_bf16(of[e] * rinv * gf[e] * silu(zf[e]));
+        *reinterpret_cast<uint2*>(p.out + (size_t)row * p.D + 4 * gi) =
+            make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+      }
     }
   }
 }
@@ -155,8 +167,13 @@ cudaError_t launch_rmsnorm(const RmsArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream) {
-  dim3 grid((a.rows + kRowsPerBlock - 1) / kRowsPerBlock, 1, 1);
-  gated_rmsnorm_kernel<<<grid, kThreads, 0, stream>>>(a);
+  if (a.D <= 128) {
+    constexpr int kR = 4;
+    const long long per_block = (long long)kWarpsPerBlock * kR;
+    gated_rmsnorm_kernel<1, kR><<<(unsigned)((a.rows + per_block - 1) / per_block), kThreads, 0, stream>>>(a);
+  } else {
+    gated_rmsnorm_kernel<8, 1><<<(unsigned)((a.rows + kWarpsPerBlock - 1) / kWarpsPerBlock), kThreads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -46,9 +46,11 @@ def test_conv_update_matches_oracle(b, lengths):
     np.testing.assert_array_equal(U.host_bits(d["conv_hist"]), hist_ref)  # bit-exact, untouched slots too
 
 
-def test_gated_rmsnorm_matches_oracle(b):
-    rng = np.random.default_rng(32)
-    T, H, D = 37, 48, 128
+@pytest.mark.parametrize("T,H,D", [(37, 48, 128), (5, 3, 64), (9, 2, 256), (3, 1, 1000), (2, 2, 1024)])
+def test_gated_rmsnorm_matches_oracle(b, T, H, D):
+    """The head dim of the layer (four rows per warp) and other row sizes (lanes past D idle, or up
+    to eight groups per lane); row counts that leave the last warp's rows partly empty."""
+    rng = np.random.default_rng(32 + D)
     o = synth.bf16_bits(rng.standard_normal((T, H, D)).astype(np.float32) * 0.3)
     z = synth.bf16_bits(rng.standard_normal((T, H, D)).astype(np.float32))
     gamma = rng.uniform(0.5, 1.5, D).astype(np.float32)
