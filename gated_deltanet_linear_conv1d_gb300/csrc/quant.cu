@@ -41,25 +41,33 @@ __device__ __forceinline__ uint32_t quant4(const float (&v)[4], float s) {
 constexpr int kActRounds = 2;
 constexpr int kActItemsPerBlock = 8 * 2 * kActRounds;
 
+// Index type I: 32-bit unsigned when the item count allows (the item -> (token,
+// group) split is then a 32-bit division, done once per item), else 64-bit.
+template <typename I>
 __global__ void __launch_bounds__(256) quant_act_kernel(const QuantActArgs p) {
-  const int groups = p.K / 128;
-  const long long items = (long long)p.T * groups;
+  const I groups = (I)(p.K / 128);
+  const I items = (I)p.T * groups;
   const int lane = threadIdx.x & 31, sub = lane & 15;
-  const long long base = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (2 * kActRounds) + (lane >> 4);
+  const I base = ((I)blockIdx.x * 8 + (I)(threadIdx.x >> 5)) * (2 * kActRounds) + (I)(lane >> 4);
   uint4 raw[kActRounds];
+  size_t off[kActRounds];  // element offset of this lane's 8 values; the scale index
+  size_t soff[kActRounds];
 #pragma unroll
   for (int r = 0; r < kActRounds; ++r) {
-    const long long item = base + 2 * r;
+    const I item = base + 2 * r;
     raw[r] = make_uint4(0u, 0u, 0u, 0u);
+    off[r] = 0;
+    soff[r] = 0;
     if (item < items) {
-      const long long t = item / groups;
-      const int g = (int)(item - t * groups);
-      raw[r] = *reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + (size_t)g * 128 + sub * 8);
+      const I t = item / groups, g = item - t * groups;
+      off[r] = (size_t)t * p.K + (size_t)g * 128 + sub * 8;
+      soff[r] = (size_t)t * p.scale_t + (size_t)g * p.scale_g;
+      raw[r] = *reinterpret_cast<const uint4*>(p.x + off[r]);
     }
   }
 #pragma unroll
   for (int r = 0; r < kActRounds; ++r) {
-    const long long item = base + 2 * r;
+    const I item = base + 2 * r;
     const uint32_t w4[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
     float v0[4], v1[4];
 #pragma unroll
@@ -76,11 +84,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const QuantActArgs p) {
     for (int m = 8; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));  // within the half
     const float s = __fdiv_rn(fmaxf(a, kMinAmax), kE4m3Max);
     if (item < items) {
-      const long long t = item / groups;
-      const int g = (int)(item - t * groups);
-      *reinterpret_cast<uint2*>(p.x8 + (size_t)t * p.K + (size_t)g * 128 + sub * 8) =
-          make_uint2(quant4(v0, s), quant4(v1, s));
-      if (sub == 0) p.scale[(size_t)t * p.scale_t + (size_t)g * p.scale_g] = s;
+      *reinterpret_cast<uint2*>(p.x8 + off[r]) = make_uint2(quant4(v0, s), quant4(v1, s));
+      if (sub == 0) p.scale[soff[r]] = s;
     }
   }
 }
@@ -133,7 +138,11 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const QuantWeightArgs
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream) {
   const long long items = (long long)a.T * (a.K / 128);
   if (items == 0) return cudaSuccess;
-  quant_act_kernel<<<(unsigned)((items + kActItemsPerBlock - 1) / kActItemsPerBlock), 256, 0, stream>>>(a);
+  const unsigned blocks = (unsigned)((items + kActItemsPerBlock - 1) / kActItemsPerBlock);
+  if (items + kActItemsPerBlock < (1LL << 32))
+    quant_act_kernel<uint32_t><<<blocks, 256, 0, stream>>>(a);
+  else
+    quant_act_kernel<unsigned long long><<<blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

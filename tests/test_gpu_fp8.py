@@ -41,6 +41,46 @@ def test_quant_act_bit_exact(b, T, K):
     np.testing.assert_array_equal(x8.cpu().numpy(), codes)
 
 
+def _e4m3_boundaries():
+    """Every rounding boundary of E4M3 below its largest finite value: midpoints between neighbouring
+    codes (subnormal spacing 2^-9 below 2^-6, then 8 steps per binade) with at most 5 significant bits."""
+    vals = [(2 * j + 1) * 2.0 ** -10 for j in range(8)]  # 0 .. 2^-6 in steps of 2^-9
+    for e in range(-6, 9):
+        vals += [(1 + (2 * j + 1) / 16) * 2.0 ** e for j in range(8)]
+    return np.array([v for v in vals if v < 448.0])
+
+
+def test_quant_act_rounding_boundaries(b):
+    """x / s landing exactly on E4M3 rounding boundaries (ties to even), once with power-of-two scales
+    (x / s exact, and x r exact too) and once with scales 1.25, 1.5, 1.75 times a power of two (x / s
+    still exact, x r not: the quotient the kernel multiplies out sits within a rounding of the
+    boundary on either side), plus each boundary's bf16 neighbours; codes and scales bit for bit."""
+    mids = _e4m3_boundaries()
+    rng = np.random.default_rng(77)
+    rows = []
+    for mult in (1.0, 1.25, 1.5, 1.75):
+        for k in (-8, -3, 0, 5):
+            sc = mult * 2.0 ** k
+            base = (mids * sc).astype(np.float32)
+            assert not np.any(base.view(np.uint32) & 0xffff)  # <= 8 significant bits: exact in bf16
+            bits = (base.view(np.uint32) >> 16).astype(np.int64)
+            for step in (0, 1, -1):  # the boundary, and the bf16 values just above and below it
+                g = np.zeros(128, np.uint16)
+                g[0] = np.float32(448.0 * sc).view(np.uint32) >> 16  # the group's largest magnitude: s = sc
+                body = (bits + step).astype(np.uint16)[:127]
+                body |= (rng.integers(0, 2, size=body.size) << 15).astype(np.uint16)  # random signs
+                g[1:1 + body.size] = body
+                rows.append(g)
+    xb = np.array(rows, np.uint16)
+    T, K = xb.shape
+    x8 = torch.zeros((T, K), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((T, 1), dtype=torch.float32, device="cuda")
+    b.gdn_fp8_quant_act(U.dev_bf16(xb), x8, xs)
+    codes, s = oracle.fp8_quant_act(xb)
+    np.testing.assert_array_equal(xs.cpu().numpy(), s)
+    np.testing.assert_array_equal(x8.cpu().numpy(), codes)
+
+
 @pytest.mark.parametrize("N,K", [(16, 128), (200, 256), (5120, 6144)])
 def test_quant_weight_bit_exact(b, N, K):
     rng = np.random.default_rng(300 + N)
