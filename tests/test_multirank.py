@@ -71,3 +71,25 @@ def test_algorithmic_byte_counts():
     chunks = 1 + 1 + 2
     assert tf32 == chunks * 48 * (2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
     assert bf16 == chunks * (48 * (4 * 128 * 64 * 128 + 2 * 128 * 64 * 64) + 16 * 2 * 128 * 64 * 128)
+
+
+def test_reference_arm_prints_one_line(tmp_path):
+    """bench.py --impl reference times the oracle on host cores and prints one JSON line with the
+    keys the driver reads; under torchrun only rank 0 prints (a rank-1 run prints nothing)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "3"]
+    out = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600, check=True)
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
+    for key in ("metric", "unit", "higher_is_better", "config", "cpu_baseline", "e2e", "dtype"):
+        assert key in line
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    out1 = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600, check=True, env=env)
+    assert out1.stdout.strip() == ""
