@@ -95,12 +95,16 @@ def test_quant_weight_bit_exact(b, N, K):
 
 
 def _operands(T, K, N, seed):
+    """Codes, block scales and a residual of the product's own magnitude (a unit-scale residual
+    would dwarf the product, and a wrong product would then still pass)."""
     rng = np.random.default_rng(seed)
     x8 = U.synth.fp8_codes(rng, (T, K))
     w8 = U.synth.fp8_codes(rng, (N, K))
     xs = rng.uniform(0.002, 0.02, size=(T, K // 128)).astype(np.float32)
     ws = rng.uniform(1e-4, 1e-3, size=((N + 127) // 128, K // 128)).astype(np.float32)
-    r = U.synth.bf16_bits(rng.normal(size=(T, N)).astype(np.float32))
+    # rms of one product entry: sum over K of two independent codes (rms 2.06 each) times the scales
+    prod_rms = np.sqrt(K) * 2.06 * 2.06 * np.sqrt(np.mean(xs ** 2)) * np.sqrt(np.mean(ws ** 2))
+    r = U.synth.bf16_bits((rng.normal(size=(T, N)) * prod_rms).astype(np.float32))
     return x8, xs, w8, ws, r
 
 
