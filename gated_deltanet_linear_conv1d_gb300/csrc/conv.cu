@@ -44,15 +44,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return r;
 }
 
-// SiLU(x) = x sigmoid(x) = (x/2)(1 + tanh(x/2)): one tanh.approx instead of an
-// exponential and a division (the result is rounded to bf16 next).
-__device__ __forceinline__ float silu_tanh(float x) {
-  const float h = 0.5f * x;
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
-  return fmaf(h, t, h);
-}
-
 // Largest n in [0, N) with qsl[n] <= t (offsets assumed non-decreasing; stays in
 // range whatever they hold).
 __device__ __forceinline__ int find_request(const int32_t* qsl, int N, int t) {

@@ -146,16 +146,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return d;
 }
 
-// SiLU(x) = x sigmoid(x) = x/2 (1 + tanh(x/2)), on the hardware tanh
-// approximation (one special-function op; its relative error, about 2^-11,
-// bounds the absolute error by |x| 2^-12).
-__device__ __forceinline__ float silu_ftz(float x) {
-  const float hx = 0.5f * x;
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hx));
-  return fmaf(hx, t, hx);
-}
-
 // Barrier 1 over warps 0-7 only (the triangular inverse runs there while the
 // other warps form Y).
 __device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -427,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       pre = fmaf(wv.y, w3[2], pre);
       pre = fmaf(wv.z, w3[1], pre);
       pre = fmaf(wv.w, w3[0], pre);
-      yv[e] = t < len ? silu_ftz(pre) : 0.f;
+      yv[e] = t < len ? silu_tanh(pre) : 0.f;
       w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
     }
     umma::st32_nowait(tm + lane_base + kT_V + tb, yv);  // v row d = this thread's lane
@@ -491,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           pre = fmaf(wqk.y, w3[2], pre);
           pre = fmaf(wqk.z, w3[1], pre);
           pre = fmaf(wqk.w, w3[0], pre);
-          ya[e] = t < L ? silu_ftz(pre) : 0.f;
+          ya[e] = t < L ? silu_tanh(pre) : 0.f;
           w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
         }
         // raw q or k, bf16: row dq of KQ, tokens (q ? 64 : 0) + tb ..
@@ -887,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           const int t = part * 16 + e;
           uint16_t* zp = ZS + t * kHeadDim + row;
           const float rinv = __shfl_sync(0xffffffffu, rinv_l, e);
-          *zp = f32_to_bf16(ov[e] * rinv * gm * silu_ftz(bf16_to_f32(*zp)));
+          *zp = f32_to_bf16(ov[e] * rinv * gm * silu_tanh(bf16_to_f32(*zp)));
         }
       }
     }

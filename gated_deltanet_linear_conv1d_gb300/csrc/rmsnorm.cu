@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const NormArgs 
         const float gf[4] = {gm.x, gm.y, gm.z, gm.w};
         uint16_t q[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) q[e] = f32_to_bf16(of[e] * rinv * gf[e] * silu(zf[e]));
+        for (int e = 0; e < 4; ++e) q[e] = f32_to_bf16(of[e] * rinv * gf[e] * silu_tanh(zf[e]));
         *reinterpret_cast<uint2*>(p.out + (size_t)row * p.D + 4 * gi) =
             make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
       }
