@@ -1,8 +1,9 @@
 """Block-scaled FP8 projections (the checkpoint format of section 04 of the Qwen3.8-27B page:
 E4M3 weights with one scale per 128 x 128 block, activations quantised per token and 128-wide
-group) against the fp64 oracle: the quantisers bit for bit (codes and scales), the tcgen05 GEMM
-element by element over ragged shapes, the split-K path at the layer's decode shapes, reuse of
-the workspace without clearing, and quantise-then-multiply end to end."""
+group) against the fp64 oracle: the quantisers bit for bit (codes and scales, including every E4M3
+rounding boundary), the tcgen05 GEMM element by element over ragged shapes, the stream-K path at
+the layer's decode shapes, the 128 x 256 wide-tile path at prefill-like token counts, reuse of the
+workspace without clearing, and quantise-then-multiply end to end."""
 import numpy as np
 import pytest
 import torch
