@@ -346,6 +346,67 @@ def timed(fn, steps: int, warmup: int, stream) -> float:
     return e0.elapsed_time(e1) / steps
 
 
+SWEEP_REQUESTS = (1, 8, 64, 256, 1024)
+SWEEP_POOL_BYTES = 512 << 20  # >= 4x L2: a slot's state is evicted before the step that uses it again
+
+
+def measure_decode_sweep(b, dev, stream, peak: float) -> dict:
+    """Decode batch sweep: R in {1, 8, 64, 256, 1024} requests x 1 token at 16/48 and at the
+    per-rank 4/12 head layout (the TP4 shard run on one GPU). The pool holds 2R slots or enough
+    slots for 512 MiB of state, whichever is more, cut into disjoint sets of R slots that the
+    steps take in turn, so every step reads states that left L2 long before (a step of R = 1 at
+    4/12 heads touches only 1.5 MiB). The steps are captured in a CUDA graph (64 launches, each
+    on its own slot set) and the graph is replayed: at small R a launch takes a few
+    microseconds, less than the Python call that issues it, so launches from Python would time
+    the host. Each point: ms per launch from CUDA events around the replays on the launching
+    stream, tokens/s, and the fraction of the measured copy bandwidth that the point's own
+    algorithmic bytes reach."""
+    import torch
+    out = {}
+    per_graph = 64
+    for name, geom in (("16x48", synth.FULL_HEADS), ("4x12", synth.RANK_HEADS)):
+        slot_bytes = geom.num_v_heads * geom.head_v_dim * geom.head_k_dim * 4
+        for R in SWEEP_REQUESTS:
+            Rs = max(2 * R, -(-SWEEP_POOL_BYTES // slot_bytes))
+            sets = Rs // R
+            d = device_workload(geom, Rs, R, seed=900 + R, dev=dev)
+            gen = torch.Generator(device="cpu")
+            gen.manual_seed(R)
+            perm = torch.randperm(Rs, generator=gen)[: sets * R].to(torch.int32).view(sets, R).to(dev)
+            D = b.make_dims(geom, Rs)
+            og = torch.empty((R, geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def launch(i):  # on the current stream (the capture stream while capturing)
+                b.gdn_decode_step(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], perm[i % sets],
+                                  d["alpha"], d["beta"], d["z"], d["gamma"], 1e-6, ogate=og, dev_err=err)
+
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for i in range(3):
+                    launch(i)
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(per_graph):
+                    launch(i)
+            probe = timed(graph.replay, 2, 2, stream) / per_graph
+            reps = int(min(200, max(3, 80.0 / max(probe * per_graph, 1e-3))))
+            ms = timed(graph.replay, reps, 2, stream) / per_graph
+            if b.gdn_read_device_error(err) != 0:
+                raise RuntimeError(f"device error flagged in the decode sweep ({name}, R={R})")
+            nbytes = decode_bytes_per_launch(geom, R)
+            out[f"{name}_R{R}"] = {"requests": R, "slots": Rs, "slot_sets": sets, "launches": reps * per_graph,
+                                   "ms_per_step": ms, "tokens_per_s": R / (ms / 1e3),
+                                   "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                                   "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peak}
+            del graph, d, perm, og
+            torch.cuda.empty_cache()
+    return out
+
+
 def measure_prefill(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
     """Varlen chunked prefill: 64 requests, log-uniform lengths in [16, 8192], half from zero."""
     import torch
@@ -849,6 +910,8 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     extra = {}
     if not args.decode_only:
+        extra["decode_sweep"] = measure_decode_sweep(b, dev, stream, peak)
+        torch.cuda.empty_cache()
         extra["prefill"] = measure_prefill(b, dev, stream)
         torch.cuda.empty_cache()
         extra["spec_mixed"] = measure_spec_mixed(b, dev, stream)

@@ -131,6 +131,16 @@ def _need(t, name: str, dtype, shape=None, optional: bool = False):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _scratch(nbytes: int, device, stream) -> torch.Tensor:
+    """Device scratch for one call. Freed when the caller drops it; recorded on the call's
+    stream, so the caching allocator does not hand it out again before that stream's work
+    (the launch that uses it) has finished."""
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if isinstance(stream, torch.cuda.Stream):
+        t.record_stream(stream)
+    return t
+
+
 def _check(status: int, what: str):
     if status != GDN_OK:
         raise GdnError(status, what)
@@ -203,7 +213,7 @@ def gdn_chunk_prefill(dims, qkv0, conv_w, conv_hist, state, query_start_loc, slo
     _need(dev_err, "dev_err", torch.int32, (1,), optional=True)
     need = gdn_prefill_workspace_bytes(dims, N, T)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=qkv0.device)
+        workspace = _scratch(need, qkv0.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.gdn_chunk_prefill(ctypes.byref(dims), _ptr(qkv0), _ptr(conv_w), _ptr(conv_hist), _ptr(state),
                                   _ptr(query_start_loc), _ptr(slot_idx), _ptr(has_init), _ptr(alpha),
@@ -234,7 +244,7 @@ def gdn_chunk_prefill_align(dims, qkv0, conv_w, conv_hist, state, query_start_lo
     _need(dev_err, "dev_err", torch.int32, (1,), optional=True)
     need = gdn_prefill_workspace_bytes(dims, N, T)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=qkv0.device)
+        workspace = _scratch(need, qkv0.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.gdn_chunk_prefill_align(ctypes.byref(dims), _ptr(qkv0), _ptr(conv_w), _ptr(conv_hist), _ptr(state),
                                         _ptr(query_start_loc), _ptr(slot_idx), _ptr(has_init), _ptr(alpha),

@@ -164,14 +164,14 @@ gdn_status gdn_spec_verify(const gdn_dims* d, const uint16_t* qkv0, const float*
   if (!o && !ogate) return GDN_ERR_INVALID_ARG;
   if (ogate && (!z || !gamma)) return GDN_ERR_INVALID_ARG;
   if (!eps_ok(eps)) return GDN_ERR_INVALID_ARG;
-  if (!aligned(state, 16) || !aligned(conv_w, 16)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(state, 16) || !aligned(conv_w, 16) || !aligned(qkv0, 16) || !aligned(conv_hist, 16) ||
+      (ogate && !aligned(z, 16)))
+    return GDN_ERR_INVALID_ARG;
   StepArgs a{qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma, eps, o, ogate,
              dev_err, d->num_k_heads, d->num_v_heads, d->num_v_heads / d->num_k_heads, channels(d),
              d->num_slots, num_seqs, num_pos};
-  // the streaming kernel when its shared-memory ring fits, else one CTA per (head, request)
-  if (stream_supported(a.G, a.P) && aligned(qkv0, 16) && aligned(conv_hist, 16) && (!ogate || aligned(z, 16)))
-    return from_cuda(launch_stream(a, static_cast<cudaStream_t>(stream)));
-  return from_cuda(launch_step(a, /*spec=*/true, static_cast<cudaStream_t>(stream)));
+  if (!stream_supported(a.G, a.P)) return GDN_ERR_UNSUPPORTED;  // never for the supported geometry
+  return from_cuda(launch_stream(a, static_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_spec_commit(const gdn_dims* d, const int32_t* accepted, const int32_t* spec_slot_idx,
@@ -261,7 +261,7 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
                                      int32_t* dev_err, void* stream) {
   gdn_status st = check_dims(d);
   if (st != GDN_OK) return st;
-  if (num_seqs < 0 || num_tokens < 0 || num_seqs > 65535) return GDN_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_tokens < 0) return GDN_ERR_INVALID_ARG;
   if (num_seqs > gdn::kStaticPrefillMaxSeqs ||
       (long long)num_seqs * d->num_k_heads > gdn::kStaticPrefillMaxTickets)
     return GDN_ERR_INVALID_ARG;  // beyond the fixed schedule arrays

@@ -144,8 +144,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (function, device).
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
-size_t step_smem_bytes(int P);
-cudaError_t launch_step(const StepArgs& a, bool spec, cudaStream_t stream);
 // Persistent state-streaming kernel (decode: P = 1, spec_slot NULL; verify: P >= 1).
 bool stream_supported(int G, int P);
 cudaError_t launch_stream(const StepArgs& a, cudaStream_t stream);
@@ -154,8 +152,9 @@ cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
 // Largest request count the allocation-free prefill accepts: the size of its
-// file-scope schedule array (one int32 per request, 256 KiB).
-constexpr int kStaticPrefillMaxSeqs = 65536;
+// file-scope schedule array (one int32 per request, just under 256 KiB). It is
+// also the largest count any prefill launch takes (requests go on gridDim.y).
+constexpr int kStaticPrefillMaxSeqs = 65535;
 constexpr int kStaticPrefillMaxTickets = 1 << 20;  // requests x key heads
 // Device address of that array on the current device, looked up once per
 // device with cudaGetSymbolAddress and cached.

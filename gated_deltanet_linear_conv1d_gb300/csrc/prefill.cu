@@ -1039,25 +1039,62 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 static __device__ __align__(256) int32_t g_static_prefill_order[kStaticPrefillMaxSeqs];
 static __device__ __align__(256) int32_t g_static_prefill_tickets[kStaticPrefillMaxTickets];
 
+namespace {
+
+// Id of the calling thread's current CUDA context (0 when there is none yet).
+// The arrays above get new addresses when the device's context is torn down and
+// made again (cudaDeviceReset), so the cached addresses are keyed by it.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+}  // namespace
+
 cudaError_t static_prefill_order(int32_t** order, int32_t** tickets) {
   constexpr int kMaxDevices = 64;
+  struct Entry {
+    unsigned long long ctx;
+    int32_t* order;
+    int32_t* tickets;
+  };
   static std::mutex mu;
-  static int32_t* cache[kMaxDevices][2] = {};
+  static Entry cache[kMaxDevices] = {};
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev][0]) {
+  Entry& e = cache[dev];
+  const unsigned long long ctx = current_context_id();
+  if (!e.order || ctx == 0 || ctx != e.ctx) {
     void* po = nullptr;
     void* pt = nullptr;
     if ((err = cudaGetSymbolAddress(&po, g_static_prefill_order)) != cudaSuccess) return err;
     if ((err = cudaGetSymbolAddress(&pt, g_static_prefill_tickets)) != cudaSuccess) return err;
-    cache[dev][0] = static_cast<int32_t*>(po);
-    cache[dev][1] = static_cast<int32_t*>(pt);
+    e.order = static_cast<int32_t*>(po);
+    e.tickets = static_cast<int32_t*>(pt);
+    e.ctx = current_context_id();  // the lookup above has made the context current
   }
-  *order = cache[dev][0];
-  *tickets = cache[dev][1];
+  *order = e.order;
+  *tickets = e.tickets;
   return cudaSuccess;
 }
 

@@ -136,7 +136,9 @@ gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *x, const float 
  * counter that the library keeps per stream (a static array of 64, given to
  * streams in order of first use and reused round-robin after that). Calls on
  * one stream run one after another; calls that run at the same time must be
- * on streams holding different counters, i.e. at most 64 streams in use. A
+ * on streams holding different counters, i.e. at most 64 streams in use. The
+ * per-thread default stream (cudaStreamPerThread) is a different stream in
+ * every thread, and each calling thread gets its own counter for it. A
  * captured graph keeps the counter of the stream it was captured on. The same
  * holds for gdn_spec_verify.
  */
@@ -225,13 +227,16 @@ gdn_status gdn_chunk_prefill_align(const gdn_dims *dims, const uint16_t *qkv0, c
  * computes.
  *
  * Its scratch is two fixed file-scope device arrays per device: the schedule,
- * 65536 int32 (256 KiB), and the (request, key head) tickets, 2^20 int32
- * (4 MiB): num_seqs above 65536, or num_seqs x num_k_heads above 2^20, is
- * rejected with GDN_ERR_INVALID_ARG. The library allocates nothing; the first call on each
- * device looks up the arrays' addresses (cudaGetSymbolAddress) and caches them, so
- * make that first call before any stream capture. The scratch needs no
- * clearing. Calls that overlap in time on one device (two streams, or two
- * threads) race on the arrays: serialise them.
+ * 65535 int32 (just under 256 KiB), and the (request, key head) tickets, 2^20
+ * int32 (4 MiB): num_seqs above 65535, or num_seqs x num_k_heads above 2^20,
+ * is rejected with GDN_ERR_INVALID_ARG before anything is launched. Every GPU
+ * that loads the library holds the two arrays until the process exits. The
+ * library allocates nothing; the first call on each device looks up the
+ * arrays' addresses (cudaGetSymbolAddress) and caches them per device and
+ * context (looked up again after cudaDeviceReset), so make that first call
+ * before any stream capture. The scratch needs no clearing. Calls that
+ * overlap in time on one device (two streams, or two threads) race on the
+ * arrays: serialise them.
  *
  * Arguments, layouts, errors: as gdn_chunk_prefill, without workspace and
  * workspace_bytes.
@@ -259,6 +264,8 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims *dims, const uint16_t *qkv0,
  *   conv_hist, state: the pools (live slots read, checkpoint slots written)
  *   slot_idx [N];  spec_slot_idx [N][P] int32, distinct from every live slot
  *   num_pos: 1 <= P <= 8
+ * qkv0, conv_w, conv_hist, state and (with ogate) z must be 16-byte aligned
+ * (GDN_ERR_INVALID_ARG otherwise): the kernel stages them with bulk copies.
  */
 gdn_status gdn_spec_verify(const gdn_dims *dims, const uint16_t *qkv0, const float *conv_w,
                            uint16_t *conv_hist, float *state, const int32_t *slot_idx,

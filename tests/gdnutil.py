@@ -76,7 +76,7 @@ def to_device(w: dict) -> dict:
     return d
 
 
-def oracle_compact(w: dict, requests, qsl=None, ckpt=False):
+def oracle_compact(w: dict, requests, qsl=None, want_y=False):
     """Runs the oracle on the given requests only, with their slots gathered into a compact pool.
 
     Returns (result dict, token index array). Slot gather/scatter is exercised by
@@ -95,5 +95,28 @@ def oracle_compact(w: dict, requests, qsl=None, ckpt=False):
     has_init = None if "has_init" not in w else np.ascontiguousarray(w["has_init"][requests])
     r = oracle.forward(dims, w["qkv0"][toks], w["conv_w"], hist, st, sub_qsl,
                        np.arange(len(requests), dtype=np.int32), w["alpha"][toks], w["beta"][toks],
-                       w["z"][toks], w["gamma"], w["eps"], has_init=has_init, inplace=True)
+                       w["z"][toks], w["gamma"], w["eps"], has_init=has_init, want_y=want_y, inplace=True)
+    return r, toks
+
+
+def oracle_spec_compact(w: dict, requests):
+    """The oracle's speculative verify on the given requests only: their live slots and
+    checkpoint slots are gathered into a compact pool (live slot of request i at i, its
+    checkpoints at len(requests) + i * P + p). Returns the oracle's result dict with
+    "state" / "conv_hist" holding only the checkpoint slots, [len(requests) * P, ...],
+    in request-major order, and the token index array of the requests' positions."""
+    requests = np.asarray(requests)
+    dims = w["dims"]
+    P = int(w["spec_slot_idx"].shape[1])
+    R = len(requests)
+    live = w["slot_idx"][requests]
+    ck = w["spec_slot_idx"][requests].reshape(-1)
+    st = np.ascontiguousarray(np.concatenate([w["state"][live], w["state"][ck]]))
+    hist = np.ascontiguousarray(np.concatenate([w["conv_hist"][live], w["conv_hist"][ck]]))
+    toks = (requests[:, None] * P + np.arange(P)[None, :]).reshape(-1)
+    r = oracle.spec_verify(dims, w["qkv0"][toks], w["conv_w"], hist, st, np.arange(R, dtype=np.int32),
+                           (R + np.arange(R * P, dtype=np.int32)).reshape(R, P), w["alpha"][toks],
+                           w["beta"][toks], w["z"][toks], w["gamma"], w["eps"], inplace=True)
+    r["state"] = r["state"][R:]
+    r["conv_hist"] = r["conv_hist"][R:]
     return r, toks

@@ -130,3 +130,28 @@ def test_fp8_entry_points_reject_bad_arguments_on_the_host(b):
     assert lib.gdn_fp8_linear(p, p, p, p, odd, p, 4, 128, 32, None, 0, None, None) == b.GDN_ERR_INVALID_ARG
     assert lib.gdn_fp8_linear(None, None, None, None, None, None, 0, 128, 32, None, 0, None, None) == b.GDN_OK
     assert lib.gdn_fp8_linear_workspace_bytes(256, 100, 5120) == 0  # K not a multiple of 128
+
+
+def test_noalloc_prefill_limits_are_checked_on_the_host(b):
+    """The allocation-free prefill refuses, before any CUDA call, request counts beyond its fixed
+    schedule (65,535) and (request, key head) pairs beyond its fixed ticket array (2^20)."""
+    lib = b._lib
+    p = ctypes.c_void_p(256)  # never dereferenced
+    for geom, n in ((synth.RANK_HEADS, 65536), (synth.Dims(32, 32, 128, 128, 4), 40000),
+                    (synth.Dims(16, 16, 128, 128, 4), 65536 + 1)):
+        D = b.make_dims(geom, 4)
+        assert lib.gdn_chunk_prefill_noalloc(ctypes.byref(D), p, p, p, p, p, p, None, p, p, p, p, 1e-6, None, p,
+                                             n, 100, None, None) == b.GDN_ERR_INVALID_ARG, (geom, n)
+
+
+def test_spec_verify_rejects_misaligned_inputs_on_the_host(b):
+    """gdn_spec_verify streams qkv0, the conv history and z with 16-byte copies: a buffer off
+    that alignment is refused before any launch."""
+    lib = b._lib
+    d = b.make_dims(synth.RANK_HEADS, 8)
+    a, odd = ctypes.c_void_p(256), ctypes.c_void_p(258)  # never dereferenced
+    args = [a] * 10  # qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma
+    for i in (0, 2, 8):  # qkv0, conv_hist, z
+        bad = list(args)
+        bad[i] = odd
+        assert lib.gdn_spec_verify(ctypes.byref(d), *bad, 1e-6, None, a, 2, 4, None, None) == b.GDN_ERR_INVALID_ARG

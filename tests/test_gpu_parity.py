@@ -179,7 +179,10 @@ def test_decode_is_deterministic(b):
 
 @pytest.mark.parametrize("N", [5, 256])
 def test_spec_verify_and_commit(b, N):
-    dims = synth.FULL_HEADS if N == 5 else synth.RANK_HEADS
+    """Speculative verify at the full head layout: 5 requests (all checked) and the mixed
+    workload's 256 requests x 4 positions (32 sampled requests checked against the oracle,
+    every request's commit checked bit for bit)."""
+    dims = synth.FULL_HEADS
     w = synth.spec_workload(dims, N, num_pos=4, seed=47 + N)
     P = w["num_pos"]
     d = U.to_device(w)
@@ -190,33 +193,84 @@ def test_spec_verify_and_commit(b, N):
     b.gdn_spec_verify(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["slot_idx"], d["spec_slot_idx"],
                       d["alpha"], d["beta"], d["z"], d["gamma"], w["eps"], o=o, ogate=og, dev_err=err)
     assert b.gdn_read_device_error(err) == 0
-    sample = np.arange(N) if N <= 8 else np.sort(np.random.default_rng(1).choice(N, 24, replace=False))
-    ref = oracle.spec_verify(dims, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], w["slot_idx"],
-                             w["spec_slot_idx"], w["alpha"], w["beta"], w["z"], w["gamma"], w["eps"])
-    toks = (sample[:, None] * P + np.arange(P)[None, :]).reshape(-1)
-    U.check_out(U.host_f64_from_bf16(o)[toks], ref["o"][toks], "o")
-    U.check_out(U.host_f64_from_bf16(og)[toks], ref["ogate"][toks], "ogate")
+    sample = np.arange(N) if N <= 8 else np.sort(np.random.default_rng(1).choice(N, 32, replace=False))
+    ref, toks = U.oracle_spec_compact(w, sample)
+    U.check_out(U.host_f64_from_bf16(o)[toks], ref["o"], "o")
+    U.check_out(U.host_f64_from_bf16(og)[toks], ref["ogate"], "ogate")
     ck = w["spec_slot_idx"][sample].reshape(-1)
     idx = torch.from_numpy(ck.astype(np.int64)).cuda()
-    U.check_state(d["state"][idx].cpu().numpy(), ref["state"][ck], U.STATE_REL_L2_DECODE, "checkpoints")
-    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), ref["conv_hist"][ck])
+    U.check_state(d["state"][idx].cpu().numpy(), ref["state"], U.STATE_REL_L2_DECODE, "checkpoints")
+    np.testing.assert_array_equal(U.host_bits(d["conv_hist"][idx]), ref["conv_hist"])
     live = torch.from_numpy(w["slot_idx"].astype(np.int64)).cuda()
-    np.testing.assert_array_equal(d["state"][live].cpu().numpy(), w["state"][w["slot_idx"]])  # live untouched
+    for n in range(0, N, 64):  # live slots untouched (in slices, to bound host memory)
+        sl = live[n:n + 64]
+        np.testing.assert_array_equal(d["state"][sl].cpu().numpy(), w["state"][w["slot_idx"][n:n + 64]])
 
     # commit by copy: the live slot becomes the accepted checkpoint, bit for bit
-    state_before = d["state"].clone()
-    hist_before = d["conv_hist"].clone()
+    src = torch.from_numpy(w["spec_slot_idx"][np.arange(N), w["accepted"]].astype(np.int64)).cuda()
     b.gdn_spec_commit(D, d["accepted"], d["spec_slot_idx"], d["slot_idx"], d["state"], d["conv_hist"],
                       mode=b.GDN_COMMIT_COPY, dev_err=err)
     assert b.gdn_read_device_error(err) == 0
-    src = torch.from_numpy(w["spec_slot_idx"][np.arange(N), w["accepted"]].astype(np.int64)).cuda()
-    assert torch.equal(d["state"][live], state_before[src])
-    assert torch.equal(d["conv_hist"][live], hist_before[src])
+    assert torch.equal(d["state"][live], d["state"][src])
+    assert torch.equal(d["conv_hist"][live], d["conv_hist"][src])
     # commit by repoint: only the slot index changes
     slots = d["slot_idx"].clone()
     b.gdn_spec_commit(D, d["accepted"], d["spec_slot_idx"], slots, mode=b.GDN_COMMIT_REPOINT, dev_err=err)
     assert b.gdn_read_device_error(err) == 0
     assert torch.equal(slots.long(), src)
+
+
+@pytest.mark.parametrize("two_streams", [False, True], ids=["one_stream", "two_streams"])
+def test_mixed_verify_commit_and_prefill_step(b, two_streams):
+    """The speculative-verify step with a prefill in the same step: 256 requests x 4 positions
+    verified and committed (copy) at the full head layout, and 8 prefill requests of 2048 tokens
+    (half from zero) over their own pool, on one stream back to back or with the prefill on a
+    second stream. Verify outputs and checkpoints of 32 sampled requests against the oracle;
+    every committed slot bit for bit; every prefill output, state and history against the oracle."""
+    dims = synth.FULL_HEADS
+    N = 256
+    wv = synth.spec_workload(dims, N, num_pos=4, seed=70)
+    P = wv["num_pos"]
+    wp = synth.prefill_workload(dims, [2048] * 8, seed=71)
+    dv, dp = U.to_device(wv), U.to_device(wp)
+    Dv, Dp = b.make_dims(dims, wv["num_slots"]), b.make_dims(dims, wp["num_slots"])
+    Tp = 8 * 2048
+    og_v = torch.zeros((N * P, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    og_p = torch.zeros((Tp, dims.num_v_heads * 128), dtype=torch.bfloat16, device="cuda")
+    err_v, err_p = _dev_err(), _dev_err()
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream() if two_streams else main
+    side.wait_stream(main)
+    torch.cuda.synchronize()
+    b.gdn_spec_verify(Dv, dv["qkv0"], dv["conv_w"], dv["conv_hist"], dv["state"], dv["slot_idx"],
+                      dv["spec_slot_idx"], dv["alpha"], dv["beta"], dv["z"], dv["gamma"], wv["eps"], ogate=og_v,
+                      dev_err=err_v, stream=main)
+    b.gdn_chunk_prefill(Dp, dp["qkv0"], dp["conv_w"], dp["conv_hist"], dp["state"], dp["query_start_loc"],
+                        dp["slot_idx"], dp["alpha"], dp["beta"], dp["z"], dp["gamma"], wp["eps"], ogate=og_p,
+                        has_init=dp["has_init"], dev_err=err_p, stream=side)
+    b.gdn_spec_commit(Dv, dv["accepted"], dv["spec_slot_idx"], dv["slot_idx"], dv["state"], dv["conv_hist"],
+                      mode=b.GDN_COMMIT_COPY, dev_err=err_v, stream=main)
+    torch.cuda.synchronize()
+    assert b.gdn_read_device_error(err_v) == 0 and b.gdn_read_device_error(err_p) == 0
+    # verify: sampled requests' outputs and checkpoints
+    sample = np.sort(np.random.default_rng(2).choice(N, 32, replace=False))
+    ref, toks = U.oracle_spec_compact(wv, sample)
+    U.check_out(U.host_f64_from_bf16(og_v)[toks], ref["ogate"], "verify ogate")
+    ck = torch.from_numpy(wv["spec_slot_idx"][sample].reshape(-1).astype(np.int64)).cuda()
+    U.check_state(dv["state"][ck].cpu().numpy(), ref["state"], U.STATE_REL_L2_DECODE, "verify checkpoints")
+    np.testing.assert_array_equal(U.host_bits(dv["conv_hist"][ck]), ref["conv_hist"])
+    # commit: every live slot equals its accepted checkpoint, and for the sample the oracle's
+    live = torch.from_numpy(wv["slot_idx"].astype(np.int64)).cuda()
+    src = torch.from_numpy(wv["spec_slot_idx"][np.arange(N), wv["accepted"]].astype(np.int64)).cuda()
+    assert torch.equal(dv["state"][live], dv["state"][src])
+    assert torch.equal(dv["conv_hist"][live], dv["conv_hist"][src])
+    acc = wv["accepted"][sample]
+    sel = np.arange(len(sample)) * P + acc
+    live_s = torch.from_numpy(wv["slot_idx"][sample].astype(np.int64)).cuda()
+    U.check_state(dv["state"][live_s].cpu().numpy(), ref["state"][sel], U.STATE_REL_L2_DECODE, "committed state")
+    np.testing.assert_array_equal(U.host_bits(dv["conv_hist"][live_s]), ref["conv_hist"][sel])
+    # prefill: all 8 requests
+    _check_prefill(wp, dp, None, og_p, np.arange(8))
 
 
 def test_spec_commit_rejects_bad_accepted_length(b):
@@ -291,14 +345,15 @@ def test_prefill_many_short_requests(b):
     np.testing.assert_array_equal(U.host_bits(d["conv_hist"][slots]), r["conv_hist"])
 
 
-def test_prefill_varlen_64_requests_sampled(b):
-    """64 requests, log-uniform lengths in [16, 8192], half from zero; sampled requests checked."""
+def test_prefill_varlen_64_requests(b):
+    """64 requests, log-uniform lengths in [16, 8192] (71,068 tokens at this seed), half from
+    zero: every request's outputs, final state and conv history against the oracle (checked in
+    groups of requests to bound host memory)."""
     lengths = synth.loguniform_lengths(np.random.default_rng(3), 64, 16, 8192)
     w = synth.prefill_workload(synth.FULL_HEADS, lengths, seed=3)
     d, o, og = _run_prefill(b, w, want_o=False)
-    order = np.argsort(lengths)
-    sample = np.unique(np.concatenate([order[:2], order[-1:], order[30:32]]))
-    _check_prefill(w, d, None, og, sample)
+    for g in range(0, 64, 16):
+        _check_prefill(w, d, None, og, np.arange(g, g + 16))
 
 
 def test_prefill_then_decode_continues_the_request(b):

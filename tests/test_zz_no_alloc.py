@@ -71,9 +71,44 @@ def test_noalloc_prefill_matches_the_workspace_entry_point(b):
 
 
 def test_noalloc_prefill_rejects_too_many_requests(b):
-    D = b.make_dims(synth.RANK_HEADS, 4)
+    """Beyond the fixed arrays: more than 65,535 requests, or more than 2^20 (request, key head)
+    tickets with an accepted request count (40,000 requests x 32 key heads)."""
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
-    st = b._lib.gdn_chunk_prefill_noalloc(b.ctypes.byref(D), None, dummy.data_ptr(), dummy.data_ptr(),
-                                          dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), None, None, None,
-                                          None, None, 1e-6, None, dummy.data_ptr(), 65537, 0, None, None)
-    assert st == b.GDN_ERR_INVALID_ARG
+    p = dummy.data_ptr()
+    for geom, n in ((synth.RANK_HEADS, 65536), (synth.RANK_HEADS, 65537), (synth.Dims(32, 32, 128, 128, 4), 40000)):
+        D = b.make_dims(geom, 4)
+        st = b._lib.gdn_chunk_prefill_noalloc(b.ctypes.byref(D), None, p, p, p, p, p, None, None, None, None, None,
+                                              1e-6, None, p, n, 0, None, None)
+        assert st == b.GDN_ERR_INVALID_ARG, (geom, n)
+
+
+def test_noalloc_prefill_at_its_request_limit(b):
+    """65,535 one-token requests from zero (one key head and one value head, so the pools stay
+    small): the largest count the fixed schedule takes runs, and matches gdn_chunk_prefill."""
+    geom = synth.Dims(1, 1, 128, 128, 4)
+    N = 65535
+    D = b.make_dims(geom, N)
+    rng = np.random.default_rng(62)
+    T = N
+    qkv0 = U.dev_bf16(synth.bf16_bits(rng.standard_normal((T, geom.channels)).astype(np.float32)))
+    conv_w = U.dev((rng.standard_normal((geom.channels, 4)) * 0.25).astype(np.float32))
+    alpha = U.dev(np.exp(-rng.uniform(0.001, 0.1, (T, 1))).astype(np.float32))
+    beta = U.dev(rng.uniform(0, 1, (T, 1)).astype(np.float32))
+    z = U.dev_bf16(synth.bf16_bits(rng.standard_normal((T, 1, 128)).astype(np.float32)))
+    gamma = torch.ones(128, dtype=torch.float32, device="cuda")
+    qsl = torch.arange(N + 1, dtype=torch.int32, device="cuda")
+    slots = torch.from_numpy(rng.permutation(N).astype(np.int32)).cuda()
+    has_init = torch.zeros(N, dtype=torch.uint8, device="cuda")
+    outs = []
+    for fn, ws in ((b.gdn_chunk_prefill, True), (b.gdn_chunk_prefill_noalloc, False)):
+        state = torch.zeros((N, 1, 128, 128), dtype=torch.float32, device="cuda")
+        hist = torch.zeros((N, geom.channels, 3), dtype=torch.bfloat16, device="cuda")
+        og = torch.zeros((T, 128), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fn(D, qkv0, conv_w, hist, state, qsl, slots, alpha, beta, z, gamma, 1e-6, ogate=og, has_init=has_init,
+           dev_err=err)
+        assert b.gdn_read_device_error(err) == 0
+        outs.append((og, state, hist))
+    assert outs[0][0].any()
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
