@@ -579,14 +579,13 @@ def measure_conv(b, dev, stream, steps: int = 10, warmup: int = 3) -> dict:
 
 
 def measure_out_proj(b, dev, stream) -> dict:
-    """Wo projection + residual add (6144 -> 5120, bf16, cuBLASLt) at the decode batch (weight-streaming:
+    """Wo projection + residual add (6144 -> 5120, bf16, the library's tcgen05 GEMM) at the decode batch (weight-streaming:
     four distinct weight matrices in rotation, 252 MB, so no step finds its weights in L2) and at the
     prefill batch's token count (tensor-bound)."""
     import torch
     K, N = 6144, 5120
     g = torch.Generator(device=dev)
     g.manual_seed(5)
-    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device=dev)
     weights = [(torch.randn((N, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16) for _ in range(4)]
     res = {}
     p_bf16, _, kind = load_bf16_peak()
@@ -597,7 +596,7 @@ def measure_out_proj(b, dev, stream) -> dict:
         it = [0]
 
         def run():
-            b.gdn_out_proj(a, weights[it[0] % 4], hidden, residual=hidden, workspace=ws, stream=stream)
+            b.gdn_out_proj(a, weights[it[0] % 4], hidden, residual=hidden, stream=stream)
             it[0] += 1
 
         ms = timed(run, steps, 4, stream)
@@ -608,12 +607,14 @@ def measure_out_proj(b, dev, stream) -> dict:
                      "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
         del a, hidden
     return {"workload": "out = Ogate Wo^T + residual, K=6144 -> N=5120, bf16 in/out, fp32 accumulation",
-            "kernel": "cuBLASLt (gdn_out_proj)", "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
+            "kernel": "gemm_bf16_kernel (gdn_out_proj): at the decode batch swapped 128-weight-row x 256-token "
+                      "tiles, K split 3 ways over clusters; at the prefill batch 128 x 256 tiles on persistent CTAs",
+            "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
             "hbm_peak_gbs": hbm_peak, **res}
 
 
 def measure_in_proj(b, dev, stream, geom, D) -> dict:
-    """The in_proj rows (hidden 5120 -> QKV0 10240, Z 6144, a|b 96 fp32; three cuBLASLt GEMMs) at the
+    """The in_proj rows (hidden 5120 -> QKV0 10240, Z 6144, a|b 96 fp32; one launch of the tcgen05 GEMM) at the
     decode batch (weight-streaming: two weight sets in rotation, 338 MB, so no step finds its weights in
     L2) and at the prefill batch's token count (tensor-bound)."""
     import torch
@@ -621,7 +622,6 @@ def measure_in_proj(b, dev, stream, geom, D) -> dict:
     CH, NZ, NAB = geom.channels, geom.num_v_heads * geom.head_v_dim, 2 * geom.num_v_heads
     g = torch.Generator(device=dev)
     g.manual_seed(6)
-    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device=dev)
     sets = [[(torch.randn((n, Dh), generator=g, device=dev) / Dh ** 0.5).to(torch.bfloat16) for n in (CH, NZ, NAB)]
             for _ in range(2)]
     res = {}
@@ -636,20 +636,20 @@ def measure_in_proj(b, dev, stream, geom, D) -> dict:
 
         def run():
             wq, wz, wab = sets[it[0] % 2]
-            b.gdn_in_proj(D, u, wq, wz, qkv0, z, w_ab=wab, ab=ab, workspace=ws, stream=stream)
+            b.gdn_in_proj(D, u, wq, wz, qkv0, z, w_ab=wab, ab=ab, stream=stream)
             it[0] += 1
 
         ms = timed(run, steps, 4, stream)
         flops = 2.0 * T * Dh * (CH + NZ + NAB)
-        # weights once, the hidden rows once per GEMM, the outputs once
-        nbytes = (CH + NZ + NAB) * Dh * 2 + 3 * T * Dh * 2 + T * (CH + NZ) * 2 + T * NAB * 4
+        # weights once, the hidden rows once, the outputs once
+        nbytes = (CH + NZ + NAB) * Dh * 2 + T * Dh * 2 + T * (CH + NZ) * 2 + T * NAB * 4
         res[name] = {"tokens": T, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
                      "tensor_frac": flops / (ms / 1e3) / 1e12 / p_bf16,
                      "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
         del u, qkv0, z, ab
     return {"workload": "QKV0 = U Wqkv^T, Z = U Wz^T, [a|b] = U Wab^T, 5120 -> 10240 / 6144 / 96, bf16 in, "
                         "bf16 / bf16 / fp32 out, fp32 accumulation",
-            "kernel": "cuBLASLt (gdn_in_proj)", "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
+            "kernel": "gemm_bf16_kernel (gdn_in_proj, the three outputs in one launch)", "peak_bf16_tflops": p_bf16, "peak_kind": f"{kind} bf16 burst",
             "hbm_peak_gbs": hbm_peak, **res}
 
 

@@ -65,8 +65,8 @@ def _load() -> ctypes.CDLL:
         "gdn_spec_verify": [D, P, P, P, P, P, P, P, P, P, P, f32, P, P, i32, i32, P, P],
         "gdn_spec_commit": [D, P, P, P, P, P, i32, i32, i32, P, P],
         "gdn_gated_rmsnorm": [P, P, P, f32, P, i32, i32, i32, P],
-        "gdn_out_proj": [P, P, P, P, i32, i32, i32, P, sz, P],
-        "gdn_in_proj": [D, P, i32, P, P, P, P, P, P, i32, P, sz, P],
+        "gdn_out_proj": [P, P, P, P, i32, i32, i32, P, P],
+        "gdn_in_proj": [D, P, i32, P, P, P, P, P, P, i32, P, P],
         "gdn_rmsnorm": [P, P, P, f32, P, i32, i32, P],
         "gdn_fp8_quant_act": [P, P, P, i32, i32, P],
         "gdn_fp8_quant_weight": [P, P, P, i32, i32, P],
@@ -82,8 +82,6 @@ def _load() -> ctypes.CDLL:
         getattr(lib, name).restype = sz
     lib.gdn_prefill_workspace_bytes.argtypes = [D, i32, i32]
     lib.gdn_prefill_workspace_bytes.restype = sz
-    lib.gdn_out_proj_workspace_bytes.argtypes = []
-    lib.gdn_out_proj_workspace_bytes.restype = sz
     lib.gdn_fp8_linear_workspace_bytes.argtypes = [i32, i32, i32]
     lib.gdn_fp8_linear_workspace_bytes.restype = sz
     lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -277,11 +275,7 @@ def gdn_chunk_prefill_noalloc(dims, qkv0, conv_w, conv_hist, state, query_start_
            "gdn_chunk_prefill_noalloc")
 
 
-def gdn_out_proj_workspace_bytes() -> int:
-    return int(_lib.gdn_out_proj_workspace_bytes())
-
-
-def gdn_out_proj(ogate, w, out, residual=None, workspace=None, stream=None):
+def gdn_out_proj(ogate, w, out, residual=None, dev_err=None, stream=None):
     """out[T][N] = ogate[T][K] w[N][K]^T (+ residual[T][N]); residual may be out itself."""
     T, K = ogate.shape
     N = w.shape[0]
@@ -289,8 +283,8 @@ def gdn_out_proj(ogate, w, out, residual=None, workspace=None, stream=None):
     _need(w, "w", torch.bfloat16, (N, K))
     _need(out, "out", torch.bfloat16, (T, N))
     _need(residual, "residual", torch.bfloat16, (T, N), optional=True)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_lib.gdn_out_proj(_ptr(ogate), _ptr(w), _ptr(residual), _ptr(out), T, K, N, _ptr(workspace), ws_bytes,
+    _need(dev_err, "dev_err", torch.int32, (1,), optional=True)
+    _check(_lib.gdn_out_proj(_ptr(ogate), _ptr(w), _ptr(residual), _ptr(out), T, K, N, _ptr(dev_err),
                              _stream(stream)), "gdn_out_proj")
 
 
@@ -345,8 +339,9 @@ def gdn_fp8_linear(x8, x_scale, w8, w_scale, out, residual=None, workspace=None,
                                _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)), "gdn_fp8_linear")
 
 
-def gdn_in_proj(dims, hidden, w_qkv, w_z, qkv0, z, w_ab=None, ab=None, workspace=None, stream=None):
-    """QKV0 = hidden W_qkv^T, Z = hidden W_z^T and, when given, [a | b] = hidden W_ab^T (fp32)."""
+def gdn_in_proj(dims, hidden, w_qkv, w_z, qkv0, z, w_ab=None, ab=None, dev_err=None, stream=None):
+    """QKV0 = hidden W_qkv^T, Z = hidden W_z^T and, when given, [a | b] = hidden W_ab^T (fp32), in one
+    launch."""
     T, Dh = hidden.shape
     _need(hidden, "hidden", torch.bfloat16, (T, Dh))
     _need(w_qkv, "w_qkv", torch.bfloat16, (dims.channels, Dh))
@@ -355,9 +350,9 @@ def gdn_in_proj(dims, hidden, w_qkv, w_z, qkv0, z, w_ab=None, ab=None, workspace
     _need(z, "z", torch.bfloat16, (T, dims.num_v_heads * dims.head_v_dim))
     _need(w_ab, "w_ab", torch.bfloat16, (2 * dims.num_v_heads, Dh), optional=True)
     _need(ab, "ab", torch.float32, (T, 2 * dims.num_v_heads), optional=True)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _need(dev_err, "dev_err", torch.int32, (1,), optional=True)
     _check(_lib.gdn_in_proj(ctypes.byref(dims), _ptr(hidden), Dh, _ptr(w_qkv), _ptr(w_z), _ptr(w_ab), _ptr(qkv0),
-                            _ptr(z), _ptr(ab), T, _ptr(workspace), ws_bytes, _stream(stream)), "gdn_in_proj")
+                            _ptr(z), _ptr(ab), T, _ptr(dev_err), _stream(stream)), "gdn_in_proj")
 
 
 def gdn_spec_verify(dims, qkv0, conv_w, conv_hist, state, slot_idx, spec_slot_idx, alpha, beta, z, gamma, eps,

@@ -71,7 +71,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     newest = max(os.path.getmtime(o) for o in objs)
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lcublasLt",
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static",
                "-Xlinker", "-rpath=" + os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -285,29 +285,27 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* d, const uint16_t* qkv0, co
   return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
-size_t gdn_out_proj_workspace_bytes(void) { return (size_t)32 << 20; }
-
 gdn_status gdn_out_proj(const uint16_t* ogate, const uint16_t* w, const uint16_t* residual, uint16_t* out,
-                        int32_t num_tokens, int32_t in_features, int32_t out_features, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+                        int32_t num_tokens, int32_t in_features, int32_t out_features, int32_t* dev_err,
+                        void* stream) {
   if (num_tokens < 0 || in_features <= 0 || out_features <= 0) return GDN_ERR_INVALID_ARG;
   if (in_features % 8 != 0 || out_features % 8 != 0) return GDN_ERR_UNSUPPORTED;
   if (num_tokens == 0) return GDN_OK;
   if (!ogate || !w || !out) return GDN_ERR_INVALID_ARG;
   if (!aligned(ogate, 16) || !aligned(w, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
     return GDN_ERR_INVALID_ARG;
-  if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return GDN_ERR_INVALID_ARG;
-  bool unsupported = false;
-  const cudaError_t e = launch_linear(ogate, w, residual, out, false, num_tokens, in_features, out_features,
-                                      workspace_bytes ? workspace : nullptr, workspace_bytes,
-                                      static_cast<cudaStream_t>(stream), &unsupported);
-  if (unsupported) return GDN_ERR_UNSUPPORTED;
-  return from_cuda(e);
+  GemmOperands o{};
+  o.x = ogate;
+  o.T = num_tokens;
+  o.K = in_features;
+  o.nseg = 1;
+  o.seg[0] = GemmSegOperands{w, out, residual, out_features, false};
+  return from_cuda(launch_gemm(o, dev_err, static_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_in_proj(const gdn_dims* d, const uint16_t* hidden, int32_t hidden_size, const uint16_t* w_qkv,
                        const uint16_t* w_z, const uint16_t* w_ab, uint16_t* qkv0, uint16_t* z, float* ab,
-                       int32_t num_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+                       int32_t num_tokens, int32_t* dev_err, void* stream) {
   gdn_status st = check_dims(d);
   if (st != GDN_OK) return st;
   if (num_tokens < 0 || hidden_size <= 0) return GDN_ERR_INVALID_ARG;
@@ -318,20 +316,18 @@ gdn_status gdn_in_proj(const gdn_dims* d, const uint16_t* hidden, int32_t hidden
   if (!aligned(hidden, 16) || !aligned(w_qkv, 16) || !aligned(qkv0, 16) || !aligned(w_z, 16) || !aligned(z, 16) ||
       (w_ab && (!aligned(w_ab, 16) || !aligned(ab, 16))))
     return GDN_ERR_INVALID_ARG;
-  if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return GDN_ERR_INVALID_ARG;
-  void* ws = workspace_bytes ? workspace : nullptr;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  bool unsupported = false;
-  cudaError_t e = launch_linear(hidden, w_qkv, nullptr, qkv0, false, num_tokens, hidden_size, CH, ws,
-                                workspace_bytes, s, &unsupported);
-  if (e == cudaSuccess)
-    e = launch_linear(hidden, w_z, nullptr, z, false, num_tokens, hidden_size, NZ, ws, workspace_bytes, s,
-                      &unsupported);
-  if (e == cudaSuccess && w_ab)
-    e = launch_linear(hidden, w_ab, nullptr, ab, true, num_tokens, hidden_size, NAB, ws, workspace_bytes, s,
-                      &unsupported);
-  if (unsupported) return GDN_ERR_UNSUPPORTED;
-  return from_cuda(e);
+  GemmOperands o{};
+  o.x = hidden;
+  o.T = num_tokens;
+  o.K = hidden_size;
+  o.seg[0] = GemmSegOperands{w_qkv, qkv0, nullptr, CH, false};
+  o.seg[1] = GemmSegOperands{w_z, z, nullptr, NZ, false};
+  o.nseg = 2;
+  if (w_ab) {
+    o.seg[2] = GemmSegOperands{w_ab, ab, nullptr, NAB, true};
+    o.nseg = 3;
+  }
+  return from_cuda(launch_gemm(o, dev_err, static_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_gated_rmsnorm(const uint16_t* o, const uint16_t* z, const float* gamma, float eps, uint16_t* out,

@@ -303,10 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
         if (tid == 2 * 32)
           flags[1] = aborted ? 0 : (atomicAdd(p.tile_cnt + t, 1) == (int)(c_last - c_first));
         promo_sync();
-        if (flags[1] != 0) {  // this CTA finished the tile's last piece: add the others
+        if (flags[1] != 0) {  // this CTA finished the tile's last piece: add up the pieces
           __threadfence();
+          // every piece (this CTA's too) from the workspace, in CTA order: the sum does
+          // not depend on which CTA finished last, so results are reproducible
+#pragma unroll
+          for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
           for (long long c2 = c_first; c2 <= c_last; ++c2) {
-            if (c2 == blockIdx.x) continue;
             const int first_t = (int)((c2 * p.total / G) / p.KB);
             const float4* src = slice(c2, t == first_t ? 0 : 1);
 #pragma unroll

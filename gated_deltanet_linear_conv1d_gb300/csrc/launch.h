@@ -160,11 +160,43 @@ constexpr int kStaticPrefillMaxTickets = 1 << 20;  // requests x key heads
 // device with cudaGetSymbolAddress and cached.
 cudaError_t static_prefill_order(int32_t** order, int32_t** tickets);
 
-// out[T][N] = x[T][K] w[N][K]^T (+ residual[T][N]) through cuBLASLt, bf16
-// operands, fp32 accumulation, out (and residual) bf16 or fp32; sets
-// *unsupported when the library offers no algorithm for the shape.
-cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, const void* residual, void* out, bool out_f32, int T,
-                          int K, int N, void* workspace, size_t ws_bytes, cudaStream_t stream, bool* unsupported);
+// bf16 GEMM with up to three outputs sharing one input:
+//   out_s[T][N_s] = x[T][K] w_s[N_s][K]^T (+ residual_s[T][N_s]), fp32 accumulation,
+// out_s bf16 (with an optional bf16 residual, in place allowed) or fp32.
+struct GemmSegOperands {
+  const uint16_t* w;         // [N][K] bf16
+  void* out;                 // [T][N] bf16 or fp32
+  const uint16_t* residual;  // [T][N] bf16 or nullptr (bf16 out only)
+  int N;
+  bool out_f32;
+};
+struct GemmOperands {
+  const uint16_t* x;  // [T][K] bf16
+  int T, K;
+  GemmSegOperands seg[3];
+  int nseg;
+};
+struct GemmSeg {
+  uint16_t* out_bf16;
+  float* out_f32;
+  const uint16_t* residual;
+  int N;
+  int tiles;  // n-tiles of this output per m-tile
+};
+struct GemmArgs {
+  GemmSeg seg[3];
+  int nseg;
+  int T, K, KB;
+  int swap;         // 1: A = 128 weight rows, B = all T <= 256 tokens
+  int nt_tok;       // swapped: MMA N = T rounded up to 16
+  int mt;           // m-tiles (1 when swapped)
+  int tiles_per_m;  // sum of the outputs' n-tiles
+  int pairs;        // pair tiles: two A tiles sharing one B tile
+  int split;        // pairs per cluster, each one split-th of K; 1: clusters of one pair, persistent
+  int32_t* dev_err;
+};
+// Launches the bf16 GEMM (no scratch memory: a split K meets in a cluster's shared memory).
+cudaError_t launch_gemm(const GemmOperands& o, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t stream);
 cudaError_t launch_rmsnorm(const RmsArgs& a, cudaStream_t stream);
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream);

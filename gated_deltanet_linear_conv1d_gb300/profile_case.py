@@ -5,6 +5,7 @@
     python -m gated_deltanet_linear_conv1d_gb300.profile_case spec    --requests 64 --launches 2
     python -m gated_deltanet_linear_conv1d_gb300.profile_case commit  --requests 256 --launches 3
     python -m gated_deltanet_linear_conv1d_gb300.profile_case fp8     --requests 4096 --k 6144 --n 5120
+    python -m gated_deltanet_linear_conv1d_gb300.profile_case gemm    --requests 256 --k 6144 --n 5120
 
 Each launch is preceded by the same warm-up launches (--warmup) and followed
 by a device synchronisation; nothing else runs on the GPU besides the input
@@ -45,14 +46,14 @@ def _lengths(spec: str) -> list[int]:
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["decode", "prefill", "spec", "commit", "conv", "rmsnorm", "fp8"])
+    ap.add_argument("case", choices=["decode", "prefill", "spec", "commit", "conv", "rmsnorm", "fp8", "gemm"])
     ap.add_argument("--heads", choices=["full", "rank"], default="full")
     ap.add_argument("--requests", type=int, default=64)
     ap.add_argument("--slots", type=int, default=0)
     ap.add_argument("--lengths", default="2048x8", help="prefill lengths, e.g. 2048x8 or 16,300,8192")
     ap.add_argument("--loguniform", type=int, default=0, help="prefill: N log-uniform lengths in [16, 8192]")
-    ap.add_argument("--k", type=int, default=6144, help="fp8: input features")
-    ap.add_argument("--n", type=int, default=5120, help="fp8: output features")
+    ap.add_argument("--k", type=int, default=6144, help="fp8, gemm: input features")
+    ap.add_argument("--n", type=int, default=5120, help="fp8, gemm: output features")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     args = ap.parse_args(argv)
@@ -117,6 +118,17 @@ def main(argv=None):
 
         def run():
             b.gdn_fp8_linear(x8, xs, w8, ws, out, workspace=wsp, dev_err=err)
+    elif args.case == "gemm":
+        # out [T, N] = x [T, K] w[N, K]^T + out (gdn_out_proj, the residual in place)
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        T, K, N = args.requests, args.k, args.n
+        x = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+        wt = (torch.randn((N, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+        out = torch.randn((T, N), generator=g, device=dev).to(torch.bfloat16)
+
+        def run():
+            b.gdn_out_proj(x, wt, out, residual=out, dev_err=err)
     else:
         rng = np.random.default_rng(5)
         T = args.requests
@@ -140,7 +152,7 @@ def main(argv=None):
             times.append(e0.elapsed_time(e1))
     flag = b.gdn_read_device_error(err)
     tokens = {"decode": args.requests, "spec": args.requests * 4, "commit": args.requests,
-              "fp8": args.requests}.get(args.case)
+              "fp8": args.requests, "gemm": args.requests}.get(args.case)
     if args.case in ("prefill", "conv"):
         tokens = T
     ms = sum(times) / max(1, len(times))

@@ -110,7 +110,7 @@ def shard_out_proj_weight(shard: HeadShard, wo):
 
 
 def decode_out_proj_step(b, shard: HeadShard, dims_rank, num_slots: int, inputs: dict, slot_idx, gamma, eps,
-                         wo_rank, hidden, group=None, workspace=None, stream=None):
+                         wo_rank, hidden, group=None, stream=None):
     """One decode step of the rank's heads, then its Wo partial, then the sum over ranks.
 
     inputs: the rank's slices (shard_step_inputs) as device tensors; the rank's state and history
@@ -125,8 +125,7 @@ def decode_out_proj_step(b, shard: HeadShard, dims_rank, num_slots: int, inputs:
     b.gdn_decode_step(D, inputs["qkv0"], inputs["conv_w"], inputs["conv_hist"], inputs["state"], slot_idx,
                       inputs["alpha"], inputs["beta"], inputs["z"], gamma, eps, ogate=og, stream=stream)
     part = torch.empty((N, wo_rank.shape[0]), dtype=torch.bfloat16, device=og.device)
-    b.gdn_out_proj(og, wo_rank, part, residual=hidden if shard.rank == 0 else None, workspace=workspace,
-                   stream=stream)
+    b.gdn_out_proj(og, wo_rank, part, residual=hidden if shard.rank == 0 else None, stream=stream)
     if shard.world > 1 and dist.is_available() and dist.is_initialized():
         dist.all_reduce(part, op=dist.ReduceOp.SUM, group=group)
     return part

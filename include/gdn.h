@@ -323,25 +323,24 @@ gdn_status gdn_rmsnorm(const uint16_t *x, uint16_t *residual, const float *gamma
 /*
  * gdn_in_proj - the input projections in front of the mixer core: QKV0 = U
  * W_qkv^T, Z = U W_z^T and (optionally) the raw a, b projections [a | b] = U
- * W_ab^T, bf16 operands, fp32 accumulation. Page: section 01 GDN operator
- * table, the in_proj rows ([T,5120] -> QKV0 [T,10240], Z [T,6144], a and b
- * [T,48]). The 4-tap conv that the table puts right after is fused into the
- * mixer entry points that read QKV0; the map from a, b to alpha, beta is not
- * on the pages, so a, b come out raw (fp32).
+ * W_ab^T, bf16 operands, fp32 accumulation, in one launch of the library's
+ * tcgen05 GEMM (the three outputs share the input tiles). Page: section 01 GDN
+ * operator table, the in_proj rows ([T,5120] -> QKV0 [T,10240], Z [T,6144], a
+ * and b [T,48]). The 4-tap conv that the table puts right after is fused into
+ * the mixer entry points that read QKV0; the map from a, b to alpha, beta is
+ * not on the pages, so a, b come out raw (fp32).
  *
  *   hidden  [T][D] bf16, D = hidden_size (a multiple of 8)
  *   w_qkv   [CH][D] bf16;  qkv0 [T][CH] bf16 out      (the nn.Linear weight layout)
  *   w_z     [Hv*dv][D] bf16;  z [T][Hv*dv] bf16 out
  *   w_ab    [2*Hv][D] bf16 or NULL;  ab [T][2*Hv] fp32 out or NULL (both or neither;
  *           a in columns 0 .. Hv-1, b in Hv .. 2Hv-1)
- *   workspace, workspace_bytes: as gdn_out_proj (shared by the three GEMMs,
- *           which run one after another on the stream)
+ *   dev_err GDN_DEVERR_TIMEOUT if a bounded wait inside the kernel ran out, or NULL
  * Pointers 16-byte aligned.
  */
 gdn_status gdn_in_proj(const gdn_dims *dims, const uint16_t *hidden, int32_t hidden_size,
                        const uint16_t *w_qkv, const uint16_t *w_z, const uint16_t *w_ab, uint16_t *qkv0,
-                       uint16_t *z, float *ab, int32_t num_tokens, void *workspace, size_t workspace_bytes,
-                       void *stream);
+                       uint16_t *z, float *ab, int32_t num_tokens, int32_t *dev_err, void *stream);
 
 /*
  * FP8 block-scaled projections. Page "Qwen3.8-27B: from model structure to vLLM
@@ -386,29 +385,29 @@ gdn_status gdn_fp8_linear(const uint8_t *x8, const float *x_scale, const uint8_t
 
 /*
  * gdn_out_proj - the output projection after the mixer core and the residual
- * add: out = ogate W^T (+ residual), bf16 operands, fp32 accumulation, bf16
- * out (round to nearest even). Page: section 01 GDN operator table, the Wo row
- * ([T,6144] -> [T,5120]) and the residual stream around the mixer. The gated
- * RMSNorm that the page puts before Wo is fused into the mixer entry points'
- * ogate output, so this is a plain GEMM; it runs through cuBLASLt.
+ * add: out = ogate W^T (+ residual), bf16 operands, fp32 accumulation in tensor
+ * memory, bf16 out (round to nearest even). Page: section 01 GDN operator
+ * table, the Wo row ([T,6144] -> [T,5120]) and the residual stream around the
+ * mixer. The gated RMSNorm that the page puts before Wo is fused into the mixer
+ * entry points' ogate output, so this is a plain GEMM, run by the library's own
+ * tcgen05 kernel: 128-token x 256-output tiles for large T; for T <= 256 the
+ * operands swap (128 weight rows x all tokens per tile, every weight byte read
+ * once); when the tiles leave at least half the SMs idle, a cluster of up to 4
+ * CTAs splits each tile's K range and adds the partial tiles up in shared
+ * memory, in a fixed order (the bits do not depend on timing). It allocates
+ * nothing and takes no workspace.
  *
  *   ogate     [T][K] bf16 (T = num_tokens, K = in_features)
  *   w         [N][K] bf16, the nn.Linear weight layout (N = out_features)
  *   residual  [T][N] bf16 or NULL; may equal out (in-place residual add)
  *   out       [T][N] bf16
- *   workspace device scratch of workspace_bytes (may be 0 / NULL; the
- *             library's choice of algorithm can depend on it), 256-byte aligned;
- *             gdn_out_proj_workspace_bytes() is the recommended size. Two
- *             calls in flight at once need two workspaces.
+ *   dev_err   GDN_DEVERR_TIMEOUT if a bounded wait inside the kernel ran out, or NULL.
  * Pointers 16-byte aligned; K and N multiples of 8 (GDN_ERR_UNSUPPORTED
- * otherwise, and when the library has no algorithm for the shape).
+ * otherwise).
  */
 gdn_status gdn_out_proj(const uint16_t *ogate, const uint16_t *w, const uint16_t *residual, uint16_t *out,
-                        int32_t num_tokens, int32_t in_features, int32_t out_features, void *workspace,
-                        size_t workspace_bytes, void *stream);
-
-/* Recommended workspace for gdn_out_proj: 32 MiB. */
-size_t gdn_out_proj_workspace_bytes(void);
+                        int32_t num_tokens, int32_t in_features, int32_t out_features, int32_t *dev_err,
+                        void *stream);
 
 /* Bytes of one slot of the fp32 state pool: Hv*dv*dk*4 (3 MiB at 48x128x128,
  * the L00 table's "3 MiB per sequence per layer"). 0 for invalid dims. */

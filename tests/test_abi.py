@@ -96,14 +96,14 @@ def test_in_proj_rejects_bad_arguments_on_the_host(b):
     P = ctypes.c_void_p
     fake = P(256)  # never dereferenced: every call below is rejected or returns before a launch
     # hidden size not a multiple of 8
-    assert lib.gdn_in_proj(ctypes.byref(D), fake, 5121, fake, fake, None, fake, fake, None, 4, None, 0,
-                           None) == b.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_in_proj(ctypes.byref(D), fake, 5121, fake, fake, None, fake, fake, None, 4,
+                           None, None) == b.GDN_ERR_UNSUPPORTED
     # w_ab without ab
-    assert lib.gdn_in_proj(ctypes.byref(D), fake, 5120, fake, fake, fake, fake, fake, None, 4, None, 0,
-                           None) == b.GDN_ERR_INVALID_ARG
+    assert lib.gdn_in_proj(ctypes.byref(D), fake, 5120, fake, fake, fake, fake, fake, None, 4,
+                           None, None) == b.GDN_ERR_INVALID_ARG
     # no tokens: nothing to do
-    assert lib.gdn_in_proj(ctypes.byref(D), None, 5120, None, None, None, None, None, None, 0, None, 0,
-                           None) == b.GDN_OK
+    assert lib.gdn_in_proj(ctypes.byref(D), None, 5120, None, None, None, None, None, None, 0,
+                           None, None) == b.GDN_OK
 
 
 def test_rmsnorm_rejects_bad_arguments_on_the_host(b):

@@ -33,8 +33,7 @@ def _case(T, K, N, seed):
 def test_out_proj_matches_oracle(b, T, K, N, res):
     a, w, r = _case(T, K, N, 80 + T)
     out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device="cuda")
-    b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), out, residual=U.dev_bf16(r) if res else None, workspace=ws)
+    b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), out, residual=U.dev_bf16(r) if res else None)
     U.check_out(U.host_f64_from_bf16(out), oracle.out_proj(a, w, r if res else None), "out")
 
 
@@ -43,12 +42,11 @@ def test_out_proj_full_layer_in_place_residual(b):
     T, K, N = 256, 6144, 5120
     a, w, r = _case(T, K, N, 90)
     hidden = U.dev_bf16(r)
-    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device="cuda")
-    b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), hidden, residual=hidden, workspace=ws)
+    b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), hidden, residual=hidden)
     U.check_out(U.host_f64_from_bf16(hidden), oracle.out_proj(a, w, r), "hidden")
 
 
-def test_out_proj_without_workspace_and_empty(b):
+def test_out_proj_small_and_empty(b):
     a, w, _ = _case(33, 128, 256, 91)
     out = torch.zeros((33, 256), dtype=torch.bfloat16, device="cuda")
     b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), out)
@@ -76,9 +74,8 @@ def test_in_proj_matches_oracle(b, heads, T, Dh, with_ab):
     qkv0 = torch.zeros((T, dims.channels), dtype=torch.bfloat16, device="cuda")
     z = torch.zeros((T, dims.num_v_heads * dims.head_v_dim), dtype=torch.bfloat16, device="cuda")
     ab = torch.zeros((T, 2 * dims.num_v_heads), dtype=torch.float32, device="cuda") if with_ab else None
-    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device="cuda")
     b.gdn_in_proj(D, U.dev_bf16(u), U.dev_bf16(w_qkv), U.dev_bf16(w_z), qkv0, z,
-                  w_ab=U.dev_bf16(w_ab) if with_ab else None, ab=ab, workspace=ws)
+                  w_ab=U.dev_bf16(w_ab) if with_ab else None, ab=ab)
     U.check_out(U.host_f64_from_bf16(qkv0), oracle.out_proj(u, w_qkv), "qkv0")
     U.check_out(U.host_f64_from_bf16(z), oracle.out_proj(u, w_z), "z")
     if with_ab:
@@ -86,3 +83,47 @@ def test_in_proj_matches_oracle(b, heads, T, Dh, with_ab):
         ref = oracle.out_proj(u, w_ab)
         # fp32 output: only the accumulation order differs from the fp64 sum
         assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max()), "ab"
+
+
+# ---------------------------------------------------------------- the GEMM's schedules and tile shapes
+
+@pytest.mark.parametrize("T,K,N", [
+    (1, 200, 136),      # swapped tiles (<= 256 tokens): one token, a ragged K slice, a partial weight tile
+    (17, 6144, 520),    # swapped, 5 weight tiles: K split over clusters of 4 CTAs
+    (128, 64, 8),       # swapped, one K slice (no split possible), eight weight rows
+    (129, 1000, 1032),  # swapped, the second half of the token columns partly used, K split 4 ways
+    (256, 5120, 384),   # swapped, the full token width (N = 256 MMAs), K split 4 ways
+    (256, 6144, 5120),  # the decode-batch Wo: 40 weight tiles, K split 3 ways
+    (257, 640, 264),    # 128-token tiles (more than 256 tokens), a partial token tile, K split 4 ways
+    (1000, 6144, 512),  # 128-token tiles, 16 tiles, K split 4 ways
+    (20000, 256, 1032), # 128-token tiles, many waves: whole tiles on persistent CTAs
+])
+def test_gemm_schedules_match_oracle(b, T, K, N):
+    a, w, r = _case(T, K, N, 300 + T)
+    out = U.dev_bf16(r)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), out, residual=out, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    U.check_out(U.host_f64_from_bf16(out), oracle.out_proj(a, w, r), "out")
+    # the split K adds its partial tiles in a fixed order: a second call gives the same bits
+    out2 = U.dev_bf16(r)
+    b.gdn_out_proj(U.dev_bf16(a), U.dev_bf16(w), out2, residual=out2, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("T", [3, 300])
+def test_in_proj_three_outputs_one_launch_ragged(b, T):
+    """Three outputs of ragged widths (a 4/12-head layer: 2560, 1536 and 24 fp32 columns) from one
+    input, swapped (3 tokens) and 128-token (300 tokens) tiles."""
+    dims = U.synth.RANK_HEADS
+    u, (w_qkv, w_z, w_ab) = _in_proj_case(dims, T, 5120, 500 + T)
+    D = b.make_dims(dims, 1)
+    qkv0 = torch.zeros((T, dims.channels), dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros((T, dims.num_v_heads * dims.head_v_dim), dtype=torch.bfloat16, device="cuda")
+    ab = torch.zeros((T, 2 * dims.num_v_heads), dtype=torch.float32, device="cuda")
+    b.gdn_in_proj(D, U.dev_bf16(u), U.dev_bf16(w_qkv), U.dev_bf16(w_z), qkv0, z, w_ab=U.dev_bf16(w_ab), ab=ab)
+    U.check_out(U.host_f64_from_bf16(qkv0), oracle.out_proj(u, w_qkv), "qkv0")
+    U.check_out(U.host_f64_from_bf16(z), oracle.out_proj(u, w_z), "z")
+    ref = oracle.out_proj(u, w_ab)
+    assert np.abs(ab.cpu().numpy().astype(np.float64) - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())

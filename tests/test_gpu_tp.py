@@ -32,7 +32,6 @@ def test_tp_decode_out_proj_matches_unsharded_oracle(b, world):
     hidden = synth.bf16_bits(rng.normal(size=(N, 5120)).astype(np.float32))
     d = U.to_device(w)
     wo_d, hid_d = U.dev_bf16(wo), U.dev_bf16(hidden)
-    ws = torch.empty(b.gdn_out_proj_workspace_bytes(), dtype=torch.uint8, device="cuda")
     total = torch.zeros((N, 5120), dtype=torch.float32, device="cuda")
     states = []
     for r in range(world):
@@ -40,7 +39,7 @@ def test_tp_decode_out_proj_matches_unsharded_oracle(b, world):
         part = tp.shard_step_inputs(s, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], d["alpha"], d["beta"],
                                     d["z"])
         out = tp.decode_out_proj_step(b, s, s.geometry(dims.conv_kernel), w["num_slots"], part, d["slot_idx"],
-                                      d["gamma"], w["eps"], tp.shard_out_proj_weight(s, wo_d), hid_d, workspace=ws)
+                                      d["gamma"], w["eps"], tp.shard_out_proj_weight(s, wo_d), hid_d)
         total += out.float()  # the all-reduce of the ranks' partials
         states.append((s, part["state"]))
     torch.cuda.synchronize()
