@@ -23,10 +23,10 @@
 // the whole request. The raw QKV0 rows and the z rows of the next chunk are
 // fetched by TMA while the current chunk runs. Per chunk:
 //   conv + SiLU (CUDA cores, thread = channel x token range) -> raw q, k (bf16,
-//       channel-major), k e^g (bf16), k (tf32, channel-major), v (fp32), |q|, |k|
+//       channel-major), k (tf32, channel-major), v (fp32), |q|, |k|
 //   [K;Q] K^T                 tcgen05 bf16  M=128 N=64  K=128  (operands MN-major)
 //   S0 -> bf16 operand, S *= e^{g_C} in tensor memory
-//   X = S0 Kg^T, Z = S0 Q^T   tcgen05 bf16  M=128 N=64  K=128
+//   [X' | Z] = S0 [K;Q]^T      tcgen05 bf16  M=128 N=128 K=128 (X = X' diag(e^g) at read-out)
 //   A, P from K K^T, Q K^T;  T = (I + A)^-1 on CUDA cores (recursive doubling
 //       over 16-row blocks), written as Tb = T diag(b) in tf32
 //   Y = V^T - X  -> tf32;  E^T = Y Tb^T   tcgen05 tf32 M=128 N=64 K=64
@@ -58,7 +58,7 @@ constexpr float kInvSqrtDk = 0.08838834764831845f;
 
 // Shared-memory regions (byte offsets, 1024-aligned).
 constexpr int kKQ = 0;                  // bf16 [128 dk][128 t]: k tokens 0-63, q tokens 64-127 (MN-major)
-constexpr int kKG = kKQ + 32768;        // bf16 [128 dk][64 t]: k e^g (MN-major B)      | later E bf16 [128 dv][64 t]
+constexpr int kKG = kKQ + 32768;        // bf16 [128 dv][64 t]: E (K-major A of O' = E^T P^T)
 constexpr int kKT = kKG + 16384;        // tf32 [128 dk][64 t]: raw k (K-major B)
 constexpr int kS0 = kKT + 32768;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
 // Scratch: raw q and k rows of a chunk [2 parts][64 t][128] bf16 (TMA, read by
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   umma::fence_after_sync();
 
   const uint32_t id_kk = umma::idesc(umma::kBF16, true, true, 128, 128);
-  const uint32_t id_xz = umma::idesc(umma::kBF16, false, true, 128, 64);
+  const uint32_t id_xz = umma::idesc(umma::kBF16, false, true, 128, 128);  // [X' | Z] = S0 [K; Q]^T
   const uint32_t id_e = umma::idesc(umma::kTF32, false, false, 128, 64);
   const uint32_t id_s = umma::idesc(umma::kTF32, false, false, 128, 128);
   const uint32_t id_o = umma::idesc(umma::kBF16, false, false, 128, 64);
@@ -488,10 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(dq, ((isq ? kC : 0) + tb) * 2, 256)) =
             make_uint4(pack_bf16(ya[0], ya[1]), pack_bf16(ya[2], ya[3]), pack_bf16(ya[4], ya[5]), pack_bf16(ya[6], ya[7]));
         if (!isq) {
-          // k e^g (bf16) and raw k (tf32)
-          *reinterpret_cast<uint4*>(KGb + umma::tile_off(dq, tb * 2, 128)) =
-              make_uint4(pack_bf16(ya[0] * egv[tb + 0], ya[1] * egv[tb + 1]), pack_bf16(ya[2] * egv[tb + 2], ya[3] * egv[tb + 3]),
-                         pack_bf16(ya[4] * egv[tb + 4], ya[5] * egv[tb + 5]), pack_bf16(ya[6] * egv[tb + 6], ya[7] * egv[tb + 7]));
+          // raw k (tf32)
           *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4, 256)) =
               make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
           *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4 + 16, 256)) =
@@ -536,14 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       umma::st32(tm + lane_base + col, v);
     }
     sync_for_mma();
-    // ---- X = S0 Kg^T and Z = S0 Q^T (bf16)
+    // ---- X' = S0 K^T and Z = S0 Q^T in one MMA over [K; Q] (bf16)
     if (tid == 0) {
 #pragma unroll
-      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-        const uint64_t a = umma::smem_desc(sS0 + kk * 256, 256, false);
-        umma::mma<umma::kBF16>(tm + kT_X, a, umma::smem_desc(sKG + kk * 2048, 128, true), id_xz, kk > 0);
-        umma::mma<umma::kBF16>(tm + kT_Z, a, umma::smem_desc(sKQ + 1024 + kk * 4096, 256, true), id_xz, kk > 0);
-      }
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        umma::mma<umma::kBF16>(tm + kT_X, umma::smem_desc(sS0 + kk * 256, 256, false),
+                               umma::smem_desc(sKQ + kk * 4096, 256, true), id_xz, kk > 0);
       umma::commit(&bars[1]);
     }
 
@@ -740,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         }
       }
     } else {
-      // ---- Y = V^T - X (tf32, rows dv), over S0's space once X, Z are done;
+      // ---- Y = V^T - X (tf32, rows dv), X = (S0 K^T) diag(e^g / |k|), over S0's space once X, Z are done;
       // warps 8-11 take columns 0-31, warps 12-15 columns 32-63
       part_ok = mbar_wait_bounded(&bars[1], par);
       umma::fence_after_sync();
@@ -756,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int t = c0 + q4 * 4 + e;
-            y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * ikv[t]);
+            y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * (egv[t] * ikv[t]));  // X = (S0 K^T) e^g / |k|
           }
           *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (c0 + q4 * 4) * 4, 256)) =
               make_float4(y4[0], y4[1], y4[2], y4[3]);
