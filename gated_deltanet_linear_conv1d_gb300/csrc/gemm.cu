@@ -58,9 +58,9 @@ namespace {
 constexpr int kBM = 128;  // MMA M: tokens, or weight rows when swapped
 constexpr int kBN = 256;  // MMA N at most: weight rows, or tokens when swapped
 constexpr int kBK = 64;   // K elements per stage: one 128-byte swizzled row of bf16
-constexpr int kStages = 4;
-constexpr int kTileA = kBM * 128;  // 16 KB
-constexpr int kTileB = kBN * 128;  // 32 KB
+constexpr int kStages = 6;
+constexpr int kTileA = kBM * 128;        // 16 KB: this CTA's 128 A rows
+constexpr int kTileB = (kBN / 2) * 128;  // 16 KB: this CTA's half of the B rows
 constexpr int kStageBytes = kTileA + kTileB;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
@@ -73,10 +73,6 @@ constexpr int kMaxSplit = 4;
 // not swapped 128 tokens x 256 outputs, swapped up to 256 tokens x 128 outputs.
 constexpr int kPadNormal = kBN + 4, kPadSwap = kBM + 4;
 static_assert(kBM * kPadNormal * 4 <= kBarOff && kBN * kPadSwap * 4 <= kBarOff, "partial tile overruns the ring");
-
-__device__ __forceinline__ void arrive_one(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -110,22 +106,48 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* tma
       : "memory");
 }
 
-// TMA tile load delivered to the same shared-memory offset (and its mbarrier)
-// in every CTA of `mask` within the cluster, with an L2 eviction-priority policy.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const void* tmap, int x, int y, uint64_t* bar,
-                                               uint16_t mask, uint64_t policy) {
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// `bar_cluster`, a barrier of the pair (a shared::cluster address, here the even
+// CTA's), with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int x, int y, uint32_t bar_cluster,
+                                                 uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
       : "memory");
 }
 
-// Arrives once on `bar` in every CTA of `mask` when this thread's MMAs so far have completed.
-__device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+// shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+
+// One arrival on a barrier given by its shared::cluster address (possibly another CTA's).
+__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// Arrives once on `bar` in both CTAs of the pair (`mask`) when the pair's MMAs
+// issued so far by this thread have completed.
+__device__ __forceinline__ void commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
                    "r"(smem_u32(bar)), "h"(mask)
                : "memory");
+}
+
+// One MMA of the pair: D (this CTA's and the partner's tensor memory at the same
+// address, 128 rows each) (+)= A (128 rows from each CTA's shared memory at the
+// descriptor's address) B^T (N/2 rows from each); issued by the even CTA.
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Output segment and tile of a tile index: tiles run m-tile major, then over
@@ -254,17 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // this CTA's MMAs and the pair partner's
+      mbar_init(&full[s], 1);   // even CTA: its producer's arrival + both CTAs' bytes
+      mbar_init(&empty[s], 1);  // the pair's MMA completion (multicast to both CTAs)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kEpiWarps);
+      mbar_init(&tempty[b], 2 * kEpiWarps);  // even CTA: both CTAs' epilogue warps
     }
     flags[0] = 0;
     fence_mbar_init();
   }
-  if (warp == 1) umma::tmem_alloc(tmem_slot, 2 * kBN);
+  if (warp == 1) {  // one allocation for the pair: a warp of each CTA takes part
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(2 * kBN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
   umma::fence_before_sync();
   __syncthreads();
   cluster_sync_all();  // every CTA's barriers are initialised before the partner copies or arrives on them
@@ -272,16 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   const uint32_t tm = *tmem_slot;
   volatile int* abort_flag = flags;
   const uint32_t b_rows = p.swap ? (uint32_t)p.nt_tok : (uint32_t)kBN;
-  const uint32_t stage_tx = (uint32_t)kTileA + b_rows * 128u;  // own A tile + both halves of B
+  const uint32_t stage_tx = 2u * ((uint32_t)kTileA + (b_rows / 2) * 128u);  // both CTAs' A tile and B half
 
   // ---- cluster layout: rank = pair member pr + 2 x K part rs. The cluster
-  // takes pair tiles first, first + stride, ...; of each, this CTA computes
-  // the A tile of its pair member over K slices kb_lo .. kb_hi-1 and copies
-  // half pr of the shared B tile into both members' shared memory.
+  // takes pair tiles first, first + stride, ...; of each, this CTA loads the A
+  // tile of its pair member and half pr of the shared B tile over K slices
+  // kb_lo .. kb_hi-1, and the pair's even CTA issues M = 256 MMAs over both.
   const int split = p.split;
   const int crank = (int)cluster_ctarank();
   const int pr = crank & 1, rs = crank >> 1;
   const uint16_t pair_mask = (uint16_t)(3u << (2 * rs));
+  const uint32_t lead = (uint32_t)(2 * rs);  // the pair's even CTA: it issues the MMAs
   const int csize = 2 * split;
   const int first = (int)blockIdx.x / csize;
   const int stride = split > 1 ? p.pairs : (int)gridDim.x / 2;  // split: one pair tile per cluster
@@ -294,7 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       valid = w < p.tiles_per_m;
       return tile_ref(p, valid ? w : p.tiles_per_m - 1);
     }
-    const int mp = u / p.tiles_per_m, n_idx = u - mp * p.tiles_per_m;
+    // bands of group_n weight tiles, each walked down all token-tile pairs, so a
+    // band's weights stay in L2 while every token tile passes them
+    const int mpairs = (p.mt + 1) / 2;
+    const int band = u / (mpairs * p.group_n), in_band = u - band * (mpairs * p.group_n);
+    const int width = min(p.group_n, p.tiles_per_m - band * p.group_n);
+    const int mp = in_band / width, n_idx = band * p.group_n + in_band % width;
     TileRef r = tile_ref(p, n_idx);
     r.m_t = 2 * mp + pr;
     valid = r.m_t < p.mt;
@@ -325,29 +358,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           }
           if (*abort_flag) { ok = false; break; }
           unsigned char* st = smem + s * kStageBytes;
-          unsigned char* bh = st + kTileA + pr * b_half_rows * 128;
-          mbar_arrive_expect_tx(&full[s], stage_tx);
+          const uint32_t fb = cluster_addr(&full[s], lead);  // both CTAs' copies count on the even CTA's barrier
+          if (pr == 0) mbar_arrive_expect_tx(&full[s], stage_tx);
           if (p.swap) {
-            tma_load_2d_hint(st, mw, kb * kBK, tr.n_t * kBM, &full[s], stream_pol);
-            tma_load_2d_mc(bh, &tmx, kb * kBK, pr * (int)b_half_rows, &full[s], pair_mask, keep);
+            tma_load_2d_pair(st, mw, kb * kBK, tr.n_t * kBM, fb, stream_pol);
+            tma_load_2d_pair(st + kTileA, &tmx, kb * kBK, pr * (int)b_half_rows, fb, keep);
           } else {
-            tma_load_2d_hint(st, &tmx, kb * kBK, tr.m_t * kBM, &full[s], a_pol);
-            tma_load_2d_mc(bh, mw, kb * kBK, tr.n_t * kBN + pr * (int)b_half_rows, &full[s], pair_mask, keep);
+            tma_load_2d_pair(st, &tmx, kb * kBK, tr.m_t * kBM, fb, a_pol);
+            tma_load_2d_pair(st + kTileA, mw, kb * kBK, tr.n_t * kBN + pr * (int)b_half_rows, fb, keep);
           }
         }
       }
       if (!ok) {
         report(p.dev_err, GDN_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        // copies still in flight land before the CTA goes on (bounded waits)
-        for (uint32_t j = (gk > (uint32_t)kStages ? gk - kStages : 0); j < gk; ++j)
-          mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
+        // copies still in flight land before the CTA goes on (bounded waits; the
+        // even CTA holds the barriers that count them)
+        if (pr == 0)
+          for (uint32_t j = (gk > (uint32_t)kStages ? gk - kStages : 0); j < gk; ++j)
+            mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: one accumulator per tile, alternating between the two
-    if (lane == 0) {
-      const uint32_t idesc = umma::idesc(umma::kBF16, false, false, kBM, p.swap ? p.nt_tok : kBN);
+    // ---- MMA issuer (the pair's even CTA): one accumulator per tile,
+    // alternating between the two; M = 256 over the pair
+    if (lane == 0 && pr == 0) {
+      const uint32_t idesc = umma::idesc(umma::kBF16, false, false, 2 * kBM, p.swap ? p.nt_tok : kBN);
       uint32_t gk = 0, piece = 0;
       bool ok = true;
       for (int u = first; ok && u < p.pairs; u += stride) {
@@ -367,12 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kTileA;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma::mma<umma::kKindF16>(tm + b * kBN, umma::smem_desc_sw128(sa + kk * 32),
-                                      umma::smem_desc_sw128(sb + kk * 32), idesc, (kb > kb_lo || kk > 0) ? 1u : 0u);
-          commit_mc(&empty[s], pair_mask);  // the stage is free in both members once both have arrived
+            mma_pair(tm + b * kBN, umma::smem_desc_sw128(sa + kk * 32), umma::smem_desc_sw128(sb + kk * 32), idesc,
+                     (kb > kb_lo || kk > 0) ? 1u : 0u);
+          commit_pair(&empty[s], pair_mask);  // the stage may be refilled in both CTAs
         }
         if (!ok) break;
-        umma::commit(&tfull[b]);
+        commit_pair(&tfull[b], pair_mask);  // both CTAs' epilogues may read their halves
         ++piece;
       }
       if (!ok) {
@@ -419,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       }
       umma::fence_before_sync();
       __syncwarp();
-      if (lane == 0) arrive_one(&tempty[b]);  // the accumulator may be refilled
+      if (lane == 0) arrive_cluster(cluster_addr(&tempty[b], lead));  // the even CTA may refill the accumulator
     }
   }
 
@@ -492,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   // barriers, or a peer may still read its partial tile
   cluster_sync_all();
   umma::fence_after_sync();
-  if (warp == 1) umma::tmem_dealloc(tm, 2 * kBN);
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(2 * kBN) : "memory");
 }
 
 // bf16 [rows][cols] tensor map, box 64 columns x box_rows rows, 128-byte swizzle.
@@ -577,6 +614,10 @@ cudaError_t launch_gemm(const GemmOperands& o, int32_t* dev_err, cudaStream_t st
     }
   }
   a.dev_err = dev_err;
+  // band width: about 24 MB of weights (256 rows x K bf16 per weight tile)
+  a.group_n = (int)((24ll << 20) / ((long long)kBN * o.K * 2));
+  if (a.group_n < 1) a.group_n = 1;
+  if (a.group_n > a.tiles_per_m) a.group_n = a.tiles_per_m;
   const long long pairs = a.swap ? (a.tiles_per_m + 1) / 2 : (long long)((a.mt + 1) / 2) * a.tiles_per_m;
   if (pairs >= (1LL << 30)) return cudaErrorInvalidValue;
   a.pairs = (int)pairs;

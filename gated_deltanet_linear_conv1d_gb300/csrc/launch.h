@@ -192,6 +192,7 @@ struct GemmArgs {
   int mt;           // m-tiles (1 when swapped)
   int tiles_per_m;  // sum of the outputs' n-tiles
   int pairs;        // pair tiles: two A tiles sharing one B tile
+  int group_n;      // not swapped: weight tiles per band of the tile order
   int split;        // pairs per cluster, each one split-th of K; 1: clusters of one pair, persistent
   int32_t* dev_err;
 };
