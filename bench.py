@@ -350,7 +350,7 @@ SWEEP_REQUESTS = (1, 8, 64, 256, 1024)
 SWEEP_POOL_BYTES = 512 << 20  # >= 4x L2: a slot's state is evicted before the step that uses it again
 
 
-def measure_decode_sweep(b, dev, stream, peak: float) -> dict:
+def measure_decode_sweep(b, dev, stream, peak: float, max_reps: int = 200) -> dict:
     """Decode batch sweep: R in {1, 8, 64, 256, 1024} requests x 1 token at 16/48 and at the
     per-rank 4/12 head layout (the TP4 shard run on one GPU). The pool holds 2R slots or enough
     slots for 512 MiB of state, whichever is more, cut into disjoint sets of R slots that the
@@ -393,7 +393,7 @@ def measure_decode_sweep(b, dev, stream, peak: float) -> dict:
                 for i in range(per_graph):
                     launch(i)
             probe = timed(graph.replay, 2, 2, stream) / per_graph
-            reps = int(min(200, max(3, 80.0 / max(probe * per_graph, 1e-3))))
+            reps = int(min(max_reps, max(3, 80.0 / max(probe * per_graph, 1e-3))))
             ms = timed(graph.replay, reps, 2, stream) / per_graph
             if b.gdn_read_device_error(err) != 0:
                 raise RuntimeError(f"device error flagged in the decode sweep ({name}, R={R})")
@@ -910,7 +910,8 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     extra = {}
     if not args.decode_only:
-        extra["decode_sweep"] = measure_decode_sweep(b, dev, stream, peak)
+        # graph replays per point: up to 200 for a full run, fewer for a short one
+        extra["decode_sweep"] = measure_decode_sweep(b, dev, stream, peak, max_reps=max(3, min(200, args.steps // 5)))
         torch.cuda.empty_cache()
         extra["prefill"] = measure_prefill(b, dev, stream)
         torch.cuda.empty_cache()
