@@ -445,6 +445,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     const float* glv = gv + 128;
     const float* bv = gv + 192;
 
+    // ---- S0 as a bf16 operand (A of the [X' | Z] MMA), and S *= e^{g_C} in
+    // tensor memory for this chunk's update; first thing in the chunk, so it
+    // overlaps the wait for the raw q, k rows (the previous chunk's MMAs on S
+    // and on the shared-memory tiles have completed)
+    {
+      const float decay = egv[L - 1];
+      float v[32];
+      const uint32_t col = kTS_S + part * 32;
+      umma::ld32(tm + lane_base + col, v);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint4 pk;
+        pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
+        pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
+        pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
+        pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
+        const int dk = part * 32 + q8 * 8;
+        *reinterpret_cast<uint4*>(S0b + umma::tile_off(row, dk * 2, 256)) = pk;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= decay;
+      umma::st32(tm + lane_base + col, v);
+    }
     // ---- conv + SiLU of q and k from the TMA-staged raw rows, written
     // channel-major to shared memory (v was done during the previous chunk).
     // Every token row of the staging area is valid to read (rows past T arrive
@@ -511,30 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         umma::mma<umma::kBF16>(tm + kT_D1, a, a, id_kk, kk > 0);
       }
       umma::commit(&bars[0]);
-    }
-    // ---- S0 as a bf16 operand; S *= e^{g_C} in tensor memory for the update below
-    {
-      const float decay = egv[L - 1];
-      float v[32];
-      const uint32_t col = kTS_S + part * 32;
-      umma::ld32(tm + lane_base + col, v);
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        uint4 pk;
-        pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
-        pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
-        pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
-        pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
-        const int dk = part * 32 + q8 * 8;
-        *reinterpret_cast<uint4*>(S0b + umma::tile_off(row, dk * 2, 256)) = pk;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= decay;
-      umma::st32(tm + lane_base + col, v);
-    }
-    sync_for_mma();
-    // ---- X' = S0 K^T and Z = S0 Q^T in one MMA over [K; Q] (bf16)
-    if (tid == 0) {
+    } else if (tid == 32) {
+      // ---- X' = S0 K^T and Z = S0 Q^T in one MMA over [K; Q] (bf16; S0 was
+      // written at the start of the chunk), issued from another warp so that the
+      // Gram product's issue does not wait behind it
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
         umma::mma<umma::kBF16>(tm + kT_X, umma::smem_desc(sS0 + kk * 256, 256, false),
@@ -601,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       // ---- T = (I + A)^-1 by recursive doubling over 16-row blocks (T row-major
       // in TS, rows of kLd floats), with T diag(beta) written as the tf32 K-major
       // operand as each block is finished:
-      //   diagonal blocks T_aa by forward substitution (one column per thread);
+      //   diagonal blocks T_aa by forward substitution (one column per thread,
+      //   the rows of A in 16-byte loads, two partial sums per row);
       //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
       //   then the lower-left 32x32 block = -T_hi (A_lo-left T_lo), T_hi and T_lo
       //   being the two 32x32 diagonal blocks.
@@ -610,14 +614,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       // the left operand come in 16-byte loads.
       if (tid < kC) {
         const int a = tid >> 4, cc = tid & 15;
-        const float* Ab = AM + (16 * a) * kLd + 16 * a;
+        const float* Ab = AM + (16 * a) * kLd + 16 * a;  // 16-byte aligned rows
         float x[16];
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float s = 0.f;
-  #pragma unroll
-          for (int i = 0; i < r; ++i) s = fmaf(Ab[r * kLd + i], x[i], s);
-          x[r] = r < cc ? 0.f : (r == cc ? 1.f : -s);
+          // row r of A in 16-byte loads, two partial sums (half the dependent chain)
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            if (4 * i4 >= r) break;
+            const float4 a4 = *reinterpret_cast<const float4*>(Ab + r * kLd + 4 * i4);
+            if (4 * i4 + 0 < r) s0 = fmaf(a4.x, x[4 * i4 + 0], s0);
+            if (4 * i4 + 1 < r) s1 = fmaf(a4.y, x[4 * i4 + 1], s1);
+            if (4 * i4 + 2 < r) s0 = fmaf(a4.z, x[4 * i4 + 2], s0);
+            if (4 * i4 + 3 < r) s1 = fmaf(a4.w, x[4 * i4 + 3], s1);
+          }
+          x[r] = r < cc ? 0.f : (r == cc ? 1.f : -(s0 + s1));
         }
         const int col = 16 * a + cc;
         const float bc = bv[col];
