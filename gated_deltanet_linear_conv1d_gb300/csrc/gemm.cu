@@ -96,16 +96,6 @@ __device__ __forceinline__ float4 ld_cluster_v4(const float* local, uint32_t ran
   return v;
 }
 
-// TMA tile load with an L2 eviction-priority policy.
-__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* tmap, int x, int y, uint64_t* bar,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // `bar_cluster`, a barrier of the pair (a shared::cluster address, here the even
 // CTA's), with an L2 eviction-priority policy.
