@@ -117,15 +117,15 @@ TF32_PER_BF16 = 1.1 / 2.25
 def prefill_flops(geom, lengths) -> tuple[float, float]:
     """Tensor-core FLOPs (bf16, tf32) of the chunked prefill for these request lengths.
 
-    Per 64-token chunk and value head: S0 Kg^T and S0 Q^T (bf16, 2 x 2*128*64*128),
-    E^T P^T (bf16, 2*128*64*64), E^T = Y Tb^T (tf32, 2*128*64*64), the state update
+    Per 64-token chunk and value head: S0 K^T and S0 Q^T (bf16, 2 x 2*128*64*128),
+    E^T = Y Tb^T (tf32, 2*128*64*64), E^T P^T (tf32, 2*128*64*64), the state update
     (tf32, 2*128*128*64); per key head [K;Q] K^T (bf16, 2*128*64*128). A partial last
     chunk is computed as a full one.
     """
     chunks = sum((int(L) + 63) // 64 for L in lengths)
     hv, hk = geom.num_v_heads, geom.num_k_heads
-    bf16 = chunks * (hv * (2 * 2 * 128 * 64 * 128 + 2 * 128 * 64 * 64) + hk * 2 * 128 * 64 * 128)
-    tf32 = chunks * hv * (2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
+    bf16 = chunks * (hv * 2 * 2 * 128 * 64 * 128 + hk * 2 * 128 * 64 * 128)
+    tf32 = chunks * hv * (2 * 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
     return float(bf16), float(tf32)
 
 

@@ -22,20 +22,25 @@
 // of the 152 SMs idle at this kernel's footprint). The fp32 state lives in tensor memory (128 lanes x 128 columns) for
 // the whole request. The raw QKV0 rows and the z rows of the next chunk are
 // fetched by TMA while the current chunk runs. Per chunk:
+//   S0 -> packed bf16 pairs in tensor memory, S *= e^{g_C} in tensor memory
 //   conv + SiLU (CUDA cores, thread = channel x token range) -> raw q, k (bf16,
-//       channel-major), k (tf32, channel-major), v (fp32), |q|, |k|
-//   [K;Q] K^T                 tcgen05 bf16  M=128 N=64  K=128  (operands MN-major)
-//   S0 -> bf16 operand, S *= e^{g_C} in tensor memory
-//   [X' | Z] = S0 [K;Q]^T      tcgen05 bf16  M=128 N=128 K=128 (X = X' diag(e^g) at read-out)
+//       channel-major), k (fp32, channel-major), |q|, |k|
+//   [K;Q] K^T                 tcgen05 bf16  M=128 N=128 K=128 (operands MN-major)
+//   [X' | Z] = S0 [K;Q]^T      tcgen05 bf16  M=128 N=128 K=128 (A = S0 from tensor
+//       memory; X = X' diag(e^g) at read-out)
 //   A, P from K K^T, Q K^T;  T = (I + A)^-1 on CUDA cores (recursive doubling
 //       over 16-row blocks), written as Tb = T diag(b) in tf32
-//   Y = V^T - X  -> tf32;  E^T = Y Tb^T   tcgen05 tf32 M=128 N=64 K=64
-//   S += (E^T diag(Gamma_C / |k|)) K     tcgen05 tf32 M=128 N=128 K=64 (accumulate)
-//   O' = E^T P^T                tcgen05 bf16 M=128 N=64 K=64
-//   o = e^g Z / |q| + O',  gated RMSNorm, bf16 out.
+//   Y = V^T - X -> tf32 in tensor memory;  E^T = Y Tb^T   tcgen05 tf32 M=128 N=64 K=64
+//   K' = diag(Gamma_C / |k|) K in tf32 (shared memory, in place)
+//   S += E^T K'                 tcgen05 tf32 M=128 N=128 K=64 (accumulate; A = E^T
+//       straight from tensor memory)
+//   O' = E^T P^T                tcgen05 tf32 M=128 N=64 K=64 (A = E^T from tensor memory)
+//   o = e^g Z / |q| + O' -> token-major in shared memory, then the gated
+//       RMSNorm with eight threads per token, bf16 out.
 // The two products that feed the carried state (E and the state update) take
-// tf32 operands; the others take bf16 (measured against the fp64 oracle:
-// state error ~6e-4, output error ~3e-3 relative L2).
+// tf32 operands, and so does O'; the Gram product and [X' | Z] take bf16
+// (measured against the fp64 oracle: state error ~6e-4, output error ~3e-3
+// relative L2).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -58,13 +63,12 @@ constexpr float kInvSqrtDk = 0.08838834764831845f;
 
 // Shared-memory regions (byte offsets, 1024-aligned).
 constexpr int kKQ = 0;                  // bf16 [128 dk][128 t]: k tokens 0-63, q tokens 64-127 (MN-major)
-constexpr int kKG = kKQ + 32768;        // bf16 [128 dv][64 t]: E (K-major A of O' = E^T P^T)
-constexpr int kKT = kKG + 16384;        // tf32 [128 dk][64 t]: raw k (K-major B)
-constexpr int kS0 = kKT + 32768;        // bf16 [128 dv][128 dk]: S0 (K-major A)       | later Y, E' tf32 [128][64]
+constexpr int kKT = kKQ + 32768;        // fp32 [128 dk][64 t]: raw k, then k diag(Gamma_C / |k|) as tf32 (K-major B)
+constexpr int kOT = kKT + 32768;        // fp32 [64 t][128 dv]: o of the chunk, token-major (the gate's input)
 // Scratch: raw q and k rows of a chunk [2 parts][64 t][128] bf16 (TMA, read by
 // the conv), later the inverse's A [64][68], T [64][68] and block products
 // [32][36]; then the q and k rows of the next chunk.
-constexpr int kSCR = kS0 + 32768;
+constexpr int kSCR = kOT + 32768;
 constexpr int kScrBytes = 40960;
 constexpr int kXS = kSCR;               // raw q, k rows, 32768 B
 constexpr int kLd = 68;                 // row stride (floats) of A and T: 16-byte aligned rows
@@ -77,51 +81,21 @@ static_assert(2 * kC * kHeadDim * 2 <= kScrBytes, "q, k rows overrun the scratch
 constexpr int kXV = kSCR + kScrBytes;   // bf16 [64 t][128]: raw v rows of the next chunk (TMA)
 constexpr int kZS = kXV + 16384;        // bf16 [64][128]: z rows, then Ogate rows
 constexpr int kTB = kZS + 16384;        // tf32 [64 r][64 i]: T diag(b) (K-major B)
-constexpr int kPB = kTB + 16384;        // bf16 [64 r][64 i]: P (K-major B)
-constexpr int kSmall = kPB + 8192;      // small per-chunk vectors
-constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 2 + 4 * 64;
+constexpr int kPB = kTB + 16384;        // tf32 [64 r][64 i]: P (K-major B)
+constexpr int kSmall = kPB + 16384;     // small per-chunk vectors
+constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 2;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
 
-// Tensor-memory columns (v, fp32 channel-major, lives in the last 64).
-// D1 = [K;Q][K;Q]^T takes 128 columns; E reuses its first 64 once A, P and the
-// norms have been read out of it.
-constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_E = 128, kT_X = 256, kT_Z = 320, kT_O = 384, kT_V = 448,
-                   kTmemCols = 512;
+// Tensor-memory columns. D1 = [K;Q][K;Q]^T takes 128 columns; E reuses its
+// first 64 once A, P and the norms have been read out of it. X' (then Y in
+// place) and Z share 128. S0 as packed bf16 pairs (the A operand of [X' | Z])
+// sits in O''s 64 columns until O' is written. v (fp32, channel-major) lives
+// in the last 64.
+constexpr uint32_t kTS_S = 0, kT_D1 = 128, kT_E = 128, kT_X = 256, kT_Z = 320, kT_O = 384, kT_S0 = 384,
+                   kT_V = 448, kTmemCols = 512;
 
 __device__ __forceinline__ float to_tf32(float x) { return umma::to_tf32(x); }
-
-// Sums v[0..7] over the 32 lanes of a warp, 8 values at once (9 shuffles).
-// Returns the total of value index tok8(lane) in every lane.
-__device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
-  {
-    const bool hi = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float send = hi ? v[i] : v[i + 4], keep = hi ? v[i + 4] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-  }
-  {
-    const bool hi = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-  }
-  {
-    const bool hi = lane & 4;
-    const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
-    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-  return v[0];
-}
-__device__ __forceinline__ int tok8(int lane) {
-  return ((lane >> 2) & 1) | (((lane >> 3) & 1) << 1) | (((lane >> 4) & 1) << 2);
-}
 
 // 2^x via the hardware approximation (ex2.approx); its error is far below the
 // bf16 / tf32 rounding that every use of it is followed by.
@@ -202,14 +176,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const bool init = p.has_init ? p.has_init[n] != 0 : true;
 
   uint16_t* KQ = reinterpret_cast<uint16_t*>(smem + kKQ);
-  unsigned char* KGb = smem + kKG;
   unsigned char* KTb = smem + kKT;
   const uint16_t* XS = reinterpret_cast<const uint16_t*>(smem + kXS);
   uint16_t* const ZS = reinterpret_cast<uint16_t*>(smem + kZS);
   const uint16_t* XV = reinterpret_cast<const uint16_t*>(smem + kXV);
-  unsigned char* S0b = smem + kS0;
+  float* OT = reinterpret_cast<float*>(smem + kOT);
   float* AM = reinterpret_cast<float*>(smem + kAM);
   float* TS = reinterpret_cast<float*>(smem + kTS);
+  // the four 16 x 16 diagonal blocks of A, transposed (block a: [16 i][16 r]),
+  // for the forward substitution; in OT, which is free until the chunk's o
+  float* ATD = OT;
   unsigned char* TBb = smem + kTB;
   unsigned char* PBb = smem + kPB;
   float* small = reinterpret_cast<float*>(smem + kSmall);
@@ -219,7 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* gates = small;          // [2][4][64]
   float* iqv = gates + 2 * 4 * 64;  // [64] 1/|q|
   float* ikv = iqv + 64;         // [64] 1/|k|
-  float* rpart = ikv + 64;       // [4][64] gate partials
   float* MS = reinterpret_cast<float*>(smem + kMS);
   // MMA completions 0: [K;Q][K;Q]^T  1: X,Z  2: E  3: S, O';  copies 4: raw q, k rows
   // 5: z rows  6: raw v rows
@@ -246,25 +221,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   };
 
   // ---- conv work of this thread. q and k at the start of every chunk: thread t
-  // takes channel t % 256 (q below 128, k above) for tokens 32 (t / 256) .. + 31.
-  // v one chunk early, during the previous chunk's triangular inverse: warps
-  // 8-15, channel d = row (its tensor-memory lane), tokens 32 (part - 2) .. + 31.
+  // takes the adjacent channels 2 (t % 128), + 1 of the key head's 256 q and k
+  // channels (q below 128, k above) for tokens 16 (t / 128) .. + 15, the pair
+  // computed together in packed fp32x2 arithmetic. v one chunk early, during the
+  // previous chunk's triangular inverse: warps 8-15, channel d = row (its
+  // tensor-memory lane), tokens 32 (part - 2) .. + 31.
   const int d = row;
-  const int qch = tid & 255, dq = qch & 127, qhalf = tid >> 8;
-  const bool isq = qch < 128;
+  const int qp = tid & 127, qq = tid >> 7;
+  const bool isq = qp < 64;
+  const int dq = (2 * qp) & 127;  // the pair's first channel within its q or k head
   const int gqk = isq ? j * kHeadDim + dq : (p.Hk + j) * kHeadDim + dq;
-  const float4 wqk = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gqk * kTaps);
+  float2 wqk[kTaps];  // tap i of the pair's two channels
+  {
+    const float4 wa = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gqk * kTaps);
+    const float4 wb = *reinterpret_cast<const float4*>(p.conv_w + (size_t)(gqk + 1) * kTaps);
+    wqk[0] = make_float2(wa.x, wb.x); wqk[1] = make_float2(wa.y, wb.y);
+    wqk[2] = make_float2(wa.z, wb.z); wqk[3] = make_float2(wa.w, wb.w);
+  }
   const int gvc = (2 * p.Hk + h) * kHeadDim + d;
   const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (size_t)gvc * kTaps);
-  const bool own_qk = qhalf == 0;  // carries channel qch's running q/k window
+  const bool own_qk = qq == 0;    // carries the pair's running q/k window
   const bool own_v = part == 2;    // carries channel d's running v window
-  // running windows (raw inputs, oldest first); hv_end is the v window at the end
-  // of the current chunk once hv has moved on to the next one
-  uint16_t hqk[3] = {0, 0, 0}, hv[3] = {0, 0, 0}, hv_end[3] = {0, 0, 0};
+  // running windows (raw inputs, oldest first; the q/k window as bf16 pairs, the
+  // pair's first channel in the low half); hv_end is the v window at the end of
+  // the current chunk once hv has moved on to the next one
+  uint32_t hqk[3] = {0, 0, 0};
+  uint16_t hv[3] = {0, 0, 0}, hv_end[3] = {0, 0, 0};
   if (init) {
     if (own_qk) {
       const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gqk) * 3;
-      hqk[0] = hp[0]; hqk[1] = hp[1]; hqk[2] = hp[2];
+      hqk[0] = hp[0] | ((uint32_t)hp[3] << 16);
+      hqk[1] = hp[1] | ((uint32_t)hp[4] << 16);
+      hqk[2] = hp[2] | ((uint32_t)hp[5] << 16);
     }
     if (own_v) {
       const uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gvc) * 3;
@@ -316,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const uint32_t id_xz = umma::idesc(umma::kBF16, false, true, 128, 128);  // [X' | Z] = S0 [K; Q]^T
   const uint32_t id_e = umma::idesc(umma::kTF32, false, false, 128, 64);
   const uint32_t id_s = umma::idesc(umma::kTF32, false, false, 128, 128);
-  const uint32_t id_o = umma::idesc(umma::kBF16, false, false, 128, 64);
-  const uint32_t sKQ = smem_u32(KQ), sKG = smem_u32(KGb), sKT = smem_u32(KTb), sS0 = smem_u32(S0b);
+  const uint32_t id_o = umma::idesc(umma::kTF32, false, false, 128, 64);
+  const uint32_t sKQ = smem_u32(KQ), sKT = smem_u32(KTb);
   const uint32_t sTB = smem_u32(TBb), sPB = smem_u32(PBb);
 
   // chunks end on absolute multiples of 64 (p0 tokens precede this call), so
@@ -405,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (own_v) {
       w3[0] = bf16_to_f32(hv[0]); w3[1] = bf16_to_f32(hv[1]); w3[2] = bf16_to_f32(hv[2]);
     } else {
-      w3[0] = bf16_to_f32(xv[29 * kHeadDim]); w3[1] = bf16_to_f32(xv[30 * kHeadDim]);
-      w3[2] = bf16_to_f32(xv[31 * kHeadDim]);
+      w3[0] = bf16_to_f32(xv[(tb - 3) * kHeadDim]); w3[1] = bf16_to_f32(xv[(tb - 2) * kHeadDim]);
+      w3[2] = bf16_to_f32(xv[(tb - 1) * kHeadDim]);
     }
     float yv[32];
 #pragma unroll
@@ -417,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       pre = fmaf(wv.y, w3[2], pre);
       pre = fmaf(wv.z, w3[1], pre);
       pre = fmaf(wv.w, w3[0], pre);
-      yv[e] = t < len ? silu_tanh(pre) : 0.f;
+      const float y = silu_tanh(pre);
+      yv[e] = t < len ? y : 0.f;
       w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
     }
     umma::st32_nowait(tm + lane_base + kT_V + tb, yv);  // v row d = this thread's lane
@@ -445,27 +434,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     const float* glv = gv + 128;
     const float* bv = gv + 192;
 
-    // ---- S0 as a bf16 operand (A of the [X' | Z] MMA), and S *= e^{g_C} in
-    // tensor memory for this chunk's update; first thing in the chunk, so it
-    // overlaps the wait for the raw q, k rows (the previous chunk's MMAs on S
-    // and on the shared-memory tiles have completed)
+    // ---- S0 as packed bf16 pairs in tensor memory (the A operand of the
+    // [X' | Z] MMA), and S *= e^{g_C} in place for this chunk's update; first
+    // thing in the chunk, so it overlaps the wait for the raw q, k rows (the
+    // previous chunk's MMAs on S have completed and its o has been read)
     {
       const float decay = egv[L - 1];
-      float v[32];
+      float v[32], pk[16];
       const uint32_t col = kTS_S + part * 32;
       umma::ld32(tm + lane_base + col, v);
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        uint4 pk;
-        pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
-        pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
-        pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
-        pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
-        const int dk = part * 32 + q8 * 8;
-        *reinterpret_cast<uint4*>(S0b + umma::tile_off(row, dk * 2, 256)) = pk;
-      }
+      for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(v[2 * i], v[2 * i + 1]));
+      umma::st16_nowait(tm + lane_base + kT_S0 + part * 16, pk);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= decay;
+      for (int i = 0; i < 32; i += 2) {
+        const float2 d2 = __fmul2_rn(make_float2(v[i], v[i + 1]), make_float2(decay, decay));
+        v[i] = d2.x;
+        v[i + 1] = d2.y;
+      }
       umma::st32(tm + lane_base + col, v);
     }
     // ---- conv + SiLU of q and k from the TMA-staged raw rows, written
@@ -482,40 +468,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       if (c + 1 < nchunks) issue_v(tc + L);  // XV is free: the v rows of the next chunk
     }
     {
-      const uint16_t* xs = XS + (isq ? 0 : kC) * kHeadDim + dq;
-      uint16_t nw[3];
-      if (own_qk) next_window(xs, hqk, nw, L);
-      float w3[3];
+      // raw rows as bf16 pairs: word t * 64 holds the pair's two channels of token t
+      const uint32_t* xs = reinterpret_cast<const uint32_t*>(XS + (isq ? 0 : kC) * kHeadDim + dq);
+      auto unpack = [](uint32_t u) { return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)); };
+      uint32_t nw[3];
       if (own_qk) {
-        w3[0] = bf16_to_f32(hqk[0]); w3[1] = bf16_to_f32(hqk[1]); w3[2] = bf16_to_f32(hqk[2]);
-      } else {
-        w3[0] = bf16_to_f32(xs[29 * kHeadDim]); w3[1] = bf16_to_f32(xs[30 * kHeadDim]);
-        w3[2] = bf16_to_f32(xs[31 * kHeadDim]);
+        nw[0] = L >= 3 ? xs[(L - 3) * 64] : (L == 2 ? hqk[2] : hqk[1]);
+        nw[1] = L >= 2 ? xs[(L - 2) * 64] : hqk[2];
+        nw[2] = xs[(L - 1) * 64];
       }
+      float2 w3[3];
+      if (own_qk) {
+        w3[0] = unpack(hqk[0]); w3[1] = unpack(hqk[1]); w3[2] = unpack(hqk[2]);
+      } else {
+        const int t3 = 16 * qq - 3;
+        w3[0] = unpack(xs[t3 * 64]); w3[1] = unpack(xs[(t3 + 1) * 64]); w3[2] = unpack(xs[(t3 + 2) * 64]);
+      }
+      const float2 half2 = make_float2(0.5f, 0.5f);
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi) {
-        const int tb = 32 * qhalf + 8 * gi;
-        float ya[8];
+      for (int gi = 0; gi < 2; ++gi) {
+        const int tb = 16 * qq + 8 * gi;
+        float2 ya[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int t = tb + e;
-          const float x = bf16_to_f32(xs[t * kHeadDim]);
-          float pre = wqk.x * x;
-          pre = fmaf(wqk.y, w3[2], pre);
-          pre = fmaf(wqk.z, w3[1], pre);
-          pre = fmaf(wqk.w, w3[0], pre);
-          ya[e] = t < L ? silu_tanh(pre) : 0.f;
+          const float2 x = unpack(xs[t * 64]);
+          float2 pre = __fmul2_rn(wqk[0], x);
+          pre = __ffma2_rn(wqk[1], w3[2], pre);
+          pre = __ffma2_rn(wqk[2], w3[1], pre);
+          pre = __ffma2_rn(wqk[3], w3[0], pre);
+          // SiLU(x) = h + h tanh(h), h = x / 2
+          const float2 hh = __fmul2_rn(pre, half2);
+          float2 th;
+          asm("tanh.approx.f32 %0, %1;" : "=f"(th.x) : "f"(hh.x));
+          asm("tanh.approx.f32 %0, %1;" : "=f"(th.y) : "f"(hh.y));
+          const float2 y = __ffma2_rn(hh, th, hh);
+          ya[e] = t < L ? y : make_float2(0.f, 0.f);
           w3[0] = w3[1]; w3[1] = w3[2]; w3[2] = x;
         }
-        // raw q or k, bf16: row dq of KQ, tokens (q ? 64 : 0) + tb ..
-        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(KQ) + umma::tile_off(dq, ((isq ? kC : 0) + tb) * 2, 256)) =
-            make_uint4(pack_bf16(ya[0], ya[1]), pack_bf16(ya[2], ya[3]), pack_bf16(ya[4], ya[5]), pack_bf16(ya[6], ya[7]));
+        // raw q or k, bf16: rows dq, dq + 1 of KQ, tokens (q ? 64 : 0) + tb ..
+        unsigned char* kq = reinterpret_cast<unsigned char*>(KQ);
+        const int cb = ((isq ? kC : 0) + tb) * 2;
+        *reinterpret_cast<uint4*>(kq + umma::tile_off(dq, cb, 256)) =
+            make_uint4(pack_bf16(ya[0].x, ya[1].x), pack_bf16(ya[2].x, ya[3].x), pack_bf16(ya[4].x, ya[5].x),
+                       pack_bf16(ya[6].x, ya[7].x));
+        *reinterpret_cast<uint4*>(kq + umma::tile_off(dq + 1, cb, 256)) =
+            make_uint4(pack_bf16(ya[0].y, ya[1].y), pack_bf16(ya[2].y, ya[3].y), pack_bf16(ya[4].y, ya[5].y),
+                       pack_bf16(ya[6].y, ya[7].y));
         if (!isq) {
-          // raw k (tf32)
+          // raw k in fp32 (scaled and rounded to tf32 once the norms are known)
           *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4, 256)) =
-              make_float4(to_tf32(ya[0]), to_tf32(ya[1]), to_tf32(ya[2]), to_tf32(ya[3]));
+              make_float4(ya[0].x, ya[1].x, ya[2].x, ya[3].x);
           *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4 + 16, 256)) =
-              make_float4(to_tf32(ya[4]), to_tf32(ya[5]), to_tf32(ya[6]), to_tf32(ya[7]));
+              make_float4(ya[4].x, ya[5].x, ya[6].x, ya[7].x);
+          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq + 1, tb * 4, 256)) =
+              make_float4(ya[0].y, ya[1].y, ya[2].y, ya[3].y);
+          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq + 1, tb * 4 + 16, 256)) =
+              make_float4(ya[4].y, ya[5].y, ya[6].y, ya[7].y);
         }
       }
       if (own_qk) {
@@ -536,12 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       umma::commit(&bars[0]);
     } else if (tid == 32) {
       // ---- X' = S0 K^T and Z = S0 Q^T in one MMA over [K; Q] (bf16; S0 was
-      // written at the start of the chunk), issued from another warp so that the
-      // Gram product's issue does not wait behind it
+      // packed into tensor memory at the start of the chunk), issued from another
+      // warp so that the Gram product's issue does not wait behind it
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        umma::mma<umma::kBF16>(tm + kT_X, umma::smem_desc(sS0 + kk * 256, 256, false),
-                               umma::smem_desc(sKQ + kk * 4096, 256, true), id_xz, kk > 0);
+        umma::mma_ts<umma::kKindF16>(tm + kT_X, tm + kT_S0 + kk * 8, umma::smem_desc(sKQ + kk * 4096, 256, true),
+                                     id_xz, kk > 0);
       umma::commit(&bars[1]);
     }
 
@@ -559,22 +568,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       else iqv[row - 64] = inv;
     }
     __syncthreads();
-    // ---- A (for the inverse) and P from K K^T and Q K^T
-    {
+    // ---- A (for the inverse) and P from K K^T and Q K^T; the warps whose 32
+    // rows lie wholly above their 16 columns (strictly lower A, lower P) only
+    // write zeros
+    if ((quarter & 1) == 0 && part >= 2) {
+      const int r = row & 63;
+      if (row < 64) {
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4)
+          *reinterpret_cast<float4*>(AM + r * kLd + part * 16 + e4 * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4)
+          *reinterpret_cast<float4*>(PBb + umma::tile_off(r, (part * 16 + e4 * 4) * 4, 256)) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else {
       float v[16];
       umma::ld16(tm + lane_base + kT_D1 + part * 16, v);
       if (row < 64) {
         const int r = row;
-        const float br = bv[r], gr = gv[r], ikr = ikv[r];
+        const float gr = gv[r], bkr = bv[r] * ikv[r];
+        float a16[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-          float a4[4];
+        for (int e = 0; e < 16; ++e) {
+          const int i = part * 16 + e;
+          // masked entries take ex2(-inf) = 0: no select around the exponential
+          a16[e] = (bkr * ex2(i < r ? gr - gv[i] : -INFINITY)) * (v[e] * ikv[i]);
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = part * 16 + e4 * 4 + e;
-            a4[e] = i < r ? br * ex2(gr - gv[i]) * v[e4 * 4 + e] * ikr * ikv[i] : 0.f;
-          }
-          *reinterpret_cast<float4*>(AM + r * kLd + part * 16 + e4 * 4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        for (int e4 = 0; e4 < 4; ++e4)
+          *reinterpret_cast<float4*>(AM + r * kLd + part * 16 + e4 * 4) =
+              make_float4(a16[4 * e4], a16[4 * e4 + 1], a16[4 * e4 + 2], a16[4 * e4 + 3]);
+        if (part == (r >> 4)) {  // a diagonal block: also transposed (after the branch-free part)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ATD[part * 256 + e * 16 + (r & 15)] = a16[e];
         }
       } else {
         const int r = row - 64;
@@ -585,14 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int i = part * 16 + q8 * 8 + e;
-            pe[e] = i <= r ? ex2(gr - gv[i]) * v[q8 * 8 + e] * iqr * ikv[i] : 0.f;
+            pe[e] = to_tf32((iqr * ex2(i <= r ? gr - gv[i] : -INFINITY)) * (v[q8 * 8 + e] * ikv[i]));
           }
-          uint4 pk;
-          pk.x = pack_bf16(pe[0], pe[1]);
-          pk.y = pack_bf16(pe[2], pe[3]);
-          pk.z = pack_bf16(pe[4], pe[5]);
-          pk.w = pack_bf16(pe[6], pe[7]);
-          *reinterpret_cast<uint4*>(PBb + umma::tile_off(r, (part * 16 + q8 * 8) * 2, 128)) = pk;
+          // P as tf32 (the B operand of O' = E^T P^T, K-major over i)
+          const int i0 = part * 16 + q8 * 8;
+          *reinterpret_cast<float4*>(PBb + umma::tile_off(r, i0 * 4, 256)) = make_float4(pe[0], pe[1], pe[2], pe[3]);
+          *reinterpret_cast<float4*>(PBb + umma::tile_off(r, i0 * 4 + 16, 256)) =
+              make_float4(pe[4], pe[5], pe[6], pe[7]);
         }
       }
     }
@@ -613,30 +640,60 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       // the inner index (the partner lane's half is added with shuffles); rows of
       // the left operand come in 16-byte loads.
       if (tid < kC) {
-        const int a = tid >> 4, cc = tid & 15;
-        const float* Ab = AM + (16 * a) * kLd + 16 * a;  // 16-byte aligned rows
-        float x[16];
+        // 8 x 8 diagonal blocks of T by right-looking forward substitution: thread
+        // (block b8, column cc) solves for column cc of (I + A_b8)^-1; once x[i]
+        // is final, s[r] += A[r][i] x[i] for every r > i (one dependent FMA per
+        // step), column i of A_b8 read from the transposed 16-block in two
+        // 16-byte broadcast loads
+        const int b8 = tid >> 3, cc = tid & 7, o = 8 * (b8 & 1);
+        const float* ATc = ATD + (b8 >> 1) * 256 + o * 16 + o;  // ATc[i * 16 + r] = A[8 b8 + r][8 b8 + i]
+        float s8[8], x[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          // row r of A in 16-byte loads, two partial sums (half the dependent chain)
-          float s0 = 0.f, s1 = 0.f;
+        for (int r = 0; r < 8; ++r) s8[r] = 0.f;
 #pragma unroll
-          for (int i4 = 0; i4 < 4; ++i4) {
-            if (4 * i4 >= r) break;
-            const float4 a4 = *reinterpret_cast<const float4*>(Ab + r * kLd + 4 * i4);
-            if (4 * i4 + 0 < r) s0 = fmaf(a4.x, x[4 * i4 + 0], s0);
-            if (4 * i4 + 1 < r) s1 = fmaf(a4.y, x[4 * i4 + 1], s1);
-            if (4 * i4 + 2 < r) s0 = fmaf(a4.z, x[4 * i4 + 2], s0);
-            if (4 * i4 + 3 < r) s1 = fmaf(a4.w, x[4 * i4 + 3], s1);
+        for (int i = 0; i < 8; ++i) {
+          x[i] = i < cc ? 0.f : (i == cc ? 1.f : -s8[i]);
+          if (i < 7) {
+            const float4 lo = *reinterpret_cast<const float4*>(ATc + i * 16);
+            const float4 hi = *reinterpret_cast<const float4*>(ATc + i * 16 + 4);
+            const float ac[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+            for (int r = i + 1; r < 8; ++r) s8[r] = fmaf(ac[r], x[i], s8[r]);
           }
-          x[r] = r < cc ? 0.f : (r == cc ? 1.f : -(s0 + s1));
         }
-        const int col = 16 * a + cc;
+        const int col = 8 * b8 + cc;
         const float bc = bv[col];
-  #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          TS[(16 * a + r) * kLd + col] = x[r];
-          *reinterpret_cast<float*>(TBb + umma::tile_off(16 * a + r, col * 4, 256)) = to_tf32(x[r] * bc);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          TS[(8 * b8 + r) * kLd + col] = x[r];
+          *reinterpret_cast<float*>(TBb + umma::tile_off(8 * b8 + r, col * 4, 256)) = to_tf32(x[r] * bc);
+        }
+      }
+      inv_sync();
+      {  // 8 -> 16 in each 16-block a: T_10 = -T_11 (A_10 T_00); 256 threads = 4 blocks x 8 x 8
+        const int a = tid >> 6, r = (tid >> 3) & 7, c = tid & 7, R0 = 16 * a;
+        float* Mb = MS + a * 64;  // [8][8] A_10 T_00 of block a
+        {
+          // A_10 T_00: T_00 is zero above its diagonal, so all eight terms are taken
+          const float4 a0 = *reinterpret_cast<const float4*>(AM + (R0 + 8 + r) * kLd + R0);
+          const float4 a1 = *reinterpret_cast<const float4*>(AM + (R0 + 8 + r) * kLd + R0 + 4);
+          const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          float m = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m = fmaf(ar[i], TS[(R0 + i) * kLd + R0 + c], m);
+          Mb[r * 8 + c] = m;
+        }
+        inv_sync();
+        {
+          const float4 t0 = *reinterpret_cast<const float4*>(TS + (R0 + 8 + r) * kLd + R0 + 8);
+          const float4 t1 = *reinterpret_cast<const float4*>(TS + (R0 + 8 + r) * kLd + R0 + 12);
+          const float tr[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+          float t = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t = fmaf(tr[i], Mb[i * 8 + c], t);
+          TS[(R0 + 8 + r) * kLd + R0 + c] = -t;
+          *reinterpret_cast<float*>(TBb + umma::tile_off(R0 + 8 + r, (R0 + c) * 4, 256)) = to_tf32(-t * bv[R0 + c]);
+          TS[(R0 + r) * kLd + R0 + 8 + c] = 0.f;  // the 16-block's upper-right 8 x 8 is zero
         }
       }
       inv_sync();
@@ -758,23 +815,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         umma::ld16(tm + lane_base + kT_X + c0, v);
         umma::ld16(tm + lane_base + kT_V + c0, vv);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float y4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = c0 + q4 * 4 + e;
-            y4[e] = to_tf32(vv[q4 * 4 + e] - v[q4 * 4 + e] * (egv[t] * ikv[t]));  // X = (S0 K^T) e^g / |k|
-          }
-          *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (c0 + q4 * 4) * 4, 256)) =
-              make_float4(y4[0], y4[1], y4[2], y4[3]);
+        for (int e = 0; e < 16; ++e) {
+          const int t = c0 + e;
+          v[e] = to_tf32(vv[e] - v[e] * (egv[t] * ikv[t]));  // X = (S0 K^T) e^g / |k|
         }
+        // Y in place of X' (the A operand of E^T = Y Tb^T, read from tensor memory)
+        umma::st16_nowait(tm + lane_base + kT_X + c0, v);
       }
+      umma::wait_st();
       // the next chunk's gates while the inverse runs (published by the barrier below),
       // and the alpha, beta of the one after into the registers
       if (warp == kGateWarp && c + 1 < nchunks) {
         const int tn = tc + L, ln = min(kC, t1 - tn);
         make_gates(gates + ((c + 1) & 1) * 256, ln);
         if (c + 2 < nchunks) load_ab(tn + ln, min(kC, t1 - tn - ln));
+      }
+      // K' = diag(Gamma_C / |k|) K as tf32, in place (the B operand of the state
+      // update): thread (dk row, 32-token half), rows of 16-byte groups
+      {
+        const int u = tid - 256, r = u & 127, th = u >> 7;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int t = 32 * th + 4 * q;
+          float4* kp = reinterpret_cast<float4*>(KTb + umma::tile_off(r, t * 4, 256));
+          const float4 k4 = *kp;
+          const float4 g4 = *reinterpret_cast<const float4*>(glv + t);
+          const float4 n4 = *reinterpret_cast<const float4*>(ikv + t);
+          *kp = make_float4(to_tf32(k4.x * (g4.x * n4.x)), to_tf32(k4.y * (g4.y * n4.y)),
+                            to_tf32(k4.z * (g4.z * n4.z)), to_tf32(k4.w * (g4.w * n4.w)));
+        }
       }
       // the next chunk's v into tensor memory (this chunk's was read by Y above)
       if (c + 1 < nchunks) {
@@ -788,103 +857,86 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     umma::fence_after_sync();
     // the scratch area is free again (A and T consumed): raw rows of the next chunk
     if (tid == kTmaThread && c + 1 < nchunks) issue_x(tc + L);
-    // ---- E^T = Y Tb^T (tf32)
+    // ---- E^T = Y Tb^T (tf32, Y from tensor memory); once E is in tensor memory,
+    // S += E^T K' and O' = E^T P^T (tf32) with E^T read from there in turn (the
+    // tensor core reads the fp32 accumulator at tf32 precision, low bits dropped)
     if (tid == 0) {
 #pragma unroll
       for (int kk = 0; kk < kC / 8; ++kk)
-        umma::mma<umma::kTF32>(tm + kT_E, umma::smem_desc(sS0 + kk * 256, 256, false),
-                               umma::smem_desc(sTB + kk * 256, 256, false), id_e, kk > 0);
+        umma::mma_ts<umma::kKindTF32>(tm + kT_E, tm + kT_X + kk * 8, umma::smem_desc(sTB + kk * 256, 256, false),
+                                      id_e, kk > 0);
       umma::commit(&bars[2]);
-    }
-    if (!wait_mma(&bars[2], par)) { ok = false; break; }
-    // ---- E as bf16 (A of O' = E^T P^T) and E' = E diag(Gamma_C / |k|) as tf32 (A of the update)
-    {
-      float v[16];
-      umma::ld16(tm + lane_base + kT_E + part * 16, v);
+      if (mbar_wait_bounded(&bars[2], par)) {
+        umma::fence_after_sync();
 #pragma unroll
-      for (int q8 = 0; q8 < 2; ++q8) {
-        uint4 pk;
-        pk.x = pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]);
-        pk.y = pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]);
-        pk.z = pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]);
-        pk.w = pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(KGb + umma::tile_off(row, (part * 16 + q8 * 8) * 2, 128)) = pk;
+        for (int kk = 0; kk < kC / 8; ++kk)
+          umma::mma_ts<umma::kKindTF32>(tm + kTS_S, tm + kT_E + kk * 8, umma::smem_desc(sKT + kk * 256, 256, false),
+                                        id_s, 1);
+#pragma unroll
+        for (int kk = 0; kk < kC / 8; ++kk)
+          umma::mma_ts<umma::kKindTF32>(tm + kT_O, tm + kT_E + kk * 8, umma::smem_desc(sPB + kk * 256, 256, false),
+                                        id_o, kk > 0);
+        umma::commit(&bars[3]);
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float e4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = part * 16 + q4 * 4 + e;
-          e4[e] = to_tf32(v[q4 * 4 + e] * glv[t] * ikv[t]);
-        }
-        *reinterpret_cast<float4*>(S0b + umma::tile_off(row, (part * 16 + q4 * 4) * 4, 256)) =
-            make_float4(e4[0], e4[1], e4[2], e4[3]);
-      }
-    }
-    sync_for_mma();
-    // ---- S += E' K (tf32, accumulate) and O' = E^T P^T (bf16)
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < kC / 8; ++kk)
-        umma::mma<umma::kTF32>(tm + kTS_S, umma::smem_desc(sS0 + kk * 256, 256, false),
-                               umma::smem_desc(sKT + kk * 256, 256, false), id_s, 1);
-#pragma unroll
-      for (int kk = 0; kk < kC / 16; ++kk)
-        umma::mma<umma::kBF16>(tm + kT_O, umma::smem_desc(sKG + kk * 256, 128, false),
-                               umma::smem_desc(sPB + kk * 256, 128, false), id_o, kk > 0);
-      umma::commit(&bars[3]);
     }
     if (!wait_mma(&bars[3], par)) { ok = false; break; }
-    // ---- o = (e^g Z / |q| + O') / sqrt(dk), then the gated RMSNorm over dv
-    float ov[16];
+    // ---- o = (e^g Z / |q| + O') / sqrt(dk), written token-major to OT (thread:
+    // dv row `row`, tokens 16 part ..; a warp writes 32 consecutive floats)
     {
-      float z[16];
+      float z[16], ov[16];
       umma::ld16(tm + lane_base + kT_Z + part * 16, z);
       umma::ld16(tm + lane_base + kT_O + part * 16, ov);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = part * 16 + e;
-        ov[e] = fmaf(egv[t] * iqv[t], z[e], ov[e]) * kInvSqrtDk;
-      }
-#pragma unroll
-      for (int q8 = 0; q8 < 2; ++q8) {
-        float sq[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sq[e] = ov[q8 * 8 + e] * ov[q8 * 8 + e];
-        const float tot = reduce8(sq, lane);
-        if ((lane & 3) == 0) rpart[quarter * 64 + part * 16 + q8 * 8 + tok8(lane)] = tot;
+        OT[t * kHeadDim + row] = fmaf(egv[t] * iqv[t], z[e], ov[e]) * kInvSqrtDk;
       }
     }
-    // one barrier: the RMS partials are published and (when gating) the z rows have landed
+    // one barrier: o is in OT and (when gating) the z rows have landed
     if (want_gate) {
       if (!wait_mma(&bars[5], par)) { ok = false; break; }
     } else {
       __syncthreads();
     }
-    // 1/rms of this warp's 16 tokens: lane e < 16 takes token 16 part + e (shuffled out below)
-    float rinv_l = 0.f;
-    if (lane < 16) {
-      const int t = part * 16 + lane;
-      rinv_l = rsqrtf(((rpart[t] + rpart[64 + t]) + (rpart[128 + t] + rpart[192 + t])) * (1.0f / kHeadDim) + p.eps);
-    }
+    // ---- the gated RMSNorm over dv, token-major: eight threads per token, each
+    // with four groups of 4 dv (group q at 4 (s8 + 8 q)), the sum of squares
+    // over the eight by shuffles
     {
-      if (p.o) {
+      const int t = tid >> 3, s8 = tid & 7;
+      const float* orow = OT + t * kHeadDim;
+      float4 o4[4];
+      float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int t = part * 16 + e;
-          if (t < L) p.o[((size_t)(tc + t) * p.Hv + h) * kHeadDim + row] = f32_to_bf16(ov[e]);
-        }
+      for (int q = 0; q < 4; ++q) {
+        o4[q] = *reinterpret_cast<const float4*>(orow + 4 * (s8 + 8 * q));
+        ss = fmaf(o4[q].x, o4[q].x, ss);
+        ss = fmaf(o4[q].y, o4[q].y, ss);
+        ss = fmaf(o4[q].z, o4[q].z, ss);
+        ss = fmaf(o4[q].w, o4[q].w, ss);
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      const float rinv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+      if (p.o && t < L) {
+        uint16_t* op = p.o + ((size_t)(tc + t) * p.Hv + h) * kHeadDim;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint2*>(op + 4 * (s8 + 8 * q)) =
+              make_uint2(pack_bf16(o4[q].x, o4[q].y), pack_bf16(o4[q].z, o4[q].w));
       }
       if (want_gate) {
-        // Ogate over the z rows in place (thread: column `row` of 16 token rows) ...
-        const float gm = p.gamma[row];
+        // Ogate over the z rows in place ...
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int t = part * 16 + e;
-          uint16_t* zp = ZS + t * kHeadDim + row;
-          const float rinv = __shfl_sync(0xffffffffu, rinv_l, e);
-          *zp = f32_to_bf16(ov[e] * rinv * gm * silu_tanh(bf16_to_f32(*zp)));
+        for (int q = 0; q < 4; ++q) {
+          const int dv0 = 4 * (s8 + 8 * q);
+          uint2* zp = reinterpret_cast<uint2*>(ZS + t * kHeadDim + dv0);
+          const uint2 z2 = *zp;
+          const float4 g4 = __ldg(reinterpret_cast<const float4*>(p.gamma + dv0));
+          const float z0 = __uint_as_float(z2.x << 16), z1 = __uint_as_float(z2.x & 0xffff0000u);
+          const float z2f = __uint_as_float(z2.y << 16), z3 = __uint_as_float(z2.y & 0xffff0000u);
+          *zp = make_uint2(pack_bf16(o4[q].x * rinv * g4.x * silu_tanh(z0), o4[q].y * rinv * g4.y * silu_tanh(z1)),
+                           pack_bf16(o4[q].z * rinv * g4.z * silu_tanh(z2f), o4[q].w * rinv * g4.w * silu_tanh(z3)));
         }
       }
     }
@@ -918,7 +970,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           }
           if (own_qk && g == 0) {
             uint16_t* hp = p.conv_hist + ((size_t)ss * p.CH + gqk) * 3;
-            hp[0] = hqk[0]; hp[1] = hqk[1]; hp[2] = hqk[2];
+            hp[0] = (uint16_t)hqk[0]; hp[1] = (uint16_t)hqk[1]; hp[2] = (uint16_t)hqk[2];
+            hp[3] = (uint16_t)(hqk[0] >> 16); hp[4] = (uint16_t)(hqk[1] >> 16); hp[5] = (uint16_t)(hqk[2] >> 16);
           }
         }
       }
@@ -946,7 +999,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // CTA to start (its ticket, taken after the old history was read)
     if (*last_of_group && own_qk) {
       uint16_t* hp = p.conv_hist + ((size_t)slot * p.CH + gqk) * 3;
-      hp[0] = hqk[0]; hp[1] = hqk[1]; hp[2] = hqk[2];
+      hp[0] = (uint16_t)hqk[0]; hp[1] = (uint16_t)hqk[1]; hp[2] = (uint16_t)hqk[2];
+      hp[3] = (uint16_t)(hqk[0] >> 16); hp[4] = (uint16_t)(hqk[1] >> 16); hp[5] = (uint16_t)(hqk[2] >> 16);
     }
   } else {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);

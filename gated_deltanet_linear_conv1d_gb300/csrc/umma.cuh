@@ -113,6 +113,29 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t adesc, uint64_t bd
   }
 }
 
+// The same MMA with the A operand read from tensor memory instead of shared
+// memory: row m of A is lane m (M = 128), and its K elements run along the
+// columns from a_tmem, one 32-bit column per tf32 element or per pair of bf16
+// elements (the lower-indexed element in the low half).
+template <uint32_t kKind>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc_v,
+                                       uint32_t accumulate) {
+  static_assert(kKind == kKindTF32 || kKind == kKindF16, "tf32 or bf16 A from tensor memory");
+  if constexpr (kKind == kKindTF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc_v), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc_v), "r"(accumulate)
+        : "memory");
+  }
+}
+
 // Arrives once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -240,11 +263,14 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t
   return base + (lane << 16) + col;
 }
 
-// fp32 -> tf32 (round to nearest, ties away), kept in an fp32 container.
+// fp32 -> tf32 (round to nearest, ties away from zero), kept in an fp32
+// container: adding half a tf32 unit in the last place (bit 12) to the bit
+// pattern rounds the magnitude, a carry out of the mantissa moving into the
+// exponent as it should, and clearing the 13 bits that tf32 does not keep
+// truncates the rest. Two integer operations (finite inputs; a NaN may come out
+// as an infinity).
 __device__ __forceinline__ float to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 }  // namespace umma

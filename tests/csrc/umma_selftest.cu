@@ -97,6 +97,86 @@ __global__ void __launch_bounds__(128) selftest_kernel(const Args p) {
   if (warp == 0) umma::tmem_dealloc(tmem, 256);
 }
 
+// The same GEMM with A read from tensor memory (columns 128.. of the
+// allocation): tf32 as one 32-bit column per element (a_raw: the unrounded
+// fp32 value, to see how the tensor core reads it), bf16 as one column per
+// pair of elements, the lower-indexed one in the low half. B is K-major in
+// shared memory.
+__global__ void __launch_bounds__(128) selftest_ts_kernel(const Args p, int a_raw) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tbase;
+  unsigned char* sB = smem + kBOffset;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool tf32 = p.kind == umma::kTF32;
+  const int es = tf32 ? 4 : 2;
+  const int b_row_bytes = p.K * es;
+  for (int i = tid; i < p.N * p.K; i += blockDim.x) {
+    const int n = i / p.K, k = i % p.K;
+    const uint32_t off = umma::tile_off(n, k * es, b_row_bytes);
+    if (tf32) *reinterpret_cast<float*>(sB + off) = umma::to_tf32(p.B[i]);
+    else *reinterpret_cast<uint16_t*>(sB + off) = f32_to_bf16(p.B[i]);
+  }
+  umma::fence_proxy_async_smem();
+  if (warp == 0) umma::tmem_alloc(&tbase, 256);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = tbase;
+  // row m = 32 warp + lane of A into its lane, 8 columns at a time
+  const int m = 32 * warp + lane;
+  const int acols = tf32 ? p.K : p.K / 2;
+  for (int c0 = 0; c0 < acols; c0 += 8) {
+    float v[8];
+    for (int e = 0; e < 8; ++e) {
+      const int c = c0 + e;
+      if (tf32) {
+        const float x = p.A[(size_t)m * p.K + c];
+        v[e] = a_raw ? x : umma::to_tf32(x);
+      } else {
+        const uint32_t lo = f32_to_bf16(p.A[(size_t)m * p.K + 2 * c]);
+        const uint32_t hi = f32_to_bf16(p.A[(size_t)m * p.K + 2 * c + 1]);
+        v[e] = __uint_as_float(lo | (hi << 16));
+      }
+    }
+    umma::st8(umma::taddr(tmem, 32 * warp, 128 + c0), v);
+  }
+  umma::wait_st();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  if (tid == 0) {
+    const uint32_t id = umma::idesc(p.kind, false, false, p.M, p.N);
+    const int kstep = tf32 ? 8 : 16;
+    for (int kk = 0; kk < p.K / kstep; ++kk) {
+      const uint32_t acol = 128 + kk * 8;  // 8 columns: 8 tf32 or 16 bf16 elements
+      const uint64_t bdesc = umma::smem_desc(smem_u32(sB) + kk * (kstep * es / 16) * 128, b_row_bytes, false);
+      if (tf32) umma::mma_ts<umma::kKindTF32>(tmem, tmem + acol, bdesc, id, kk > 0);
+      else umma::mma_ts<umma::kKindF16>(tmem, tmem + acol, bdesc, id, kk > 0);
+    }
+    umma::commit(&bar);
+  }
+  const int ok = __syncthreads_and(mbar_wait_bounded(&bar, 0) ? 1 : 0);
+  umma::fence_after_sync();
+  if (ok) {
+    for (int c0 = 0; c0 < p.N; c0 += 32) {
+      float v[32];
+      umma::ld32(umma::taddr(tmem, 32 * warp, c0), v);
+      for (int i = 0; i < 32; ++i) p.D[(size_t)(32 * warp + lane) * p.N + c0 + i] = v[i];
+    }
+  } else if (tid == 0) {
+    atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  if (warp == 0) umma::tmem_dealloc(tmem, 256);
+}
+
 // A wait that can never succeed (nothing arrives on the barrier): the bounded
 // wait gives up after its time limit and the kernel reports a timeout in the
 // device error word, leaving the context usable.
@@ -132,5 +212,20 @@ extern "C" int umma_selftest(const float* A, const float* B, float* D, int* err,
     return 3;
   Args a{A, B, D, err, M, N, K, kind, a_mn, b_mn, b_cols};
   selftest_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+// A from tensor memory: M = 128, N in {64, 128}, K in {64, 128}, B K-major.
+extern "C" int umma_selftest_ts(const float* A, const float* B, float* D, int* err, int N, int K, int kind,
+                                int a_raw, void* stream) {
+  if ((N != 64 && N != 128) || (K != 64 && K != 128)) return 1;
+  if (kind != umma::kBF16 && kind != umma::kTF32) return 1;
+  if (a_raw && kind != umma::kTF32) return 1;
+  const size_t smem = kSmemBytes;
+  if (cudaFuncSetAttribute(selftest_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return 3;
+  Args a{A, B, D, err, 128, N, K, kind, 0, 0, K};
+  selftest_ts_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(a, a_raw);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

@@ -69,8 +69,8 @@ def test_algorithmic_byte_counts():
         2 * 12 * 128 * 128 * 4 + 2 * 2560 * 3 * 2 + 2560 * 2 + 12 * 128 * 2 + 12 * 8 + 4 + 12 * 128 * 2)
     bf16, tf32 = bench.prefill_flops(g, [64, 1, 65])
     chunks = 1 + 1 + 2
-    assert tf32 == chunks * 48 * (2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
-    assert bf16 == chunks * (48 * (4 * 128 * 64 * 128 + 2 * 128 * 64 * 64) + 16 * 2 * 128 * 64 * 128)
+    assert tf32 == chunks * 48 * (2 * 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
+    assert bf16 == chunks * (48 * 4 * 128 * 64 * 128 + 16 * 2 * 128 * 64 * 128)
 
 
 def test_reference_arm_prints_one_line(tmp_path):
