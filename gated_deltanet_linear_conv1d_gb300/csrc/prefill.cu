@@ -62,9 +62,14 @@ constexpr int kC = 64;  // chunk length
 constexpr float kInvSqrtDk = 0.08838834764831845f;
 
 // Shared-memory regions (byte offsets, 1024-aligned).
+// The two conv-written tiles have rows of 256 bytes, their row octets 16 bytes
+// further apart than dense (2064 instead of 2048): the conv's 16-byte stores to
+// rows 2j and 2j + 1 of eight threads then hit distinct banks.
+constexpr int kOct = 2048 + 16;
 constexpr int kKQ = 0;                  // bf16 [128 dk][128 t]: k tokens 0-63, q tokens 64-127 (MN-major)
-constexpr int kKT = kKQ + 32768;        // fp32 [128 dk][64 t]: raw k, then k diag(Gamma_C / |k|) as tf32 (K-major B)
-constexpr int kOT = kKT + 32768;        // fp32 [64 t][128 dv]: o of the chunk, token-major (the gate's input)
+constexpr int kKT = kKQ + 33792;        // fp32 [128 dk][64 t]: raw k, then k diag(Gamma_C / |k|) as tf32 (K-major B)
+constexpr int kOT = kKT + 33792;        // fp32 [64 t][128 dv]: o of the chunk, token-major (the gate's input)
+static_assert(16 * kOct <= 33792, "padded tile overruns its region");
 // Scratch: raw q and k rows of a chunk [2 parts][64 t][128] bf16 (TMA, read by
 // the conv), later the inverse's A [64][68], T [64][68] and block products
 // [32][36]; then the q and k rows of the next chunk.
@@ -509,21 +514,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         // raw q or k, bf16: rows dq, dq + 1 of KQ, tokens (q ? 64 : 0) + tb ..
         unsigned char* kq = reinterpret_cast<unsigned char*>(KQ);
         const int cb = ((isq ? kC : 0) + tb) * 2;
-        *reinterpret_cast<uint4*>(kq + umma::tile_off(dq, cb, 256)) =
+        *reinterpret_cast<uint4*>(kq + umma::tile_off_oct(dq, cb, kOct)) =
             make_uint4(pack_bf16(ya[0].x, ya[1].x), pack_bf16(ya[2].x, ya[3].x), pack_bf16(ya[4].x, ya[5].x),
                        pack_bf16(ya[6].x, ya[7].x));
-        *reinterpret_cast<uint4*>(kq + umma::tile_off(dq + 1, cb, 256)) =
+        *reinterpret_cast<uint4*>(kq + umma::tile_off_oct(dq + 1, cb, kOct)) =
             make_uint4(pack_bf16(ya[0].y, ya[1].y), pack_bf16(ya[2].y, ya[3].y), pack_bf16(ya[4].y, ya[5].y),
                        pack_bf16(ya[6].y, ya[7].y));
         if (!isq) {
           // raw k in fp32 (scaled and rounded to tf32 once the norms are known)
-          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4, 256)) =
+          *reinterpret_cast<float4*>(KTb + umma::tile_off_oct(dq, tb * 4, kOct)) =
               make_float4(ya[0].x, ya[1].x, ya[2].x, ya[3].x);
-          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq, tb * 4 + 16, 256)) =
+          *reinterpret_cast<float4*>(KTb + umma::tile_off_oct(dq, tb * 4 + 16, kOct)) =
               make_float4(ya[4].x, ya[5].x, ya[6].x, ya[7].x);
-          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq + 1, tb * 4, 256)) =
+          *reinterpret_cast<float4*>(KTb + umma::tile_off_oct(dq + 1, tb * 4, kOct)) =
               make_float4(ya[0].y, ya[1].y, ya[2].y, ya[3].y);
-          *reinterpret_cast<float4*>(KTb + umma::tile_off(dq + 1, tb * 4 + 16, 256)) =
+          *reinterpret_cast<float4*>(KTb + umma::tile_off_oct(dq + 1, tb * 4 + 16, kOct)) =
               make_float4(ya[4].y, ya[5].y, ya[6].y, ya[7].y);
         }
       }
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (tid == 0) {
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-        const uint64_t a = umma::smem_desc(sKQ + kk * 4096, 256, true);
+        const uint64_t a = umma::smem_desc_oct(sKQ + kk * 2 * kOct, kOct, true);
         umma::mma<umma::kBF16>(tm + kT_D1, a, a, id_kk, kk > 0);
       }
       umma::commit(&bars[0]);
@@ -549,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
       // warp so that the Gram product's issue does not wait behind it
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        umma::mma_ts<umma::kKindF16>(tm + kT_X, tm + kT_S0 + kk * 8, umma::smem_desc(sKQ + kk * 4096, 256, true),
+        umma::mma_ts<umma::kKindF16>(tm + kT_X, tm + kT_S0 + kk * 8, umma::smem_desc_oct(sKQ + kk * 2 * kOct, kOct, true),
                                      id_xz, kk > 0);
       umma::commit(&bars[1]);
     }
@@ -837,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int t = 32 * th + 4 * q;
-          float4* kp = reinterpret_cast<float4*>(KTb + umma::tile_off(r, t * 4, 256));
+          float4* kp = reinterpret_cast<float4*>(KTb + umma::tile_off_oct(r, t * 4, kOct));
           const float4 k4 = *kp;
           const float4 g4 = *reinterpret_cast<const float4*>(glv + t);
           const float4 n4 = *reinterpret_cast<const float4*>(ikv + t);
@@ -870,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
         umma::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kC / 8; ++kk)
-          umma::mma_ts<umma::kKindTF32>(tm + kTS_S, tm + kT_E + kk * 8, umma::smem_desc(sKT + kk * 256, 256, false),
+          umma::mma_ts<umma::kKindTF32>(tm + kTS_S, tm + kT_E + kk * 8, umma::smem_desc_oct(sKT + kk * 256, kOct, false),
                                         id_s, 1);
 #pragma unroll
         for (int kk = 0; kk < kC / 8; ++kk)

@@ -39,6 +39,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t row_bytes
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) | (1ull << 46);
 }
 
+// The same layout with the row octets `octet_bytes` apart instead of
+// row_bytes * 8 (a multiple of 16): a 16-byte gap after each octet moves the
+// next octet's rows to other banks, so that eight threads storing 16 bytes
+// each to rows r, r + 2, ..., r + 14 of two octets hit eight distinct bank groups.
+__host__ __device__ __forceinline__ uint32_t tile_off_oct(int r, int c_bytes, int octet_bytes) {
+  return (uint32_t)((r >> 3) * octet_bytes + (c_bytes >> 4) * 128 + (r & 7) * 16 + (c_bytes & 15));
+}
+
+// Descriptor of a tile laid out by tile_off_oct: K-major takes LBO = 128 and
+// SBO = the octet stride, MN-major LBO = the octet stride and SBO = 128.
+__device__ __forceinline__ uint64_t smem_desc_oct(uint32_t saddr, uint32_t octet_bytes, bool mn_major) {
+  const uint64_t octet = octet_bytes, chunk = 128;
+  const uint64_t lbo = mn_major ? octet : chunk, sbo = mn_major ? chunk : octet;
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) | (1ull << 46);
+}
+
 // Descriptor of a K-major tile written by TMA with 128-byte swizzling: rows of
 // 128 bytes, 8-row groups 1024 bytes apart (SBO), the tile 1024-byte aligned.
 // A step along K inside the 128-byte row advances the start address.
