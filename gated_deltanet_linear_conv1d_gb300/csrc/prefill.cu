@@ -88,7 +88,7 @@ constexpr int kZS = kXV + 16384;        // bf16 [64][128]: z rows, then Ogate ro
 constexpr int kTB = kZS + 16384;        // tf32 [64 r][64 i]: T diag(b) (K-major B)
 constexpr int kPB = kTB + 16384;        // tf32 [64 r][64 i]: P (K-major B)
 constexpr int kSmall = kPB + 16384;     // small per-chunk vectors
-constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 2;
+constexpr int kSmallFloats = 2 * 4 * 64 + 64 * 2 + kHeadDim;
 constexpr int kBars = kSmall + kSmallFloats * 4;
 constexpr int kSmemBytes = kBars + 128;
 
@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   float* gates = small;          // [2][4][64]
   float* iqv = gates + 2 * 4 * 64;  // [64] 1/|q|
   float* ikv = iqv + 64;         // [64] 1/|k|
+  float* gam = ikv + 64;         // [128] the RMSNorm gain
   float* MS = reinterpret_cast<float*>(smem + kMS);
   // MMA completions 0: [K;Q][K;Q]^T  1: X,Z  2: E  3: S, O';  copies 4: raw q, k rows
   // 5: z rows  6: raw v rows
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     issue_v(t0);
     if (want_gate) issue_z(t0);
   }
+  if (tid < kHeadDim) gam[tid] = p.gamma[tid];
   // T diag(beta) above the block diagonal stays zero; the rest is rewritten per chunk
   for (int it = tid; it < kC * kC / 4; it += kThreads)
     reinterpret_cast<float4*>(TBb)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -888,9 +890,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     // ---- o = (e^g Z / |q| + O') / sqrt(dk), written token-major to OT (thread:
     // dv row `row`, tokens 16 part ..; a warp writes 32 consecutive floats)
     {
+      uint32_t zr[16], orr[16];
+      umma::ld16_nowait(tm + lane_base + kT_Z + part * 16, zr);
+      umma::ld16_nowait(tm + lane_base + kT_O + part * 16, orr);
+      umma::wait_ld();
       float z[16], ov[16];
-      umma::ld16(tm + lane_base + kT_Z + part * 16, z);
-      umma::ld16(tm + lane_base + kT_O + part * 16, ov);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        z[e] = __uint_as_float(zr[e]);
+        ov[e] = __uint_as_float(orr[e]);
+      }
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = part * 16 + e;
@@ -937,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
           const int dv0 = 4 * (s8 + 8 * q);
           uint2* zp = reinterpret_cast<uint2*>(ZS + t * kHeadDim + dv0);
           const uint2 z2 = *zp;
-          const float4 g4 = __ldg(reinterpret_cast<const float4*>(p.gamma + dv0));
+          const float4 g4 = *reinterpret_cast<const float4*>(gam + dv0);
           const float z0 = __uint_as_float(z2.x << 16), z1 = __uint_as_float(z2.x & 0xffff0000u);
           const float z2f = __uint_as_float(z2.y << 16), z3 = __uint_as_float(z2.y & 0xffff0000u);
           *zp = make_uint2(pack_bf16(o4[q].x * rinv * g4.x * silu_tanh(z0), o4[q].y * rinv * g4.y * silu_tanh(z1)),
