@@ -255,10 +255,17 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
           umma::ld32_nowait(tm + lane_base + b * kBN, v0);
           umma::ld32_nowait(tm + lane_base + b * kBN + 32, v1);
           umma::wait_ld();
+          const float2 sc2 = make_float2(scale, scale);  // packed fp32x2 FMAs
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            acc[i] = fmaf(scale, __uint_as_float(v0[i]), acc[i]);
-            acc[32 + i] = fmaf(scale, __uint_as_float(v1[i]), acc[32 + i]);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 a0 = __ffma2_rn(sc2, make_float2(__uint_as_float(v0[i]), __uint_as_float(v0[i + 1])),
+                                         make_float2(acc[i], acc[i + 1]));
+            acc[i] = a0.x;
+            acc[i + 1] = a0.y;
+            const float2 a1 = __ffma2_rn(sc2, make_float2(__uint_as_float(v1[i]), __uint_as_float(v1[i + 1])),
+                                         make_float2(acc[32 + i], acc[32 + i + 1]));
+            acc[32 + i] = a1.x;
+            acc[32 + i + 1] = a1.y;
           }
         }
         umma::fence_before_sync();
@@ -491,12 +498,26 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
         }
         umma::fence_after_sync();
         const uint32_t tp = tm + lane_off + b * kWN + 128 * h;
+        // 32 columns per tensor-memory round trip (two loads under one wait), folded
+        // with packed fp32x2 FMAs
+        const float2 sc2 = make_float2(scale, scale);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float v[16];
-          umma::ld16(tp + 16 * c, v);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v0[16], v1[16];
+          umma::ld16_nowait(tp + 32 * c, v0);
+          umma::ld16_nowait(tp + 32 * c + 16, v1);
+          umma::wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(scale, v[i], acc[16 * c + i]);
+          for (int i = 0; i < 16; i += 2) {
+            const float2 a0 = __ffma2_rn(sc2, make_float2(__uint_as_float(v0[i]), __uint_as_float(v0[i + 1])),
+                                         make_float2(acc[32 * c + i], acc[32 * c + i + 1]));
+            acc[32 * c + i] = a0.x;
+            acc[32 * c + i + 1] = a0.y;
+            const float2 a1 = __ffma2_rn(sc2, make_float2(__uint_as_float(v1[i]), __uint_as_float(v1[i + 1])),
+                                         make_float2(acc[32 * c + 16 + i], acc[32 * c + 16 + i + 1]));
+            acc[32 * c + 16 + i] = a1.x;
+            acc[32 * c + 16 + i + 1] = a1.y;
+          }
         }
         umma::fence_before_sync();
         __syncwarp();
