@@ -160,10 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const int quarter = warp & 3, part = warp >> 2;
   const int row = 32 * quarter + lane;  // tensor-memory lane read by this thread
 
-  // ---- request checks (uniform over the request's CTAs)
+  // ---- request checks (uniform over the request's CTAs); the request's scalars
+  // are loaded together, before the first check, so their latencies overlap
   const int slot = p.slot_idx[n];
-  if (slot < 0) return;
   const int t0 = p.qsl[n], t1 = p.qsl[n + 1];
+  const int p0 = p.pos0 ? p.pos0[n] : 0;  // tokens of the request before this call
+  const bool init = p.has_init ? p.has_init[n] != 0 : true;
+  if (slot < 0) return;
   if (t0 < 0 || t1 < t0 || t1 > p.T || (n == 0 && t0 != 0) || (n == p.N - 1 && t1 != p.T)) {
     if (tid == 0 && g == 0) report(p.dev_err, GDN_DEVERR_OFFSETS);
     return;
@@ -173,12 +176,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     return;
   }
   if (t1 == t0) return;  // no tokens: the slot is left untouched
-  const int p0 = p.pos0 ? p.pos0[n] : 0;  // tokens of the request before this call
   if (p0 < 0) {
     if (tid == 0 && g == 0) report(p.dev_err, GDN_DEVERR_OFFSETS);
     return;
   }
-  const bool init = p.has_init ? p.has_init[n] != 0 : true;
+
+  // chunks end on absolute multiples of 64 (p0 tokens precede this call), so
+  // the first one may be short
+  const int first = min(kC - p0 % kC, t1 - t0);
+  const int nchunks = 1 + (t1 - t0 - first + kC - 1) / kC;
+  // the gate warp's first alpha, beta loads are issued here, ahead of the setup
+  constexpr int kGateWarp = kThreads / 32 - 1;
+  float alpha_n0 = 1.f, beta_n0 = 0.f, alpha_n1 = 1.f, beta_n1 = 0.f;
+  auto load_ab = [&](int ts, int len) {  // alpha, beta of tokens ts .. ts + len - 1
+    if (lane < len) {
+      alpha_n0 = p.alpha[(size_t)(ts + lane) * p.Hv + h];
+      beta_n0 = p.beta[(size_t)(ts + lane) * p.Hv + h];
+    }
+    if (lane + 32 < len) {
+      alpha_n1 = p.alpha[(size_t)(ts + lane + 32) * p.Hv + h];
+      beta_n1 = p.beta[(size_t)(ts + lane + 32) * p.Hv + h];
+    }
+  };
+  if (warp == kGateWarp) load_ab(t0, first);
 
   uint16_t* KQ = reinterpret_cast<uint16_t*>(smem + kKQ);
   unsigned char* KTb = smem + kKT;
@@ -275,6 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     if (want_gate) issue_z(t0);
   }
   if (tid < kHeadDim) gam[tid] = p.gamma[tid];
+  // the initial state (thread (row, part) owns 32 columns) is loaded now and
+  // stored into tensor memory after the barrier, so its latency overlaps the setup
+  float s0v[32];
+  {
+    const float* src = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + part * 32;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 f = init ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      s0v[i] = f.x; s0v[i + 1] = f.y; s0v[i + 2] = f.z; s0v[i + 3] = f.w;
+    }
+  }
   // T diag(beta) above the block diagonal stays zero; the rest is rewritten per chunk
   for (int it = tid; it < kC * kC / 4; it += kThreads)
     reinterpret_cast<float4*>(TBb)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -292,17 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     *last_of_group = atomicAdd(p.tickets + (size_t)n * p.Hk + j, 1) == p.G - 1;
   }
 
-  // ---- initial state into tensor memory: thread (row, part) owns 32 columns
-  {
-    const float* src = p.state + (((size_t)slot * p.Hv + h) * kHeadDim + row) * kHeadDim + part * 32;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const float4 f = init ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
-    }
-    umma::st32(tm + lane_base + kTS_S + part * 32, v);
-  }
+  // ---- initial state into tensor memory
+  umma::st32(tm + lane_base + kTS_S + part * 32, s0v);
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
@@ -315,27 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
   const uint32_t sKQ = smem_u32(KQ), sKT = smem_u32(KTb);
   const uint32_t sTB = smem_u32(TBb), sPB = smem_u32(PBb);
 
-  // chunks end on absolute multiples of 64 (p0 tokens precede this call), so
-  // the first one may be short
-  const int first = min(kC - p0 % kC, t1 - t0);
-  const int nchunks = 1 + (t1 - t0 - first + kC - 1) / kC;
   bool ok = true;
   // ---- gates of a chunk (warp 15, two tokens per lane, no CTA barrier): g =
   // inclusive cumsum of log2(alpha) (so e^{g ln 2} = prod alpha), e^g,
   // e^{g_C - g_t}, beta. The chunk's alpha and beta sit in the lanes' registers,
   // loaded one chunk before they are needed.
-  constexpr int kGateWarp = kThreads / 32 - 1;
-  float alpha_n0 = 1.f, beta_n0 = 0.f, alpha_n1 = 1.f, beta_n1 = 0.f;
-  auto load_ab = [&](int ts, int len) {  // alpha, beta of tokens ts .. ts + len - 1
-    if (lane < len) {
-      alpha_n0 = p.alpha[(size_t)(ts + lane) * p.Hv + h];
-      beta_n0 = p.beta[(size_t)(ts + lane) * p.Hv + h];
-    }
-    if (lane + 32 < len) {
-      alpha_n1 = p.alpha[(size_t)(ts + lane + 32) * p.Hv + h];
-      beta_n1 = p.beta[(size_t)(ts + lane + 32) * p.Hv + h];
-    }
-  };
   auto make_gates = [&](float* gb, int len) {
     float* g_ = gb;
     float* eg = gb + 64;
@@ -363,8 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillAr
     gl_[lane] = lane < len ? ex2(gl - s0) : 0.f;
     gl_[lane + 32] = lane + 32 < len ? ex2(gl - s1) : 0.f;
   };
-  if (warp == kGateWarp) {  // chunk 0's gates now, chunk 1's alpha and beta into the registers
-    load_ab(t0, first);
+  if (warp == kGateWarp) {  // chunk 0's gates now (its alpha, beta loaded at entry), chunk 1's into the registers
     make_gates(gates, first);
     if (nchunks > 1) load_ab(t0 + first, min(kC, t1 - t0 - first));
   }
