@@ -613,6 +613,91 @@ def measure_out_proj(b, dev, stream) -> dict:
             "hbm_peak_gbs": hbm_peak, **res}
 
 
+def measure_gate_wo(b, dev, stream) -> dict:
+    """Where the gated RMSNorm in front of Wo runs. Two forms of the same work (mixer, gate, Wo with the
+    residual add), timed back to back on one stream at the decode batch (256 requests of the 512-slot
+    pool) and on the varlen prefill batch (71,068 tokens):
+      fused:    the mixer kernel applies RMSNorm(o) * gamma * SiLU(z) to o in registers and writes Ogate;
+                the Wo GEMM reads Ogate.
+      separate: the mixer writes o only; the standalone gated RMSNorm reads o and z and writes Ogate;
+                the Wo GEMM reads Ogate.
+    Both move the same z bytes; the separate form adds the o round trip (12 KB per token written and read
+    back) and a launch. `mixer_*_ms` are the mixer kernel alone in each output mode (the fused gate's
+    cost inside the mixer)."""
+    import torch
+    geom = synth.FULL_HEADS
+    H, Dv = geom.num_v_heads, geom.head_v_dim
+    K, Nout = H * Dv, 5120
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    wo = (torch.randn((Nout, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {}
+
+    def measure(name, T, mixer, z, gamma, steps, warmup):
+        og = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+        o = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+        hidden = torch.randn((T, Nout), generator=g, device=dev).to(torch.bfloat16)
+
+        def fused():
+            mixer(None, og)
+            b.gdn_out_proj(og, wo, hidden, residual=hidden, dev_err=err, stream=stream)
+
+        def separate():
+            mixer(o, None)
+            b.gdn_gated_rmsnorm(o, z, gamma, 1e-6, og, stream=stream)
+            b.gdn_out_proj(og, wo, hidden, residual=hidden, dev_err=err, stream=stream)
+
+        r = {"tokens": T,
+             "fused_ms": timed(fused, steps, warmup, stream),
+             "separate_ms": timed(separate, steps, warmup, stream),
+             "mixer_ogate_ms": timed(lambda: mixer(None, og), steps, warmup, stream),
+             "mixer_o_only_ms": timed(lambda: mixer(o, None), steps, warmup, stream)}
+        r["separate_over_fused"] = r["separate_ms"] / r["fused_ms"]
+        if b.gdn_read_device_error(err) != 0:
+            raise RuntimeError(f"device error flagged during the gate + Wo measurement ({name})")
+        res[name] = r
+        del og, o, hidden
+
+    # decode: 256 requests over a 512-slot pool (the headline step)
+    d = device_workload(geom, NUM_SLOTS, NUM_REQ, seed=12, dev=dev)
+    slots = torch.from_numpy(synth.slot_permutation(np.random.default_rng(12), NUM_REQ, NUM_SLOTS)).to(dev)
+    D = b.make_dims(geom, NUM_SLOTS)
+
+    def decode_mixer(o, og):
+        b.gdn_decode_step(D, d["qkv0"], d["conv_w"], d["conv_hist"], d["state"], slots, d["alpha"], d["beta"],
+                          d["z"], d["gamma"], 1e-6, o=o, ogate=og, dev_err=err, stream=stream)
+    measure("decode", NUM_REQ, decode_mixer, d["z"], d["gamma"], 40, 5)
+    del d
+    torch.cuda.empty_cache()
+
+    # prefill: the varlen batch of the prefill measurement
+    lengths = synth.loguniform_lengths(np.random.default_rng(3), 64, 16, 8192)
+    N, T = len(lengths), int(lengths.sum())
+    Rs = 2 * N
+    w = device_workload(geom, Rs, T, seed=3, dev=dev)
+    pslots = torch.from_numpy(synth.slot_permutation(np.random.default_rng(3), N, Rs)).to(dev)
+    qsl = torch.from_numpy(synth.pack_offsets(lengths)).to(dev)
+    has_init = np.ones(N, np.uint8)
+    has_init[: N // 2] = 0
+    hi = torch.from_numpy(has_init).to(dev)
+    Dp = b.make_dims(geom, Rs)
+    ws = torch.empty(b.gdn_prefill_workspace_bytes(Dp, N, T), dtype=torch.uint8, device=dev)
+
+    def prefill_mixer(o, og):
+        b.gdn_chunk_prefill(Dp, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], qsl, pslots, w["alpha"],
+                            w["beta"], w["z"] if og is not None else None, w["gamma"], 1e-6, o=o, ogate=og,
+                            has_init=hi, workspace=ws, dev_err=err, stream=stream)
+    measure("prefill", T, prefill_mixer, w["z"], w["gamma"], 5, 2)
+    del w
+    torch.cuda.empty_cache()
+    return {"workload": "mixer (decode step of 256 requests / varlen prefill of 71,068 tokens) + gated RMSNorm + "
+                        "Wo 6144 -> 5120 with the residual added in place, bf16",
+            "forms": "fused = mixer writes Ogate (gate in its epilogue), then Wo; separate = mixer writes o, "
+                     "gdn_gated_rmsnorm, then Wo",
+            **res}
+
+
 def measure_in_proj(b, dev, stream, geom, D) -> dict:
     """The in_proj rows (hidden 5120 -> QKV0 10240, Z 6144, a|b 96 fp32; one launch of the tcgen05 GEMM) at the
     decode batch (weight-streaming: two weight sets in rotation, 338 MB, so no step finds its weights in
@@ -925,6 +1010,8 @@ def run_gpu(args):
         extra["rmsnorm"] = measure_rmsnorm(b, dev, stream)
         torch.cuda.empty_cache()
         extra["gated_rmsnorm"] = measure_gated_rmsnorm(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["gate_wo"] = measure_gate_wo(b, dev, stream)
         torch.cuda.empty_cache()
         extra["fp8_proj"] = measure_fp8_proj(b, dev, stream)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
