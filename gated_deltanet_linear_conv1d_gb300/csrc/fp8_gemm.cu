@@ -13,16 +13,20 @@
 // product. Four tensor-memory buffers let the MMAs run up to three blocks ahead
 // of the folding.
 //
-// Two schedules. With at least two waves of 128 x 256 tiles (prefill token
-// counts) fp8_gemm_wide_kernel below takes 128 tokens x 256 outputs per tile
-// (N = 256 MMAs, two 256-column buffers). Otherwise fp8_gemm_kernel takes
-// 128 x 128 tiles: with at least two waves of those a persistent CTA takes whole
-// tiles blockIdx.x, blockIdx.x + gridDim.x, ... and stores bf16 rows directly. With fewer tiles (the decode batch) the K blocks of
-// all tiles, laid end to end, are cut into gridDim.x equal contiguous ranges
-// (stream-K), so every SM does the same work; a CTA stores the fp32 partial of a
-// tile it covers only in part into its own workspace slice (plain coalesced
-// stores), and the CTA that finishes a tile's last piece (an atomic ticket, no
-// waiting) adds the other pieces, stores the bf16 tile and resets the ticket.
+// Schedules, by the number of 128 x 256 output tiles. With at least two waves of
+// them (prefill token counts) fp8_gemm_wide_kernel below takes 128 tokens x 256
+// outputs per tile (N = 256 MMAs, two 256-column buffers) on persistent CTAs.
+// With at most one wave (decode batches) the same kernel splits each tile's K
+// blocks over a cluster of CTAs, which add their parts through the workspace
+// (see the kernel). In between, fp8_gemm_kernel takes 128 x 128 tiles: with at
+// least two waves of those a persistent CTA takes whole tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... and stores bf16 rows directly. With fewer tiles
+// the K blocks of all tiles, laid end to end, are cut into gridDim.x equal
+// contiguous ranges (stream-K), so every SM does the same work; a CTA stores the
+// fp32 partial of a tile it covers only in part into its own workspace slice
+// (plain coalesced stores), and the CTA that finishes a tile's last piece (an
+// atomic ticket, no waiting) adds the other pieces, stores the bf16 tile and
+// resets the ticket.
 //
 // Warp roles (320 threads): warp 0 lane 0 issues the TMA copies into a 4-stage
 // ring (X8 and W8 tiles, 128 B x 128 rows each, 128-byte swizzle), warp 1
@@ -30,6 +34,10 @@
 // store: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (its 32 tokens) and
 // columns 64 ((w - 2) / 4) .. +63 (its half of the 128 outputs).
 #include <cuda.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "device.cuh"
 #include "launch.h"
@@ -356,6 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
 // overlaps the MMAs of block kb + 1. The fp32 running sum of the tile stays in
 // registers: promotion warp w holds the 128 columns of half (w - 2) / 4 for the
 // 32 rows of its tensor-memory lane quarter.
+//
+// With at most one wave of such tiles (a decode batch: 40 tiles for Wo at 256
+// tokens) the same kernel splits K instead (p.split > 1): the grid is tiles x
+// split CTAs in clusters of `split`, CTA b takes K blocks [r KB / split,
+// (r + 1) KB / split) of tile b / split (r = b % split), and the parts meet
+// through the caller's workspace in L2: each part stores its running sums of
+// the whole tile with coalesced 16-byte stores, a cluster barrier orders those
+// stores before the loads, and part k adds up the parts of row band [k 128 /
+// split, (k + 1) 128 / split) in part order (the bits do not depend on timing)
+// and stores it.
 constexpr int kWN = 256;
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = kTileBytes + kWN * kBK;   // 16 KB of X rows + 32 KB of W rows
@@ -363,6 +381,13 @@ constexpr int kWBarOff = kWStages * kWStageBytes;
 constexpr int kWSmemBytes = kWBarOff + 256 + 1024;
 constexpr int kWScaleAhead = 2;  // fewer registers than the narrow kernel: the sum takes 128
 constexpr uint32_t kWIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kWN);
+constexpr int kMaxSplitW = 4;  // parts of K per tile at most
+
+// All threads of every CTA of the cluster; orders the memory accesses before it
+// (release) against those after it (acquire) at cluster scope.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8GemmArgs p,
                                                                      const __grid_constant__ CUtensorMap tmx,
@@ -396,6 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
   volatile int* abort_flag = flags;
   const int nt = (p.N + kWN - 1) / kWN;
   const int tiles = p.mt * nt;  // the launcher keeps this below 2^31
+  // split == 1: persistent CTAs take whole tiles blockIdx.x, + gridDim.x, ...;
+  // split > 1: this CTA takes part `part` of tile blockIdx.x / split, K blocks kb_lo .. kb_hi-1
+  const int split = p.split;
+  const int part = split > 1 ? (int)(blockIdx.x % (unsigned)split) : 0;
+  const int t_first = split > 1 ? (int)(blockIdx.x / (unsigned)split) : (int)blockIdx.x;
+  const int t_step = split > 1 ? tiles : (int)gridDim.x;
+  const int kb_lo = part * p.KB / split, kb_hi = (part + 1) * p.KB / split;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -403,9 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
       uint32_t gk = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t = t_first; t < tiles && ok; t += t_step) {
         const int m_t = t / nt, n_t = t % nt;
-        for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++gk) {
           const int s = gk % kWStages;
           if ((gk >= (uint32_t)kWStages && !mbar_wait_bounded(&empty[s], ((gk / kWStages) - 1) & 1)) ||
               *abort_flag) {
@@ -429,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
     if (lane == 0) {
       uint32_t gk = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+      for (int t = t_first; t < tiles && ok; t += t_step) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++gk) {
           const int s = gk % kWStages;
           const uint32_t b = gk & 1, use = gk >> 1;
           if (!mbar_wait_bounded(&full[s], (gk / kWStages) & 1) ||
@@ -459,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int NB = (p.N + 127) / 128;
     uint32_t gk = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+    for (int t = t_first; t < tiles; t += t_step) {
       const int m_t = t / nt, n_t = t % nt;
       const int row = m_t * kBM + 32 * q + lane;
       const bool live = row < p.T;
@@ -469,14 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       float sx[kWScaleAhead], sw[kWScaleAhead];
 #pragma unroll
       for (int i = 0; i < kWScaleAhead; ++i) {
-        const int kb = min(i, p.KB - 1);
+        const int kb = min(kb_lo + i, kb_hi - 1);
         sx[i] = live ? __ldg(xs_row + kb) : 0.f;
         sw[i] = __ldg(ws_row + kb);
       }
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      for (int kb = 0; kb < p.KB; ++kb, ++gk) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++gk) {
         const uint32_t b = gk & 1, use = gk >> 1;
         const float scale = sx[0] * sw[0];
 #pragma unroll
@@ -485,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
           sw[i] = sw[i + 1];
         }
         {
-          const int kn = min(kb + kWScaleAhead, p.KB - 1);
+          const int kn = min(kb + kWScaleAhead, kb_hi - 1);
           sx[kWScaleAhead - 1] = live ? __ldg(xs_row + kn) : 0.f;
           sw[kWScaleAhead - 1] = __ldg(ws_row + kn);
         }
@@ -524,6 +556,17 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
         if (lane == 0) arrive_one(&tempty[b]);
       }
       if (*abort_flag != 0 || !live) continue;
+      if (split > 1) {
+        // this part's running sums of the tile to its slot of the workspace,
+        // [64 column quads][128 rows] float4s (a warp's 32 rows are 512
+        // contiguous bytes); rows past T are never read back
+        float4* slot = reinterpret_cast<float4*>(p.partial) + ((size_t)t * split + part) * (kBM * kWN / 4);
+        const int r = 32 * q + lane;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          __stcg(slot + (size_t)(32 * h + j) * kBM + r, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+        continue;
+      }
       uint16_t* out_row = p.out + (size_t)row * p.N;
       const uint16_t* res_row = p.residual ? p.residual + (size_t)row * p.N : nullptr;
       const int n0 = n_t * kWN + 128 * h;
@@ -535,6 +578,57 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
         store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
       }
     }
+    if (split > 1) {
+      // ---- once every part of the cluster has stored its sums (the barrier), the
+      // promotion threads add up the parts of this part's band of rows, [r0, r1),
+      // in part order: item (row r, 8-column group g), consecutive threads on
+      // consecutive rows; the loads of two items are issued before either sum
+      __threadfence();
+      __syncwarp();
+      cluster_sync_all();
+      const int t = t_first, m_t = t / nt, n_t = t % nt;
+      const int r0 = part * kBM / split, nrows = (part + 1) * kBM / split - r0;
+      const int items = nrows * (kWN / 8);
+      const float4* base = reinterpret_cast<const float4*>(p.partial) + (size_t)t * split * (kBM * kWN / 4);
+      const int tp = tid - 64;
+      for (int i0 = tp; i0 < items && *abort_flag == 0; i0 += 2 * kPromo) {
+        float4 lo[2][kMaxSplitW], hi[2][kMaxSplitW];
+        int rr[2], gg[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = min(i0 + u * kPromo, items - 1);
+          gg[u] = i / nrows;
+          rr[u] = r0 + i % nrows;
+#pragma unroll
+          for (int k = 0; k < kMaxSplitW; ++k) {
+            if (k < split) {
+              const float4* src = base + (size_t)k * (kBM * kWN / 4) + (size_t)(2 * gg[u]) * kBM + rr[u];
+              lo[u][k] = __ldcg(src);
+              hi[u][k] = __ldcg(src + kBM);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int row = m_t * kBM + rr[u];
+          if (i0 + u * kPromo >= items || row >= p.T) continue;
+          float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k = 0; k < kMaxSplitW; ++k) {
+            if (k < split) {
+              v[0] += lo[u][k].x; v[1] += lo[u][k].y; v[2] += lo[u][k].z; v[3] += lo[u][k].w;
+              v[4] += hi[u][k].x; v[5] += hi[u][k].y; v[6] += hi[u][k].z; v[7] += hi[u][k].w;
+            }
+          }
+          store_row8(p.out + (size_t)row * p.N, p.residual ? p.residual + (size_t)row * p.N : nullptr,
+                     n_t * kWN + 8 * gg[u], p.N, v);
+        }
+      }
+    }
+  }
+  if (split > 1 && warp < 2) {
+    __syncwarp();
+    cluster_sync_all();  // the producer and MMA warps take part in the cluster barrier too
   }
 
   umma::fence_before_sync();
@@ -562,56 +656,100 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
+// Clusters of `csize` CTAs of the wide kernel that fit on the GPU at once (per
+// device and cluster size, queried once); 0 if the query fails.
+int wide_resident_clusters(int csize) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({dev, csize});
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)csize, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_wide_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  cache.emplace(std::make_pair(dev, csize), n);
+  return n;
+}
+
 }  // namespace
 
-// Stream-K (equal K-block ranges) when the tiles make fewer than two waves.
+// Schedules, by the number of 128 x 256 tiles:
+//  - at least two waves: the wide kernel, persistent over whole tiles;
+//  - at most one wave: the wide kernel with K split over clusters of `split`
+//    CTAs (split 1: one CTA per tile), as many parts as leave every part at
+//    least four K blocks and let all the clusters run at once;
+//  - in between: the 128 x 128 kernel, stream-K (equal K-block ranges) when its
+//    tiles make fewer than two waves.
 struct Plan8 {
+  int kind;  // 0: 128 x 128 kernel, 1: wide persistent, 2: wide, one wave, split K
+  int split;
   bool stream_k;
   long long tiles, total;
   int grid;
 };
 
 Plan8 plan_fp8(int T, int N, int K, int sms) {
-  Plan8 pl;
+  Plan8 pl{};
+  const int KB = K / kBK;
+  const long long wide_tiles = (long long)((T + kBM - 1) / kBM) * ((N + kWN - 1) / kWN);
+  if (wide_tiles >= 2LL * sms && wide_tiles < (1LL << 31)) {
+    pl.kind = 1;
+    pl.split = 1;
+    pl.tiles = wide_tiles;
+    pl.grid = sms;
+    return pl;
+  }
+  if (wide_tiles <= sms) {
+    int split = (int)(sms / wide_tiles);
+    if (split > kMaxSplitW) split = kMaxSplitW;
+    if (split > KB / 4) split = KB / 4;
+    while (split >= 2 && wide_tiles > wide_resident_clusters(split)) --split;
+    if (split < 2) split = 1;
+    pl.kind = 2;
+    pl.split = split;
+    pl.tiles = wide_tiles;
+    pl.grid = (int)(wide_tiles * split);
+    return pl;
+  }
+  pl.kind = 0;
+  pl.split = 1;
   pl.tiles = (long long)((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-  pl.total = pl.tiles * (K / kBK);
+  pl.total = pl.tiles * KB;
   pl.stream_k = pl.tiles < 2LL * sms && pl.total > pl.tiles;
   const long long work = pl.stream_k ? pl.total : pl.tiles;
   pl.grid = (int)(work < sms ? work : sms);
   return pl;
 }
 
-size_t fp8_gemm_workspace_bytes(int T, int N, int K) {
-  const Plan8 pl = plan_fp8(T, N, K, num_sms());
-  if (!pl.stream_k) return 0;
-  return (size_t)pl.grid * 2 * kBM * kBN * 4 + ((size_t)pl.tiles * 4 + 255) / 256 * 256;
+size_t plan_workspace_bytes(const Plan8& pl) {
+  if (pl.kind == 2 && pl.split > 1) return (size_t)pl.tiles * pl.split * kBM * kWN * 4;
+  if (pl.kind == 0 && pl.stream_k) return (size_t)pl.grid * 2 * kBM * kBN * 4 + ((size_t)pl.tiles * 4 + 255) / 256 * 256;
+  return 0;
 }
+
+size_t fp8_gemm_workspace_bytes(int T, int N, int K) { return plan_workspace_bytes(plan_fp8(T, N, K, num_sms())); }
 
 cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_bytes, int32_t* dev_err,
                             cudaStream_t stream) {
   if (o.T == 0) return cudaSuccess;
-  const int sms_w = num_sms();
-  const long long wide_tiles = (long long)((o.T + kBM - 1) / kBM) * ((o.N + kWN - 1) / kWN);
-  if (wide_tiles >= 2LL * sms_w && wide_tiles < (1LL << 31)) {  // many tiles: 128 x 256 tiles
-    CUtensorMap tmx{}, tmw{};
-    if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K, kWN)) return cudaErrorInvalidValue;
-    Fp8GemmArgs a{};
-    a.xs = o.xs;
-    a.ws = o.ws;
-    a.residual = o.residual;
-    a.out = o.out;
-    a.dev_err = dev_err;
-    a.T = o.T;
-    a.N = o.N;
-    a.KB = o.K / kBK;
-    a.mt = (o.T + kBM - 1) / kBM;
-    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes);
-    if (err != cudaSuccess) return err;
-    fp8_gemm_wide_kernel<<<sms_w, kThreads, kWSmemBytes, stream>>>(a, tmx, tmw);
-    return cudaGetLastError();
-  }
-  CUtensorMap tmx{}, tmw{};
-  if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K)) return cudaErrorInvalidValue;
+  const int sms = num_sms();
+  Plan8 pl = plan_fp8(o.T, o.N, o.K, sms);
+  const bool room = workspace && ws_bytes >= plan_workspace_bytes(pl);
   Fp8GemmArgs a{};
   a.xs = o.xs;
   a.ws = o.ws;
@@ -622,10 +760,40 @@ cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_byt
   a.N = o.N;
   a.KB = o.K / kBK;
   a.mt = (o.T + kBM - 1) / kBM;
+  a.split = 1;
+  if (pl.kind != 0) {  // 128 x 256 tiles
+    CUtensorMap tmx{}, tmw{};
+    if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K, kWN)) return cudaErrorInvalidValue;
+    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes);
+    if (err != cudaSuccess) return err;
+    if (pl.kind == 2 && pl.split > 1 && !room) {  // no room for the parts: one CTA per tile
+      pl.split = 1;
+      pl.grid = (int)pl.tiles;
+    }
+    if (pl.split == 1) {
+      fp8_gemm_wide_kernel<<<pl.grid, kThreads, kWSmemBytes, stream>>>(a, tmx, tmw);
+      return cudaGetLastError();
+    }
+    a.split = pl.split;
+    a.partial = static_cast<float*>(workspace);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fp8_gemm_wide_kernel, a, tmx, tmw);
+  }
+  CUtensorMap tmx{}, tmw{};
+  if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K)) return cudaErrorInvalidValue;
   a.nt = (o.N + kBN - 1) / kBN;
-  const int sms = num_sms();
-  Plan8 pl = plan_fp8(o.T, o.N, o.K, sms);
-  if (pl.stream_k && (!workspace || ws_bytes < fp8_gemm_workspace_bytes(o.T, o.N, o.K))) {
+  if (pl.stream_k && !room) {
     pl.stream_k = false;  // no room for the partial tiles: whole tiles only
     pl.grid = (int)(pl.tiles < sms ? pl.tiles : sms);
   }

@@ -129,12 +129,14 @@ struct Fp8GemmArgs {
   const float* ws;
   const uint16_t* residual;
   uint16_t* out;
-  float* partial;  // stream-K partial tiles [grid][2][128 x 128 fp32], or nullptr
+  float* partial;  // stream-K partial tiles [grid][2][128 x 128 fp32], the wide kernel's split
+                   // parts [tiles][split][128 x 256 fp32], or nullptr
   int* tile_cnt;   // stream-K tickets [tiles] (zero on entry, left zero), or nullptr
   int32_t* dev_err;
   int T, N, KB;
   int mt, nt;
   int stream_k;          // 1: equal K-block ranges per CTA; 0: whole tiles, strided
+  int split;             // wide kernel: 1 persistent over whole tiles; > 1 parts of K per tile (clusters)
   long long tiles, total;  // output tiles; tiles x K blocks
 };
 

@@ -365,13 +365,16 @@ gdn_status gdn_in_proj(const gdn_dims *dims, const uint16_t *hidden, int32_t hid
  *   cores form each 128-wide block product of K exactly (E4M3 products, fp32
  *   sums) and fp32 registers take the scaled sum over blocks. K a multiple of
  *   128, N a multiple of 16.
- *   workspace: when K is split across CTAs, one fp32 partial tile per split
- *   and a ticket per output tile, gdn_fp8_linear_workspace_bytes(T, K, N) bytes
- *   (0: this shape is not split on the current GPU), 256-byte aligned and
- *   ZERO-FILLED before its first use: the tickets must start at zero, and every
- *   call that completes resets them, so the workspace is reusable without
- *   clearing (after a call that reports a device error, clear it again). NULL or
- *   too small: K is not split. Calls sharing one workspace must not overlap.
+ *   workspace: when K is split across CTAs, the fp32 partial sums of the
+ *   parts (one 128 x 256 tile per K part at decode-sized token counts, where a
+ *   cluster of CTAs shares each output tile; one 128 x 128 tile per CTA and a
+ *   ticket per output tile for the stream-K schedule of mid-sized counts),
+ *   gdn_fp8_linear_workspace_bytes(T, K, N) bytes (0: this shape is not split
+ *   on the current GPU), 256-byte aligned and ZERO-FILLED before its first use:
+ *   the tickets must start at zero, and every call that completes resets them,
+ *   so the workspace is reusable without clearing (after a call that reports a
+ *   device error, clear it again). NULL or too small: K is not split. Calls
+ *   sharing one workspace must not overlap.
  *   dev_err: GDN_DEVERR_TIMEOUT if a bounded wait inside the kernel ran out.
  */
 gdn_status gdn_fp8_quant_act(const uint16_t *x, uint8_t *x8, float *x_scale, int32_t num_tokens, int32_t k,

@@ -174,8 +174,9 @@ def test_quantise_then_multiply_end_to_end(b):
 @pytest.mark.parametrize("T,K,N,res", [(1, 6144, 5120, True), (16, 256, 144, False), (100, 5120, 6144, True),
                                        (256, 5120, 96 * 2, False), (257, 1024, 256, False)])
 def test_fp8_linear_decode_batches(b, T, K, N, res):
-    """Decode-sized token counts (one to three m tiles, stream-K over the K blocks): a single token,
-    ragged tiles, the a|b width, and a ragged third m tile; the workspace is reused without clearing."""
+    """Decode-sized token counts (one to three m tiles of 128 x 256, each tile's K blocks split over a
+    cluster of CTAs that add their parts through the workspace): a single token, ragged tiles, the
+    a|b width, and a ragged third m tile; the workspace is reused without clearing."""
     x8, xs, w8, ws, r = _operands(T, K, N, 470 + T + N)
     out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
     wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda")
@@ -206,3 +207,29 @@ def test_fp8_linear_wide_tiles(b, T, K, N, res):
                          residual=U.dev_bf16(r) if res else None, workspace=wsp, dev_err=err)
     assert b.gdn_read_device_error(err) == 0
     U.check_out(U.host_f64_from_bf16(out), oracle.fp8_linear(x8, xs, w8, ws, r if res else None), "out")
+
+
+@pytest.mark.parametrize("T,K,N,res,with_ws", [
+    (129, 2048, 1024, True, True),     # 8 tiles, K split 4 ways; the second m tile holds one live row
+    (64, 6144, 5136, False, True),     # 21 tiles, the last one 16 outputs wide; K split 6 or 7 ways
+    (256, 6144, 5120, True, False),    # Wo at the decode batch without a workspace: one CTA per tile
+    (1000, 256, 5120, True, True),     # 160 tiles of 128 x 256: the 128 x 128 kernel, whole tiles
+    (12800, 256, 384, False, True),    # 200 tiles of 128 x 256, 300 of 128 x 128: the stream-K schedule
+])
+def test_fp8_linear_schedules(b, T, K, N, res, with_ws):
+    """Each schedule of gdn_fp8_linear on a 152-SM GB300, picked by the number of 128 x 256 output
+    tiles: at most one wave splits K over clusters (the parts meet in the workspace, in part order),
+    between one and two waves takes 128 x 128 tiles (whole tiles, or stream-K when they make fewer
+    than two waves); two calls in a row give the same bits."""
+    x8, xs, w8, ws, r = _operands(T, K, N, 520 + T + N)
+    wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda") if with_ws else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+        b.gdn_fp8_linear(_dev_u8(x8), U.dev(xs), _dev_u8(w8), U.dev(ws), out,
+                         residual=U.dev_bf16(r) if res else None, workspace=wsp, dev_err=err)
+        outs.append(out)
+    assert b.gdn_read_device_error(err) == 0
+    assert torch.equal(outs[0], outs[1])
+    U.check_out(U.host_f64_from_bf16(outs[0]), oracle.fp8_linear(x8, xs, w8, ws, r if res else None), "out")
