@@ -557,14 +557,25 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       }
       if (*abort_flag != 0 || !live) continue;
       if (split > 1) {
-        // this part's running sums of the tile to its slot of the workspace,
-        // [64 column quads][128 rows] float4s (a warp's 32 rows are 512
-        // contiguous bytes); rows past T are never read back
-        float4* slot = reinterpret_cast<float4*>(p.partial) + ((size_t)t * split + part) * (kBM * kWN / 4);
+        // this part's running sums of the tile: the rows of its own band into
+        // shared memory (the operand ring is idle now), [64 column quads][band
+        // rows] float4s; the other rows to its slot of the workspace, [64 column
+        // quads][128 rows] float4s (a warp's 32 rows are 512 contiguous bytes).
+        // Rows past T are never read back.
         const int r = 32 * q + lane;
+        const int r0 = part * kBM / split, nrows = (part + 1) * kBM / split - r0;
+        if (r >= r0 && r < r0 + nrows) {
+          float4* dst = reinterpret_cast<float4*>(smem) + (size_t)32 * h * nrows + (r - r0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          __stcg(slot + (size_t)(32 * h + j) * kBM + r, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+          for (int j = 0; j < 32; ++j)
+            dst[(size_t)j * nrows] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.partial) + ((size_t)t * split + part) * (kBM * kWN / 4) +
+                        (size_t)32 * h * kBM + r;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            __stcg(dst + (size_t)j * kBM, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+        }
         continue;
       }
       uint16_t* out_row = p.out + (size_t)row * p.N;
@@ -581,8 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
     if (split > 1) {
       // ---- once every part of the cluster has stored its sums (the barrier), the
       // promotion threads add up the parts of this part's band of rows, [r0, r1),
-      // in part order: item (row r, 8-column group g), consecutive threads on
-      // consecutive rows; the loads of two items are issued before either sum
+      // in part order (its own part from shared memory): item (row r, 8-column
+      // group g), consecutive threads on consecutive rows; the loads of three
+      // items are issued before any sum
       __threadfence();
       __syncwarp();
       cluster_sync_all();
@@ -591,17 +603,29 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       const int items = nrows * (kWN / 8);
       const float4* base = reinterpret_cast<const float4*>(p.partial) + (size_t)t * split * (kBM * kWN / 4);
       const int tp = tid - 64;
-      for (int i0 = tp; i0 < items && *abort_flag == 0; i0 += 2 * kPromo) {
-        float4 lo[2][kMaxSplitW], hi[2][kMaxSplitW];
-        int rr[2], gg[2];
+      const float4* own = reinterpret_cast<const float4*>(smem);
+      constexpr int kItems = 3;
+      for (int i0 = tp; i0 < items && *abort_flag == 0; i0 += kItems * kPromo) {
+        float4 lo[kItems][kMaxSplitW], hi[kItems][kMaxSplitW];
+        uint4 res[kItems];
+        int rr[kItems], gg[kItems];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kItems; ++u) {
           const int i = min(i0 + u * kPromo, items - 1);
           gg[u] = i / nrows;
           rr[u] = r0 + i % nrows;
+          // the residual is loaded with the parts, before any store (out may be the residual)
+          const int row = m_t * kBM + rr[u], col = n_t * kWN + 8 * gg[u];
+          res[u] = (p.residual && row < p.T && col < p.N)
+                       ? *reinterpret_cast<const uint4*>(p.residual + (size_t)row * p.N + col)
+                       : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int k = 0; k < kMaxSplitW; ++k) {
-            if (k < split) {
+            if (k == part) {
+              const float4* src = own + (size_t)(2 * gg[u]) * nrows + (rr[u] - r0);
+              lo[u][k] = src[0];
+              hi[u][k] = src[nrows];
+            } else if (k < split) {
               const float4* src = base + (size_t)k * (kBM * kWN / 4) + (size_t)(2 * gg[u]) * kBM + rr[u];
               lo[u][k] = __ldcg(src);
               hi[u][k] = __ldcg(src + kBM);
@@ -609,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
           }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kItems; ++u) {
           const int row = m_t * kBM + rr[u];
           if (i0 + u * kPromo >= items || row >= p.T) continue;
           float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -620,8 +644,13 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
               v[4] += hi[u][k].x; v[5] += hi[u][k].y; v[6] += hi[u][k].z; v[7] += hi[u][k].w;
             }
           }
-          store_row8(p.out + (size_t)row * p.N, p.residual ? p.residual + (size_t)row * p.N : nullptr,
-                     n_t * kWN + 8 * gg[u], p.N, v);
+          const uint32_t rw[4] = {res[u].x, res[u].y, res[u].z, res[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[2 * e] += bf16_to_f32(rw[e] & 0xffff);
+            v[2 * e + 1] += bf16_to_f32(rw[e] >> 16);
+          }
+          store_row8(p.out + (size_t)row * p.N, nullptr, n_t * kWN + 8 * gg[u], p.N, v);
         }
       }
     }
