@@ -30,6 +30,49 @@ cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
   return cudaSuccess;
 }
 
+int resident_clusters(const void* fn, int threads, size_t smem, int cluster_size) {
+  struct Key {
+    const void* fn;
+    int dev, threads, csize;
+    size_t smem;
+    bool operator==(const Key& o) const {
+      return fn == o.fn && dev == o.dev && threads == o.threads && csize == o.csize && smem == o.smem;
+    }
+  };
+  struct Hash {
+    size_t operator()(const Key& k) const {
+      return std::hash<const void*>()(k.fn) ^ ((size_t)k.dev << 40) ^ ((size_t)k.threads << 20) ^
+             ((size_t)k.csize << 12) ^ k.smem;
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, int, Hash> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const Key key{fn, dev, threads, cluster_size, smem};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster_size, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster_size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache.emplace(key, n);
+  return n;
+}
+
 namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

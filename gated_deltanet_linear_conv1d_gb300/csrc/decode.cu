@@ -722,27 +722,13 @@ void split_config(const StepArgs& a, int nsplit, cudaLaunchConfig_t* cfg, cudaLa
   cfg->numAttrs = 1;
 }
 
-// Clusters of the row-split kernel that fit on the GPU at once, per (device,
-// group size, split), queried once.
+// Clusters of the row-split kernel that fit on the GPU at once.
 int split_clusters_resident(const StepArgs& a, int nsplit) {
-  static std::mutex mu;
-  static std::unordered_map<long long, int> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const long long key = ((long long)dev << 32) | ((long long)a.G << 8) | nsplit;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr;
   split_config(a, nsplit, &cfg, &attr);
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, split_kernel, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    n = 0;
-  }
-  cache.emplace(key, n);
-  return n;
+  return resident_clusters(reinterpret_cast<const void*>(split_kernel), (int)cfg.blockDim.x, cfg.dynamicSmemBytes,
+                           nsplit);
 }
 
 // Rows of a unit split over nsplit CTAs when the units alone would leave SMs

@@ -35,10 +35,6 @@
 // columns 64 ((w - 2) / 4) .. +63 (its half of the 128 outputs).
 #include <cuda.h>
 
-#include <map>
-#include <mutex>
-#include <utility>
-
 #include "device.cuh"
 #include "launch.h"
 #include "umma.cuh"
@@ -685,34 +681,10 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-// Clusters of `csize` CTAs of the wide kernel that fit on the GPU at once (per
-// device and cluster size, queried once); 0 if the query fails.
+// Clusters of `csize` CTAs of the wide kernel that fit on the GPU at once.
 int wide_resident_clusters(int csize) {
-  static std::mutex mu;
-  static std::map<std::pair<int, int>, int> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find({dev, csize});
-  if (it != cache.end()) return it->second;
-  int n = 0;
-  if (ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)csize, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kWSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_wide_kernel, &cfg) != cudaSuccess) n = 0;
-  }
-  (void)cudaGetLastError();
-  cache.emplace(std::make_pair(dev, csize), n);
-  return n;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes) != cudaSuccess) return 0;
+  return resident_clusters(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kThreads, kWSmemBytes, csize);
 }
 
 }  // namespace

@@ -43,10 +43,6 @@
 // GDN_DEVERR_TIMEOUT and the CTA skips its remaining work.
 #include <cuda.h>
 
-#include <map>
-#include <mutex>
-#include <utility>
-
 #include "device.cuh"
 #include "launch.h"
 #include "umma.cuh"
@@ -542,34 +538,9 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-// Clusters of `csize` CTAs of this kernel that fit on the GPU at once (per
-// device and cluster size, queried once); 0 if the query fails.
-int resident_clusters(int csize) {
-  static std::mutex mu;
-  static std::map<std::pair<int, int>, int> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find({dev, csize});
-  if (it != cache.end()) return it->second;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)csize, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)csize;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    n = 0;
-  }
-  cache.emplace(std::make_pair(dev, csize), n);
-  return n;
+// Clusters of `csize` CTAs of this kernel that fit on the GPU at once.
+int gemm_resident_clusters(int csize) {
+  return resident_clusters(reinterpret_cast<const void*>(gemm_bf16_kernel), kThreads, kSmemBytes, csize);
 }
 
 }  // namespace
@@ -618,12 +589,12 @@ cudaError_t launch_gemm(const GemmOperands& o, int32_t* dev_err, cudaStream_t st
   int split = (int)(sms / (2 * pairs));
   if (split > kMaxSplit) split = kMaxSplit;
   if (split > a.KB) split = a.KB;
-  while (split >= 2 && pairs > resident_clusters(2 * split)) --split;
+  while (split >= 2 && pairs > gemm_resident_clusters(2 * split)) --split;
   if (split < 2) split = 1;
   a.split = split;
   long long clusters = pairs;
   if (split == 1) {  // persistent pairs: as many as fit at once
-    const int fit = resident_clusters(2);
+    const int fit = gemm_resident_clusters(2);
     const long long cap = fit > 0 ? fit : sms / 2;
     if (clusters > cap) clusters = cap;
   }

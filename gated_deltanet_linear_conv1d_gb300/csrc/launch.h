@@ -146,6 +146,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (function, device).
 cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
+// Clusters of `cluster_size` CTAs of kernel `fn` (blocks of `threads` threads,
+// `smem` bytes of dynamic shared memory, set with ensure_dynamic_smem first)
+// that the current device holds at once; queried once per (function, device,
+// cluster size, threads, shared memory); 0 if the query fails.
+int resident_clusters(const void* fn, int threads, size_t smem, int cluster_size);
+
 // Persistent state-streaming kernel (decode: P = 1, spec_slot NULL; verify: P >= 1).
 bool stream_supported(int G, int P);
 cudaError_t launch_stream(const StepArgs& a, cudaStream_t stream);
