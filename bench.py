@@ -407,6 +407,48 @@ def measure_decode_sweep(b, dev, stream, peak: float, max_reps: int = 200) -> di
     return out
 
 
+def measure_prefill_single(b, dev, stream, launches: int = 64, reps: int = 50) -> dict:
+    """The smallest prefill: one request of 64 tokens from a zero state (16/48 heads), the full mixer
+    (conv, L2 norms, one 64-token chunk on the tensor cores, gated RMSNorm). Launch-bound, so the
+    launches are captured in a CUDA graph (each on its own slot of a pool larger than L2) and the
+    graph is replayed; ms per launch from CUDA events around the replays."""
+    import torch
+    geom = synth.FULL_HEADS
+    T = 64
+    slot_bytes = geom.num_v_heads * geom.head_v_dim * geom.head_k_dim * 4
+    Rs = max(launches, -(-SWEEP_POOL_BYTES // slot_bytes))
+    w = device_workload(geom, Rs, T, seed=0, dev=dev)
+    qsl = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    zero = torch.zeros(1, dtype=torch.uint8, device=dev)
+    slots = torch.arange(Rs, dtype=torch.int32, device=dev).view(Rs, 1)
+    og = torch.empty((T, geom.num_v_heads * geom.head_v_dim), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    D = b.make_dims(geom, Rs)
+    ws = torch.empty(b.gdn_prefill_workspace_bytes(D, 1, T), dtype=torch.uint8, device=dev)
+
+    def launch(i):
+        b.gdn_chunk_prefill(D, w["qkv0"], w["conv_w"], w["conv_hist"], w["state"], qsl, slots[i % Rs], w["alpha"],
+                            w["beta"], w["z"], w["gamma"], 1e-6, ogate=og, has_init=zero, workspace=ws, dev_err=err)
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(3):
+            launch(i)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(launches):
+            launch(i)
+    ms = timed(graph.replay, reps, 2, stream) / launches
+    if b.gdn_read_device_error(err) != 0:
+        raise RuntimeError("device error flagged during the single-request prefill measurement")
+    return {"workload": "1 request x 64 tokens from a zero state, 16/48 heads (the smallest prefill)",
+            "kernels": "prefill_order_kernel + prefill_tc_kernel (48 CTAs, one chunk each)",
+            "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "launches": launches * reps}
+
+
 def measure_prefill(b, dev, stream, steps: int = 5, warmup: int = 2) -> dict:
     """Varlen chunked prefill: 64 requests, log-uniform lengths in [16, 8192], half from zero."""
     import torch
@@ -1000,6 +1042,8 @@ def run_gpu(args):
         extra["decode_sweep"] = measure_decode_sweep(b, dev, stream, peak, max_reps=max(3, min(200, args.steps // 5)))
         torch.cuda.empty_cache()
         extra["prefill"] = measure_prefill(b, dev, stream)
+        torch.cuda.empty_cache()
+        extra["prefill_single"] = measure_prefill_single(b, dev, stream)
         torch.cuda.empty_cache()
         extra["spec_mixed"] = measure_spec_mixed(b, dev, stream)
         torch.cuda.empty_cache()
