@@ -346,6 +346,28 @@ def timed(fn, steps: int, warmup: int, stream) -> float:
     return e0.elapsed_time(e1) / steps
 
 
+def graph_ms(launch, count: int, reps: int, stream, dev) -> float:
+    """Device milliseconds per launch of launch(i), i = 0 .. count-1, issued on the current stream:
+    warmed up, captured once in a CUDA graph and the graph replayed `reps` times (CUDA events on `stream`
+    around the replays). At decode sizes a kernel takes a few microseconds, less than the Python call
+    that issues it, so a loop of calls from Python would time the host instead."""
+    import torch
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(min(count, 4)):
+            launch(i)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(count):
+            launch(i)
+    ms = timed(graph.replay, reps, 2, stream) / count
+    del graph
+    return ms
+
+
 SWEEP_REQUESTS = (1, 8, 64, 256, 1024)
 SWEEP_POOL_BYTES = 512 << 20  # >= 4x L2: a slot's state is evicted before the step that uses it again
 
@@ -642,11 +664,15 @@ def measure_out_proj(b, dev, stream) -> dict:
             it[0] += 1
 
         ms = timed(run, steps, 4, stream)
+        extra = {}
+        if name == "decode":  # device time per launch (graph replays); `eager_ms` is the loop of Python calls
+            extra["eager_ms"] = ms
+            ms = graph_ms(lambda i: b.gdn_out_proj(a, weights[i % 4], hidden, residual=hidden), 16, 30, stream, dev)
         flops = 2.0 * T * K * N
         nbytes = N * K * 2 + T * K * 2 + 2 * T * N * 2
         res[name] = {"tokens": T, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
                      "tensor_frac": flops / (ms / 1e3) / 1e12 / p_bf16,
-                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, **extra}
         del a, hidden
     return {"workload": "out = Ogate Wo^T + residual, K=6144 -> N=5120, bf16 in/out, fp32 accumulation",
             "kernel": "gemm_bf16_kernel (gdn_out_proj): at the decode batch swapped 128-weight-row x 256-token "
@@ -767,12 +793,20 @@ def measure_in_proj(b, dev, stream, geom, D) -> dict:
             it[0] += 1
 
         ms = timed(run, steps, 4, stream)
+        extra = {}
+        if name == "decode":  # device time per launch (graph replays); `eager_ms` is the loop of Python calls
+            extra["eager_ms"] = ms
+
+            def launch(i):
+                wq, wz, wab = sets[i % 2]
+                b.gdn_in_proj(D, u, wq, wz, qkv0, z, w_ab=wab, ab=ab)
+            ms = graph_ms(launch, 16, 30, stream, dev)
         flops = 2.0 * T * Dh * (CH + NZ + NAB)
         # weights once, the hidden rows once, the outputs once
         nbytes = (CH + NZ + NAB) * Dh * 2 + T * Dh * 2 + T * (CH + NZ) * 2 + T * NAB * 4
         res[name] = {"tokens": T, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
                      "tensor_frac": flops / (ms / 1e3) / 1e12 / p_bf16,
-                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, **extra}
         del u, qkv0, z, ab
     return {"workload": "QKV0 = U Wqkv^T, Z = U Wz^T, [a|b] = U Wab^T, 5120 -> 10240 / 6144 / 96, bf16 in, "
                         "bf16 / bf16 / fp32 out, fp32 accumulation",
@@ -826,9 +860,22 @@ def measure_fp8_proj(b, dev, stream) -> dict:
 
             ms = timed(run, steps, 4, stream)
             ms_gemm = timed(gemms, steps, 4, stream)
+            extra = {}
+            if name == "decode":  # device time per step (graph replays); `eager_*` are loops of Python calls
+                extra = {"eager_ms": ms, "eager_gemm_ms": ms_gemm}
+
+                def gemms_i(i):
+                    for (w8, ws), out, wsp in zip(sets[i % nsets], outs, wsps):
+                        b.gdn_fp8_linear(x8, xs, w8, ws, out, workspace=wsp)
+
+                def run_i(i):
+                    b.gdn_fp8_quant_act(x, x8, xs)
+                    gemms_i(i)
+                ms = graph_ms(run_i, 16, 30, stream, dev)
+                ms_gemm = graph_ms(gemms_i, 16, 30, stream, dev)
             flops = 2.0 * T * K * sum(Ns)
             nbytes = wbytes + T * K * len(Ns) + T * sum(Ns) * 2
-            res[f"{proj}_{name}"] = {"tokens": T, "ms": ms, "gemm_ms": ms_gemm,
+            res[f"{proj}_{name}"] = {"tokens": T, "ms": ms, "gemm_ms": ms_gemm, **extra,
                                      "gemm_tflops": flops / (ms_gemm / 1e3) / 1e12,
                                      "gemm_tensor_frac_of_fp8": flops / (ms_gemm / 1e3) / 1e12 / p_fp8,
                                      "gemm_hbm_frac": nbytes / (ms_gemm / 1e3) / 1e9 / hbm_peak}
@@ -867,9 +914,17 @@ def measure_rmsnorm(b, dev, stream) -> dict:
             it[0] += 1
 
         ms = timed(run, steps, 4, stream)
+        extra = {}
+        if name == "decode":  # device time per launch (graph replays); `eager_ms` is the loop of Python calls
+            extra["eager_ms"] = ms
+
+            def launch(i):
+                x, r, u = sets[i % nset]
+                b.gdn_rmsnorm(x, gamma, 1e-6, u, residual=r)
+            ms = graph_ms(launch, 64, 30, stream, dev)
         nbytes = 4 * T * Dh * 2 + Dh * 4
         res[name] = {"tokens": T, "ms": ms, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
-                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, **extra}
         del sets
     return {"workload": "residual <- x + residual; U = RMSNorm(residual) * gamma, hidden 5120, bf16",
             "kernel": "rmsnorm_kernel (gdn_rmsnorm)", "hbm_peak_gbs": hbm_peak, **res}
@@ -897,9 +952,17 @@ def measure_gated_rmsnorm(b, dev, stream) -> dict:
             it[0] += 1
 
         ms = timed(run, steps, 4, stream)
+        extra = {}
+        if name == "decode":  # device time per launch (graph replays); `eager_ms` is the loop of Python calls
+            extra["eager_ms"] = ms
+
+            def launch(i):
+                o, z, out = sets[i % nset]
+                b.gdn_gated_rmsnorm(o, z, gamma, 1e-6, out)
+            ms = graph_ms(launch, 64, 30, stream, dev)
         nbytes = 3 * T * H * Dv * 2 + Dv * 4
         res[name] = {"tokens": T, "ms": ms, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
-                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+                     "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, **extra}
         del sets
     return {"workload": "Ogate = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z), 48 heads x 128, bf16",
             "kernel": "gated_rmsnorm_kernel (gdn_gated_rmsnorm)", "hbm_peak_gbs": hbm_peak, **res}
