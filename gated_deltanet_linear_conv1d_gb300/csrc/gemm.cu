@@ -59,7 +59,16 @@ constexpr int kTileA = kBM * 128;        // 16 KB: this CTA's 128 A rows
 constexpr int kTileB = (kBN / 2) * 128;  // 16 KB: this CTA's half of the B rows
 constexpr int kStageBytes = kTileA + kTileB;
 constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+// Swapped bf16 epilogue: each half of the epilogue warps stages 16 tokens x 128
+// outputs of fp32 here, so that rows of the token-major output leave in 16-byte
+// pieces, 256 contiguous bytes per token, instead of one 2-byte store per token
+// per thread.
+constexpr int kStgTokens = 16;
+constexpr int kStgOff = kBarOff + 256;
+constexpr int kStgBytes = 2 * kStgTokens * kBM * 4;
+constexpr int kSmemBytes = kStgOff + kStgBytes + 1024;  // + alignment slack
+// Tiles that are not swapped stage nothing: their launches take less shared memory.
+constexpr int kSmemBytesNoStage = kStgOff + 1024;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kCols = kBN / 2;  // accumulator columns per epilogue thread
@@ -431,7 +440,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       }
       aborted = __any_sync(0xffffffffu, aborted);  // warp-uniform: the tensor-memory loads are .aligned
       umma::fence_after_sync();
-      if (!aborted && valid && ncols > 0) {
+      if (p.swap && g.out_bf16 && valid) {
+        // swapped, bf16 out: the four warps of this half (the same loop count, so
+        // they pass the same named barriers) stage 16 tokens x 128 outputs at a
+        // time; thread i of the half then stores 8 consecutive outputs of a token
+        // (with their residual) as one 16-byte piece, two pieces per round
+        float* stg = reinterpret_cast<float*>(smem + kStgOff) + half * (kStgTokens * kBM);
+        const int hi = tid - 64 - 128 * half;  // 0 .. 127 within the half
+        const int row_base = tr.n_t * kBM;
+        for (int c = 0; c * kStgTokens < ncols; ++c) {
+          if (!aborted) {
+            float v[16];
+            umma::ld16(tm + lane_base + col0 + kStgTokens * c, v);
+#pragma unroll
+            for (int i = 0; i < kStgTokens; ++i) stg[i * kBM + 32 * q + lane] = v[i];
+          }
+          asm volatile("bar.sync %0, 128;" ::"r"(2 + half) : "memory");
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const int k = hi + 128 * m, t = k >> 4, rc = (k & 15) * 8;
+            const int token = c0 + kStgTokens * c + t, n = row_base + rc;
+            if (!aborted && t < ncols - kStgTokens * c && n < g.N) {
+              const float4 a = *reinterpret_cast<const float4*>(stg + t * kBM + rc);
+              const float4 bq = *reinterpret_cast<const float4*>(stg + t * kBM + rc + 4);
+              float f[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+              uint16_t* dst = g.out_bf16 + (size_t)token * g.N + n;
+              if (g.residual) {
+                const uint4 r = *reinterpret_cast<const uint4*>(g.residual + (size_t)token * g.N + n);
+                const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  f[2 * e] += bf16_to_f32(rw[e] & 0xffff);
+                  f[2 * e + 1] += bf16_to_f32(rw[e] >> 16);
+                }
+              }
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = (uint32_t)f32_to_bf16(f[2 * e]) | ((uint32_t)f32_to_bf16(f[2 * e + 1]) << 16);
+              *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+          asm volatile("bar.sync %0, 128;" ::"r"(2 + half) : "memory");  // the stage may be refilled
+        }
+      } else if (!aborted && valid && ncols > 0) {
 #pragma unroll 1
         for (int c = 0; c < kCols / 32 && 32 * c < ncols; ++c) {
           float v[32];
@@ -601,7 +653,7 @@ cudaError_t launch_gemm(const GemmOperands& o, int32_t* dev_err, cudaStream_t st
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * 2 * split), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = a.swap ? kSmemBytes : kSmemBytesNoStage;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
