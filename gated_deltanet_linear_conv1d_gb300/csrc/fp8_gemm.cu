@@ -374,7 +374,17 @@ constexpr int kWN = 256;
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = kTileBytes + kWN * kBK;   // 16 KB of X rows + 32 KB of W rows
 constexpr int kWBarOff = kWStages * kWStageBytes;
-constexpr int kWSmemBytes = kWBarOff + 256 + 1024;
+// Epilogue stage of whole tiles: each promotion warp turns its 32 token rows x
+// 128 outputs around 32 outputs at a time through [32 rows][33 floats] (the odd
+// stride keeps both the row-wise writes and the piece-wise reads free of bank
+// conflicts), so the output leaves in 16-byte pieces, 64 contiguous bytes per
+// token, with the pieces' residual loaded ahead, instead of one 16-byte store
+// per row per instruction with a dependent residual load before each.
+constexpr int kWStgLd = 33;
+constexpr int kWStgOff = kWBarOff + 256;
+constexpr int kWStgBytes = kPromoWarps * 32 * kWStgLd * 4;
+constexpr int kWSmemBytes = kWStgOff + kWStgBytes + 1024;
+static_assert(kWSmemBytes <= 227 * 1024, "wide kernel shared memory");
 constexpr int kWScaleAhead = 2;  // fewer registers than the narrow kernel: the sum takes 128
 constexpr uint32_t kWIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kWN);
 constexpr int kMaxSplitW = 4;  // parts of K per tile at most
@@ -551,6 +561,45 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
         __syncwarp();
         if (lane == 0) arrive_one(&tempty[b]);
       }
+      if (split == 1) {
+        // ---- whole tile: out (+ residual) through the warp's stage (see kWStgLd)
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) continue;
+        float* stg = reinterpret_cast<float*>(smem + kWStgOff) + (warp - 2) * (32 * kWStgLd);
+        const int tok0 = m_t * kBM + 32 * q, col_base = n_t * kWN + 128 * h;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stg[lane * kWStgLd + j] = acc[32 * st + j];
+          __syncwarp();
+          // piece k = lane + 32 m: token tok0 + k / 4, outputs col_base + 32 st + 8 (k % 4) ..
+          uint4 res[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int k = lane + 32 * m, trow = tok0 + (k >> 2), col = col_base + 32 * st + 8 * (k & 3);
+            res[m] = (p.residual && trow < p.T && col < p.N)
+                         ? *reinterpret_cast<const uint4*>(p.residual + (size_t)trow * p.N + col)
+                         : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int k = lane + 32 * m, t = k >> 2, cc = 8 * (k & 3);
+            const int trow = tok0 + t, col = col_base + 32 * st + cc;
+            if (trow < p.T && col < p.N) {
+              const uint32_t rw[4] = {res[m].x, res[m].y, res[m].z, res[m].w};
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = stg[t * kWStgLd + cc + 2 * e] + bf16_to_f32(rw[e] & 0xffff);
+                const float hi = stg[t * kWStgLd + cc + 2 * e + 1] + bf16_to_f32(rw[e] >> 16);
+                w4[e] = (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+              }
+              *reinterpret_cast<uint4*>(p.out + (size_t)trow * p.N + col) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+          __syncwarp();  // the stage is rewritten in the next step
+        }
+        continue;
+      }
       if (*abort_flag != 0 || !live) continue;
       if (split > 1) {
         // this part's running sums of the tile: the rows of its own band into
@@ -573,16 +622,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
             __stcg(dst + (size_t)j * kBM, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
         }
         continue;
-      }
-      uint16_t* out_row = p.out + (size_t)row * p.N;
-      const uint16_t* res_row = p.residual ? p.residual + (size_t)row * p.N : nullptr;
-      const int n0 = n_t * kWN + 128 * h;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = acc[8 * j + e];
-        store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
       }
     }
     if (split > 1) {
