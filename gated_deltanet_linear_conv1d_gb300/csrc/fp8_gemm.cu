@@ -60,6 +60,12 @@ constexpr int kPromo = 32 * kPromoWarps;         // promotion threads
 // f8f6f4, E4M3 x E4M3, fp32 accumulator, both K-major, M = 128, N = 128
 constexpr uint32_t kIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kBN);
 
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void promo_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Columns n .. n+7 of one output row: v (+ residual) rounded to bf16, one 16-byte store.
@@ -81,6 +87,31 @@ __device__ __forceinline__ void store_row8(uint16_t* out_row, const uint16_t* re
 #pragma unroll
   for (int e = 0; e < 4; ++e) w4[e] = (uint32_t)f32_to_bf16(f[2 * e]) | ((uint32_t)f32_to_bf16(f[2 * e + 1]) << 16);
   *reinterpret_cast<uint4*>(out_row + n) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+}
+
+// 64 consecutive outputs n0 .. n0+63 of one row (+ residual) as eight 16-byte stores, the
+// residual's eight pieces loaded before the first store (out may be the residual, so a
+// load after a store to it could not start before that store).
+__device__ __forceinline__ void store_row64(uint16_t* out_row, const uint16_t* res_row, int n0, int N,
+                                            const float (&acc)[64]) {
+  uint4 r[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    r[j] = (res_row && n0 + 8 * j < N) ? *reinterpret_cast<const uint4*>(res_row + n0 + 8 * j)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (n0 + 8 * j >= N) continue;
+    const uint32_t rw[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = acc[8 * j + 2 * e] + bf16_to_f32(rw[e] & 0xffff);
+      const float hi = acc[8 * j + 2 * e + 1] + bf16_to_f32(rw[e] >> 16);
+      w4[e] = (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+    }
+    *reinterpret_cast<uint4*>(out_row + n0 + 8 * j) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
 }
 
 __device__ __forceinline__ void arrive_one(uint64_t* bar) {
@@ -283,15 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
       uint16_t* out_row = p.out + (size_t)row * p.N;
       const uint16_t* res_row = p.residual ? p.residual + (size_t)row * p.N : nullptr;
       if (kb0 == 0 && kb1 == p.KB) {  // the whole tile
-        if (live && !aborted) {
-#pragma unroll
-          for (int j = 0; j < kCols / 8; ++j) {
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = acc[8 * j + e];
-            store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
-          }
-        }
+        if (live && !aborted) store_row64(out_row, res_row, n0, p.N, acc);
       } else {
         // a piece of the tile: partial slice (CTA, 0 for its first tile / 1 for its
         // last), float4 j of promotion thread i at [j][i], so that a warp's 32
@@ -301,43 +324,53 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_kernel(const Fp8GemmArgs
           return reinterpret_cast<float4*>(p.partial) + ((size_t)cta * 2 + slot) * (kCols / 4) * kPromo + pid;
         };
         auto owner = [&](long long L) { return ((L + 1) * G - 1) / p.total; };  // the CTA whose range holds L
-        if (!aborted) {
-          float4* dst = slice(blockIdx.x, t == my_first_tile ? 0 : 1);
-#pragma unroll
-          for (int j = 0; j < kCols / 4; ++j)
-            dst[(size_t)j * kPromo] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-        }
-        __threadfence();
-        promo_sync();
         const long long tl = (long long)t * p.KB;
         const long long c_first = owner(tl), c_last = owner(tl + p.KB - 1);
+        // The tile's first piece (K from 0) ends this CTA's range, so this CTA usually finishes the
+        // tile last. If every other piece is already in the workspace (their tickets all taken), it
+        // adds them to its own running sum in registers and stores neither its piece nor a ticket.
         if (tid == 2 * 32)
-          flags[1] = aborted ? 0 : (atomicAdd(p.tile_cnt + t, 1) == (int)(c_last - c_first));
+          flags[1] = (!aborted && blockIdx.x == c_first &&
+                      ld_acquire(p.tile_cnt + t) == (int)(c_last - c_first)) ? 2 : 0;
         promo_sync();
+        if (flags[1] == 0) {
+          if (!aborted) {
+            float4* dst = slice(blockIdx.x, t == my_first_tile ? 0 : 1);
+#pragma unroll
+            for (int j = 0; j < kCols / 4; ++j)
+              dst[(size_t)j * kPromo] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+          }
+          __threadfence();
+          promo_sync();
+          if (tid == 2 * 32)
+            flags[1] = aborted ? 0 : (atomicAdd(p.tile_cnt + t, 1) == (int)(c_last - c_first));
+          promo_sync();
+        }
         if (flags[1] != 0) {  // this CTA finished the tile's last piece: add up the pieces
           __threadfence();
-          // every piece (this CTA's too) from the workspace, in CTA order: the sum does
-          // not depend on which CTA finished last, so results are reproducible
+          // every piece in CTA order, the first one taken as it is: the sum does not depend on
+          // which CTA finished last or on which of the two ways it got here, so results repeat
+          // bit for bit (the first piece is this CTA's own running sum when flags[1] is 2)
+          auto piece = [&](long long c2) {
+            return slice(c2, t == (int)((c2 * p.total / G) / p.KB) ? 0 : 1);
+          };
+          if (flags[1] == 1) {
+            const float4* src = piece(c_first);
 #pragma unroll
-          for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
-          for (long long c2 = c_first; c2 <= c_last; ++c2) {
-            const int first_t = (int)((c2 * p.total / G) / p.KB);
-            const float4* src = slice(c2, t == first_t ? 0 : 1);
+            for (int j = 0; j < kCols / 4; ++j) {
+              const float4 v = __ldcg(src + (size_t)j * kPromo);
+              acc[4 * j] = v.x; acc[4 * j + 1] = v.y; acc[4 * j + 2] = v.z; acc[4 * j + 3] = v.w;
+            }
+          }
+          for (long long c2 = c_first + 1; c2 <= c_last; ++c2) {
+            const float4* src = piece(c2);
 #pragma unroll
             for (int j = 0; j < kCols / 4; ++j) {
               const float4 v = __ldcg(src + (size_t)j * kPromo);
               acc[4 * j] += v.x; acc[4 * j + 1] += v.y; acc[4 * j + 2] += v.z; acc[4 * j + 3] += v.w;
             }
           }
-          if (live) {
-#pragma unroll
-            for (int j = 0; j < kCols / 8; ++j) {
-              float v[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = acc[8 * j + e];
-              store_row8(out_row, res_row, n0 + 8 * j, p.N, v);
-            }
-          }
+          if (live) store_row64(out_row, res_row, n0, p.N, acc);
           if (tid == 2 * 32) p.tile_cnt[t] = 0;
         }
         promo_sync();  // flags[1] is rewritten by the next piece
@@ -733,8 +766,10 @@ int wide_resident_clusters(int csize) {
 //  - at most one wave: the wide kernel with K split over clusters of `split`
 //    CTAs (split 1: one CTA per tile), as many parts as leave every part at
 //    least four K blocks and let all the clusters run at once;
-//  - in between: the 128 x 128 kernel, stream-K (equal K-block ranges) when its
-//    tiles make fewer than two waves.
+//  - in between: the 128 x 128 kernel, stream-K (equal K-block ranges) when the
+//    last wave of whole tiles would leave SMs idle for longer than the exchange
+//    of partial tiles costs (320 tiles on 152 SMs: 3 waves of 48 blocks, or
+//    102 blocks each and the exchange).
 struct Plan8 {
   int kind;  // 0: 128 x 128 kernel, 1: wide persistent, 2: wide, one wave, split K
   int split;
@@ -742,6 +777,10 @@ struct Plan8 {
   long long tiles, total;
   int grid;
 };
+
+// The partial-tile exchange of a stream-K CTA (its partial sums to L2, the last CTA of a tile
+// adding them up) costs about as much as this many K blocks of MMAs and folding.
+constexpr int kStreamKFixupBlocks = 16;
 
 Plan8 plan_fp8(int T, int N, int K, int sms) {
   Plan8 pl{};
@@ -770,7 +809,11 @@ Plan8 plan_fp8(int T, int N, int K, int sms) {
   pl.split = 1;
   pl.tiles = (long long)((T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   pl.total = pl.tiles * KB;
-  pl.stream_k = pl.tiles < 2LL * sms && pl.total > pl.tiles;
+  // whole tiles take ceil(tiles / sms) waves of KB blocks each; stream-K takes an equal share of all
+  // K blocks per CTA plus the partial-tile exchange (counted as kStreamKFixupBlocks K blocks)
+  const long long whole_blocks = (pl.tiles + sms - 1) / sms * KB;
+  const long long sk_blocks = (pl.total + sms - 1) / sms + kStreamKFixupBlocks;
+  pl.stream_k = pl.total > pl.tiles && sk_blocks < whole_blocks;
   const long long work = pl.stream_k ? pl.total : pl.tiles;
   pl.grid = (int)(work < sms ? work : sms);
   return pl;

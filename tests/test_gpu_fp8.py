@@ -1,9 +1,10 @@
 """Block-scaled FP8 projections (the checkpoint format of section 04 of the Qwen3.8-27B page:
 E4M3 weights with one scale per 128 x 128 block, activations quantised per token and 128-wide
 group) against the fp64 oracle: the quantisers bit for bit (codes and scales, including every E4M3
-rounding boundary), the tcgen05 GEMM element by element over ragged shapes, the stream-K path at
-the layer's decode shapes, the 128 x 256 wide-tile path at prefill-like token counts, reuse of the
-workspace without clearing, and quantise-then-multiply end to end."""
+rounding boundary), the tcgen05 GEMM element by element over ragged shapes, the K split over
+clusters at the layer's decode shapes, the stream-K path at mid-sized token counts, the 128 x 256
+wide-tile path at prefill-like token counts, reuse of the workspace without clearing, and
+quantise-then-multiply end to end."""
 import numpy as np
 import pytest
 import torch
@@ -214,13 +215,15 @@ def test_fp8_linear_wide_tiles(b, T, K, N, res):
     (64, 6144, 5136, False, True),     # 21 tiles, the last one 16 outputs wide; K split 4 ways
     (256, 6144, 5120, True, False),    # Wo at the decode batch without a workspace: one CTA per tile
     (1000, 256, 5120, True, True),     # 160 tiles of 128 x 256: the 128 x 128 kernel, whole tiles
-    (12800, 256, 384, False, True),    # 200 tiles of 128 x 256, 300 of 128 x 128: the stream-K schedule
+    (12800, 256, 384, False, True),    # 300 tiles of 128 x 128 in two nearly full waves: whole tiles
+    (1000, 6144, 5120, True, True),    # Wo, 320 tiles: stream-K, 101 - 102 K blocks (three tiles) per CTA
+    (1536, 3072, 5120, False, True),   # 480 tiles: stream-K, ranges holding whole tiles between two pieces
 ])
 def test_fp8_linear_schedules(b, T, K, N, res, with_ws):
     """Each schedule of gdn_fp8_linear on a 152-SM GB300, picked by the number of 128 x 256 output
     tiles: at most one wave splits K over clusters (the parts meet in the workspace, in part order),
-    between one and two waves takes 128 x 128 tiles (whole tiles, or stream-K when they make fewer
-    than two waves); two calls in a row give the same bits."""
+    between one and two waves takes 128 x 128 tiles (whole tiles, or stream-K when the last wave of
+    whole tiles would leave SMs idle); two calls in a row give the same bits."""
     x8, xs, w8, ws, r = _operands(T, K, N, 520 + T + N)
     wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda") if with_ws else None
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
