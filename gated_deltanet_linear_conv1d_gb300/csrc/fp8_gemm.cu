@@ -37,6 +37,7 @@
 
 #include "device.cuh"
 #include "launch.h"
+#include "pair.cuh"
 #include "umma.cuh"
 
 namespace gdn {
@@ -407,6 +408,12 @@ constexpr int kWN = 256;
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = kTileBytes + kWN * kBK;   // 16 KB of X rows + 32 KB of W rows
 constexpr int kWBarOff = kWStages * kWStageBytes;
+// CTA pairs (kPair): a cluster of 2 takes 256 tokens x 256 outputs, the even CTA
+// issuing M = 256 pair MMAs; each CTA's stage holds its own 128 X rows and one
+// half (128 rows) of the W tile, 32 KB instead of 48, in a 6-deep ring.
+constexpr int kPStages = 6;
+constexpr int kPStageBytes = 2 * kTileBytes;
+static_assert(kPStages * kPStageBytes == kWBarOff, "both rings end where the barriers start");
 // Epilogue stage of whole tiles: each promotion warp turns its 32 token rows x
 // 128 outputs around 32 outputs at a time through [32 rows][33 floats] (the odd
 // stride keeps both the row-wise writes and the piece-wise reads free of bank
@@ -420,103 +427,141 @@ constexpr int kWSmemBytes = kWStgOff + kWStgBytes + 1024;
 static_assert(kWSmemBytes <= 227 * 1024, "wide kernel shared memory");
 constexpr int kWScaleAhead = 2;  // fewer registers than the narrow kernel: the sum takes 128
 constexpr uint32_t kWIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kWN);
+constexpr uint32_t kPIdesc = umma::idesc(umma::kE4M3, false, false, 2 * kBM, kWN);
 constexpr int kMaxSplitW = 4;  // parts of K per tile at most
 
-// All threads of every CTA of the cluster; orders the memory accesses before it
-// (release) against those after it (acquire) at cluster scope.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
+// kPair = false: one CTA per 128 x 256 tile (persistent, or K split over a
+// cluster); kPair = true: persistent CTA pairs (clusters of 2) over 256 x 256
+// pair tiles, p.split = 1. Either way each CTA folds and stores its own 128
+// token rows x 256 outputs; the pair only shares the W tile's loads: every
+// stage both CTAs' copies complete on the even CTA's `full` barrier, the even
+// CTA's MMA completion is multicast to both CTAs' `empty` and `tfull`
+// barriers, and both CTAs' promotion warps arrive on the even CTA's `tempty`.
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8GemmArgs p,
                                                                      const __grid_constant__ CUtensorMap tmx,
                                                                      const __grid_constant__ CUtensorMap tmw) {
+  constexpr int kStg = kPair ? kPStages : kWStages;
+  constexpr int kStgBytes = kPair ? kPStageBytes : kWStageBytes;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWBarOff);  // [kWStages] TMA -> MMA
-  uint64_t* empty = full + kWStages;                                // [kWStages] MMA -> TMA
-  uint64_t* tfull = empty + kWStages;                               // [2] K block's product ready
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWBarOff);  // [kStg] TMA -> MMA
+  uint64_t* empty = full + kStg;                                    // [kStg] MMA -> TMA
+  uint64_t* tfull = empty + kStg;                                   // [2] K block's product ready
   uint64_t* tempty = tfull + 2;                                     // [2] K block's product folded
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);               // [0] abort
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kWStages; ++s) {
+    for (int s = 0; s < kStg; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kPromoWarps);
+      mbar_init(&tempty[b], (kPair ? 2 : 1) * kPromoWarps);
     }
     flags[0] = 0;
     fence_mbar_init();
   }
-  if (warp == 1) umma::tmem_alloc(tmem_slot, 512);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_alloc_pair(tmem_slot, 512);
+    else umma::tmem_alloc(tmem_slot, 512);
+  }
   umma::fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers exist before either copies or arrives on them
   umma::fence_after_sync();
   const uint32_t tm = *tmem_slot;
   volatile int* abort_flag = flags;
   const int nt = (p.N + kWN - 1) / kWN;
-  const int tiles = p.mt * nt;  // the launcher keeps this below 2^31
-  // split == 1: persistent CTAs take whole tiles blockIdx.x, + gridDim.x, ...;
+  // pair member (0: the even CTA, which issues the MMAs) and the pair's barrier addresses
+  const int pr = kPair ? (int)(cluster_ctarank() & 1u) : 0;
+  // tiles: 128 x 256 (kPair false) or pair tiles of 256 x 256 (the launcher keeps the count below 2^31)
+  const int tiles = kPair ? ((p.mt + 1) / 2) * nt : p.mt * nt;
+  // split == 1: persistent CTAs (pairs) take whole tiles first, first + step, ...;
   // split > 1: this CTA takes part `part` of tile blockIdx.x / split, K blocks kb_lo .. kb_hi-1
-  const int split = p.split;
+  const int split = kPair ? 1 : p.split;
   const int part = split > 1 ? (int)(blockIdx.x % (unsigned)split) : 0;
-  const int t_first = split > 1 ? (int)(blockIdx.x / (unsigned)split) : (int)blockIdx.x;
-  const int t_step = split > 1 ? tiles : (int)gridDim.x;
+  const int t_first = kPair ? (int)(blockIdx.x >> 1) : (split > 1 ? (int)(blockIdx.x / (unsigned)split) : (int)blockIdx.x);
+  const int t_step = kPair ? (int)(gridDim.x >> 1) : (split > 1 ? tiles : (int)gridDim.x);
   const int kb_lo = part * p.KB / split, kb_hi = (part + 1) * p.KB / split;
+  // this CTA's 128-row token tile of tile t
+  auto m_tile = [&](int t) { return kPair ? 2 * (t / nt) + pr : t / nt; };
 
   if (warp == 0) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+      uint64_t keep = 0, normal = 0;
+      if constexpr (kPair) {
+        keep = l2_policy_evict_last();  // W: every token tile of the wave reads it
+        normal = l2_policy_evict_normal();
+      }
       uint32_t gk = 0;
       bool ok = true;
       for (int t = t_first; t < tiles && ok; t += t_step) {
-        const int m_t = t / nt, n_t = t % nt;
+        const int m_t = m_tile(t), n_t = t % nt;
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++gk) {
-          const int s = gk % kWStages;
-          if ((gk >= (uint32_t)kWStages && !mbar_wait_bounded(&empty[s], ((gk / kWStages) - 1) & 1)) ||
-              *abort_flag) {
+          const int s = gk % kStg;
+          if ((gk >= (uint32_t)kStg && !mbar_wait_bounded(&empty[s], ((gk / kStg) - 1) & 1)) || *abort_flag) {
             ok = false;
             break;
           }
-          unsigned char* st = smem + s * kWStageBytes;
-          mbar_arrive_expect_tx(&full[s], kWStageBytes);
-          tma_load_2d(st, &tmx, kb * kBK, m_t * kBM, &full[s]);
-          tma_load_2d(st + kTileBytes, &tmw, kb * kBK, n_t * kWN, &full[s]);
+          unsigned char* st = smem + s * kStgBytes;
+          if constexpr (kPair) {
+            // both CTAs' copies count on the even CTA's barrier, which expects the bytes of both
+            const uint32_t fb = cluster_addr(&full[s], 0);
+            if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kPStageBytes);
+            tma_load_2d_pair(st, &tmx, kb * kBK, m_t * kBM, fb, normal);
+            tma_load_2d_pair(st + kTileBytes, &tmw, kb * kBK, n_t * kWN + pr * (kWN / 2), fb, keep);
+          } else {
+            mbar_arrive_expect_tx(&full[s], kWStageBytes);
+            tma_load_2d(st, &tmx, kb * kBK, m_t * kBM, &full[s]);
+            tma_load_2d(st + kTileBytes, &tmw, kb * kBK, n_t * kWN, &full[s]);
+          }
         }
       }
       if (!ok) {
         report(p.dev_err, GDN_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        for (uint32_t j = (gk > (uint32_t)kWStages ? gk - kWStages : 0); j < gk; ++j)
-          mbar_wait_bounded(&full[j % kWStages], (j / kWStages) & 1);
+        // copies still in flight land before the CTA goes on (bounded waits; with
+        // pairs the even CTA holds the barriers that count them)
+        if (!kPair || pr == 0)
+          for (uint32_t j = (gk > (uint32_t)kStg ? gk - kStg : 0); j < gk; ++j)
+            mbar_wait_bounded(&full[j % kStg], (j / kStg) & 1);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && pr == 0) {
       uint32_t gk = 0;
       bool ok = true;
       for (int t = t_first; t < tiles && ok; t += t_step) {
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++gk) {
-          const int s = gk % kWStages;
+          const int s = gk % kStg;
           const uint32_t b = gk & 1, use = gk >> 1;
-          if (!mbar_wait_bounded(&full[s], (gk / kWStages) & 1) ||
+          if (!mbar_wait_bounded(&full[s], (gk / kStg) & 1) ||
               (gk >= 2 && !mbar_wait_bounded(&tempty[b], (use - 1) & 1)) || *abort_flag) {
             ok = false;
             break;
           }
           umma::fence_after_sync();
-          const uint32_t sx = smem_u32(smem + s * kWStageBytes), sw = sx + kTileBytes;
+          const uint32_t sx = smem_u32(smem + s * kStgBytes), sw = sx + kTileBytes;
+          if constexpr (kPair) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk)
-            umma::mma<umma::kKindF8>(tm + b * kWN, umma::smem_desc_sw128(sx + kk * 32),
-                                     umma::smem_desc_sw128(sw + kk * 32), kWIdesc, kk > 0);
-          umma::commit(&empty[s]);
-          umma::commit(&tfull[b]);
+            for (int kk = 0; kk < kBK / 32; ++kk)
+              mma_pair<true>(tm + b * kWN, umma::smem_desc_sw128(sx + kk * 32), umma::smem_desc_sw128(sw + kk * 32),
+                             kPIdesc, kk > 0);
+            commit_pair(&empty[s], 3);  // the stage may be refilled in both CTAs
+            commit_pair(&tfull[b], 3);  // both CTAs may fold their rows of the block product
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 32; ++kk)
+              umma::mma<umma::kKindF8>(tm + b * kWN, umma::smem_desc_sw128(sx + kk * 32),
+                                       umma::smem_desc_sw128(sw + kk * 32), kWIdesc, kk > 0);
+            umma::commit(&empty[s]);
+            umma::commit(&tfull[b]);
+          }
         }
       }
       if (!ok) {
@@ -531,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
     const int NB = (p.N + 127) / 128;
     uint32_t gk = 0;
     for (int t = t_first; t < tiles; t += t_step) {
-      const int m_t = t / nt, n_t = t % nt;
+      const int m_t = m_tile(t), n_t = t % nt;
       const int row = m_t * kBM + 32 * q + lane;
       const bool live = row < p.T;
       const int nb = min(2 * n_t + h, NB - 1);  // weight-scale block of this half
@@ -592,7 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
         }
         umma::fence_before_sync();
         __syncwarp();
-        if (lane == 0) arrive_one(&tempty[b]);
+        if (lane == 0) {
+          if constexpr (kPair) arrive_cluster(cluster_addr(&tempty[b], 0));  // the even CTA may refill the buffer
+          else arrive_one(&tempty[b]);
+        }
       }
       if (split == 1) {
         // ---- whole tile: out (+ residual) through the warp's stage (see kWStgLd)
@@ -666,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
       __threadfence();
       __syncwarp();
       cluster_sync_all();
-      const int t = t_first, m_t = t / nt, n_t = t % nt;
+      const int t = t_first, m_t = m_tile(t), n_t = t % nt;
       const int r0 = part * kBM / split, nrows = (part + 1) * kBM / split - r0;
       const int items = nrows * (kWN / 8);
       const float4* base = reinterpret_cast<const float4*>(p.partial) + (size_t)t * split * (kBM * kWN / 4);
@@ -730,8 +778,16 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_gemm_wide_kernel(const Fp8Gem
 
   umma::fence_before_sync();
   __syncthreads();
-  umma::fence_after_sync();
-  if (warp == 1) umma::tmem_dealloc(tm, 512);
+  if constexpr (kPair) {
+    // neither CTA leaves while its partner may still copy into it, read its
+    // shared memory in an MMA, or arrive on its barriers
+    cluster_sync_all();
+    umma::fence_after_sync();
+    if (warp == 1) tmem_dealloc_pair(tm, 512);
+  } else {
+    umma::fence_after_sync();
+    if (warp == 1) umma::tmem_dealloc(tm, 512);
+  }
 }
 
 bool encode_u8(CUtensorMap* m, const void* base, int rows, int cols, int box_rows = 128) {
@@ -755,14 +811,23 @@ int num_sms() {
 
 // Clusters of `csize` CTAs of the wide kernel that fit on the GPU at once.
 int wide_resident_clusters(int csize) {
-  if (ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes) != cudaSuccess) return 0;
-  return resident_clusters(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kThreads, kWSmemBytes, csize);
+  const void* fn = reinterpret_cast<const void*>(fp8_gemm_wide_kernel<false>);
+  if (ensure_dynamic_smem(fn, kWSmemBytes) != cudaSuccess) return 0;
+  return resident_clusters(fn, kThreads, kWSmemBytes, csize);
+}
+
+// CTA pairs of the pair kernel that fit on the GPU at once.
+int pair_resident_clusters() {
+  const void* fn = reinterpret_cast<const void*>(fp8_gemm_wide_kernel<true>);
+  if (ensure_dynamic_smem(fn, kWSmemBytes) != cudaSuccess) return 0;
+  return resident_clusters(fn, kThreads, kWSmemBytes, 2);
 }
 
 }  // namespace
 
 // Schedules, by the number of 128 x 256 tiles:
-//  - at least two waves: the wide kernel, persistent over whole tiles;
+//  - at least two waves: the wide kernel, persistent CTA pairs over whole 256 x
+//    256 pair tiles (persistent single CTAs if no pair fits);
 //  - at most one wave: the wide kernel with K split over clusters of `split`
 //    CTAs (split 1: one CTA per tile), as many parts as leave every part at
 //    least four K blocks and let all the clusters run at once;
@@ -773,6 +838,7 @@ int wide_resident_clusters(int csize) {
 struct Plan8 {
   int kind;  // 0: 128 x 128 kernel, 1: wide persistent, 2: wide, one wave, split K
   int split;
+  bool pair;  // kind 1: CTA pairs (grid = 2 x pairs)
   bool stream_k;
   long long tiles, total;
   int grid;
@@ -791,6 +857,12 @@ Plan8 plan_fp8(int T, int N, int K, int sms) {
     pl.split = 1;
     pl.tiles = wide_tiles;
     pl.grid = sms;
+    const long long pair_tiles = (long long)((T + 2 * kBM - 1) / (2 * kBM)) * ((N + kWN - 1) / kWN);
+    const int pairs = pair_resident_clusters();
+    if (pairs > 0) {
+      pl.pair = true;
+      pl.grid = 2 * (int)(pair_tiles < pairs ? pair_tiles : pairs);
+    }
     return pl;
   }
   if (wide_tiles <= sms) {
@@ -844,17 +916,34 @@ cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_byt
   a.KB = o.K / kBK;
   a.mt = (o.T + kBM - 1) / kBM;
   a.split = 1;
+  if (pl.pair) {  // persistent CTA pairs: each CTA loads half (128 rows) of the W tile
+    CUtensorMap tmx{}, tmw{};
+    if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K, kWN / 2)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fp8_gemm_wide_kernel<true>, a, tmx, tmw);
+  }
   if (pl.kind != 0) {  // 128 x 256 tiles
     CUtensorMap tmx{}, tmw{};
     if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K, kWN)) return cudaErrorInvalidValue;
-    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel), kWSmemBytes);
+    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fp8_gemm_wide_kernel<false>), kWSmemBytes);
     if (err != cudaSuccess) return err;
     if (pl.kind == 2 && pl.split > 1 && !room) {  // no room for the parts: one CTA per tile
       pl.split = 1;
       pl.grid = (int)pl.tiles;
     }
     if (pl.split == 1) {
-      fp8_gemm_wide_kernel<<<pl.grid, kThreads, kWSmemBytes, stream>>>(a, tmx, tmw);
+      fp8_gemm_wide_kernel<false><<<pl.grid, kThreads, kWSmemBytes, stream>>>(a, tmx, tmw);
       return cudaGetLastError();
     }
     a.split = pl.split;
@@ -871,7 +960,7 @@ cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_byt
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fp8_gemm_wide_kernel, a, tmx, tmw);
+    return cudaLaunchKernelEx(&cfg, fp8_gemm_wide_kernel<false>, a, tmx, tmw);
   }
   CUtensorMap tmx{}, tmw{};
   if (!encode_u8(&tmx, o.x8, o.T, o.K) || !encode_u8(&tmw, o.w8, o.N, o.K)) return cudaErrorInvalidValue;

@@ -26,8 +26,8 @@
 // CTA pairs: the two CTAs of a pair (a cluster of 2, or the pairs of a larger
 // cluster) compute two tiles with the same B operand (two token tiles of one
 // weight tile; when swapped, two weight tiles of the one token tile). Each
-// loads its own A tile and one half of B, multicast by TMA into both CTAs'
-// shared memory, so a CTA pulls 32 KB from L2 per K slice instead of 48 KB (at
+// loads its own A tile and one half of B into its own shared memory (the pair
+// MMA reads B from both), so a CTA pulls 32 KB from L2 per K slice instead of 48 KB (at
 // the MMA rate the unpaired kernel would need about 22 TB/s from L2 over the
 // GPU). A stage is refilled only when both CTAs' MMAs are done with it: the
 // MMA completion arrives on the stage's barrier in both CTAs.
@@ -45,6 +45,7 @@
 
 #include "device.cuh"
 #include "launch.h"
+#include "pair.cuh"
 #include "umma.cuh"
 
 namespace gdn {
@@ -79,16 +80,6 @@ constexpr int kMaxSplit = 4;
 constexpr int kPadNormal = kBN + 4, kPadSwap = kBM + 4;
 static_assert(kBM * kPadNormal * 4 <= kBarOff && kBN * kPadSwap * 4 <= kBarOff, "partial tile overruns the ring");
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // The 16 bytes at the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ float4 ld_cluster_v4(const float* local, uint32_t rank) {
   uint32_t a;
@@ -99,50 +90,6 @@ __device__ __forceinline__ float4 ld_cluster_v4(const float* local, uint32_t ran
                : "r"(a)
                : "memory");
   return v;
-}
-
-// TMA tile load into this CTA's shared memory whose completion is counted on
-// `bar_cluster`, a barrier of the pair (a shared::cluster address, here the even
-// CTA's), with an L2 eviction-priority policy.
-__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int x, int y, uint32_t bar_cluster,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
-      : "memory");
-}
-
-// shared::cluster address of the same shared-memory location in CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
-  return a;
-}
-
-// One arrival on a barrier given by its shared::cluster address (possibly another CTA's).
-__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
-}
-
-// Arrives once on `bar` in both CTAs of the pair (`mask`) when the pair's MMAs
-// issued so far by this thread have completed.
-__device__ __forceinline__ void commit_pair(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                   "r"(smem_u32(bar)), "h"(mask)
-               : "memory");
-}
-
-// One MMA of the pair: D (this CTA's and the partner's tensor memory at the same
-// address, 128 rows each) (+)= A (128 rows from each CTA's shared memory at the
-// descriptor's address) B^T (N/2 rows from each); issued by the even CTA.
-__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // Output segment and tile of a tile index: tiles run m-tile major, then over
@@ -281,12 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     flags[0] = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {  // one allocation for the pair: a warp of each CTA takes part
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(2 * kBN)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 2 * kBN);  // one allocation for the pair: a warp of each CTA takes part
   umma::fence_before_sync();
   __syncthreads();
   cluster_sync_all();  // every CTA's barriers are initialised before the partner copies or arrives on them
@@ -398,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kTileA;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_pair(tm + b * kBN, umma::smem_desc_sw128(sa + kk * 32), umma::smem_desc_sw128(sb + kk * 32), idesc,
+            mma_pair<false>(tm + b * kBN, umma::smem_desc_sw128(sa + kk * 32), umma::smem_desc_sw128(sb + kk * 32), idesc,
                      (kb > kb_lo || kk > 0) ? 1u : 0u);
           commit_pair(&empty[s], pair_mask);  // the stage may be refilled in both CTAs
         }
@@ -566,8 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   // barriers, or a peer may still read its partial tile
   cluster_sync_all();
   umma::fence_after_sync();
-  if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(2 * kBN) : "memory");
+  if (warp == 1) tmem_dealloc_pair(tm, 2 * kBN);
 }
 
 // bf16 [rows][cols] tensor map, box 64 columns x box_rows rows, 128-byte swizzle.
