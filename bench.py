@@ -884,9 +884,9 @@ def measure_fp8_proj(b, dev, stream) -> dict:
         torch.cuda.empty_cache()
     return {"workload": "E4M3 weights, one fp32 scale per 128x128 block; activations quantised per token and "
                         "128-wide group (gdn_fp8_quant_act) then gdn_fp8_linear; ms = quantise + GEMM(s)",
-            "kernel": "fp8_gemm_wide_kernel (128 x 256 tiles; persistent at prefill token counts, each tile's K "
-                      "blocks split over a cluster at decode token counts): tcgen05 kind::f8f6f4, per-block "
-                      "promotion in registers",
+            "kernel": "fp8_gemm_wide_kernel (128 x 256 tiles per CTA; at prefill token counts persistent CTA "
+                      "pairs issuing cta_group::2 MMAs of 256 x 256, at decode token counts each tile's K blocks "
+                      "split over a cluster): tcgen05 kind::f8f6f4, per-block promotion in registers",
             "peak_fp8_tflops": p_fp8, "peak_kind": f"2 x {kind} bf16 burst (nominal fp8/bf16 ratio)",
             "hbm_peak_gbs": hbm_peak, **res}
 
