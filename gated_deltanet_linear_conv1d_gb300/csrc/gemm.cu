@@ -179,14 +179,20 @@ __device__ __forceinline__ void store32(const GemmSeg& g, bool swap, int arow, i
     if (i < ncols) g.out_bf16[(size_t)(n0 + i) * g.N + arow] = f32_to_bf16(v[i] + r[i]);
 }
 
-// Four consecutive outputs (token `row`, outputs n .. n+3, n a multiple of 4) + residual.
-__device__ __forceinline__ void store4(const GemmSeg& g, int row, int n, float4 v) {
+// The residual of four consecutive outputs (token `row`, outputs n .. n+3), or zeros.
+__device__ __forceinline__ uint2 residual4(const GemmSeg& g, int row, int n) {
+  return (!g.out_f32 && g.residual) ? *reinterpret_cast<const uint2*>(g.residual + (size_t)row * g.N + n)
+                                    : make_uint2(0u, 0u);
+}
+
+// Four consecutive outputs (token `row`, outputs n .. n+3, n a multiple of 4) + their
+// residual r, loaded by residual4 before any store that might overwrite it.
+__device__ __forceinline__ void store4(const GemmSeg& g, int row, int n, float4 v, uint2 r) {
   if (g.out_f32) {
     *reinterpret_cast<float4*>(g.out_f32 + (size_t)row * g.N + n) = v;
     return;
   }
   if (g.residual) {
-    const uint2 r = *reinterpret_cast<const uint2*>(g.residual + (size_t)row * g.N + n);
     v.x += bf16_to_f32(r.x & 0xffff);
     v.y += bf16_to_f32(r.x >> 16);
     v.z += bf16_to_f32(r.y & 0xffff);
@@ -487,17 +493,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       const int C4 = (p.swap ? kBM : kBN) / 4;  // tile columns (outputs) in groups of 4
       const int row_lo = rs * R / split, row_hi = (rs + 1) * R / split;
       const int items = (row_hi - row_lo) * C4;
-      for (int i = tid; i < items; i += kThreads) {
-        const int rr = row_lo + i / C4, cc = 4 * (i % C4);
-        const int token = p.swap ? rr : tr.m_t * kBM + rr;
-        const int n = (p.swap ? tr.n_t * kBM : tr.n_t * kBN) + cc;
-        const float* src = part + rr * ld + cc;
-        float4 acc = ld_cluster_v4(src, (uint32_t)pr);
-        for (int q2 = 1; q2 < split; ++q2) {
-          const float4 x = ld_cluster_v4(src, (uint32_t)(pr + 2 * q2));
-          acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+      // a thread's kItems items (4 outputs each) at a time: the K parts of all of them
+      // (distributed shared memory) and their residual are loaded before any sum or
+      // store, so the round trips overlap instead of following one another
+      constexpr int kItems = 4;
+      for (int i0 = tid; i0 < items; i0 += kItems * kThreads) {
+        float4 pv[kItems][kMaxSplit];
+        uint2 res[kItems];
+        int tok[kItems], nn[kItems];
+        bool live[kItems];
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) {
+          const int i = i0 + u * kThreads;
+          const int ii = i < items ? i : i0;  // an item in range for the loads
+          const int rr = row_lo + ii / C4, cc = 4 * (ii % C4);
+          tok[u] = p.swap ? rr : tr.m_t * kBM + rr;
+          nn[u] = (p.swap ? tr.n_t * kBM : tr.n_t * kBN) + cc;
+          live[u] = i < items && tok[u] < p.T && nn[u] < g.N;
+          const float* src = part + rr * ld + cc;
+#pragma unroll
+          for (int q2 = 0; q2 < kMaxSplit; ++q2)
+            if (q2 < split) pv[u][q2] = ld_cluster_v4(src, (uint32_t)(pr + 2 * q2));
+          res[u] = live[u] ? residual4(g, tok[u], nn[u]) : make_uint2(0u, 0u);
         }
-        if (token < p.T && n < g.N) store4(g, token, n, acc);
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) {
+          if (!live[u]) continue;
+          float4 acc = pv[u][0];  // the parts in rank order: the same bits whichever CTA ran first
+#pragma unroll
+          for (int q2 = 1; q2 < kMaxSplit; ++q2)
+            if (q2 < split) {
+              acc.x += pv[u][q2].x; acc.y += pv[u][q2].y; acc.z += pv[u][q2].z; acc.w += pv[u][q2].w;
+            }
+          store4(g, tok[u], nn[u], acc, res[u]);
+        }
       }
     }
   }

@@ -196,9 +196,11 @@ def test_fp8_linear_decode_batches(b, T, K, N, res):
     (39000, 128, 144, True),    # 305 row tiles of one ragged column tile (N = 144 < 256)
 ])
 def test_fp8_linear_wide_tiles(b, T, K, N, res):
-    """Token counts with at least two waves of 128 x 256 tiles take the wide-tile kernel (the running
-    sum in tensor memory, the two 128-column halves folded in turn): ragged rows and columns, a half
-    tile past the last column, several tiles per CTA; called twice on the same buffers."""
+    """Token counts with at least two waves of 128 x 256 tiles take the wide kernel on persistent CTA
+    pairs (each pair multiplies 256 tokens x 256 outputs with M = 256 pair MMAs, each CTA folding its
+    own 128 rows in registers): ragged rows and columns, a half tile past the last column, an odd
+    number of row tiles (the last pair's second CTA has no rows: 9800 and 39000 tokens), several
+    tiles per CTA; called twice on the same buffers."""
     x8, xs, w8, ws, r = _operands(T, K, N, 490 + T + N)
     out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
     wsp = torch.zeros(max(256, b.gdn_fp8_linear_workspace_bytes(T, K, N)), dtype=torch.uint8, device="cuda")
@@ -236,3 +238,17 @@ def test_fp8_linear_schedules(b, T, K, N, res, with_ws):
     assert b.gdn_read_device_error(err) == 0
     assert torch.equal(outs[0], outs[1])
     U.check_out(U.host_f64_from_bf16(outs[0]), oracle.fp8_linear(x8, xs, w8, ws, r if res else None), "out")
+
+
+@pytest.mark.parametrize("T", [4836, 4964])
+def test_fp8_linear_pairs_in_place(b, T):
+    """The CTA-pair schedule with out = residual (the residual stream updated in place): 38 row tiles,
+    and 39 (the last pair's second CTA past T); the residual pieces of each stage are loaded before
+    its stores, so no store overwrites a residual value still to be read."""
+    K, N = 384, 2048
+    x8, xs, w8, ws, r = _operands(T, K, N, 530 + T)
+    hidden = U.dev_bf16(r)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.gdn_fp8_linear(_dev_u8(x8), U.dev(xs), _dev_u8(w8), U.dev(ws), hidden, residual=hidden, dev_err=err)
+    assert b.gdn_read_device_error(err) == 0
+    U.check_out(U.host_f64_from_bf16(hidden), oracle.fp8_linear(x8, xs, w8, ws, r), "in place")

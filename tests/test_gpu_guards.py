@@ -151,10 +151,11 @@ def test_standalone_kernels_write_nothing_outside_their_outputs(b):
     u.check("rmsnorm out")
 
 
-@pytest.mark.parametrize("T", [3, 256, 1000])
+@pytest.mark.parametrize("T", [3, 256, 1000, 19500])
 def test_projections_write_nothing_outside_their_outputs(b, T):
     """Wo (both tile shapes and the cluster split of the decode size), the three in_proj outputs, and
-    the FP8 path (quantisers and GEMM, whose decode-sized split uses the workspace)."""
+    the FP8 path (quantisers and GEMM: the decode-sized split through the workspace, and at 19,500
+    tokens the CTA-pair schedule over an odd number of row tiles)."""
     rng = np.random.default_rng(86 + T)
     K, N = 512, 384
     a = U.dev_bf16(synth.bf16_bits(rng.standard_normal((T, K)).astype(np.float32)))
