@@ -14,19 +14,22 @@
 // of the folding.
 //
 // Schedules, by the number of 128 x 256 output tiles. With at least two waves of
-// them (prefill token counts) fp8_gemm_wide_kernel below takes 128 tokens x 256
-// outputs per tile (N = 256 MMAs, two 256-column buffers) on persistent CTAs.
-// With at most one wave (decode batches) the same kernel splits each tile's K
-// blocks over a cluster of CTAs, which add their parts through the workspace
-// (see the kernel). In between, fp8_gemm_kernel takes 128 x 128 tiles: with at
-// least two waves of those a persistent CTA takes whole tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... and stores bf16 rows directly. With fewer tiles
-// the K blocks of all tiles, laid end to end, are cut into gridDim.x equal
+// them (prefill token counts) fp8_gemm_wide_kernel below runs on persistent CTA
+// pairs: a pair takes 256 tokens x 256 outputs with M = 256 pair MMAs
+// (cta_group::2), each CTA loading its own 128 token rows and half of the W
+// tile, and folding and storing its own 128 x 256 outputs (two 256-column
+// buffers). With at most one wave (decode batches) the same kernel, unpaired,
+// splits each tile's K blocks over a cluster of CTAs, which add their parts
+// through the workspace (see the kernel). In between, fp8_gemm_kernel takes
+// 128 x 128 tiles: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... on
+// persistent CTAs, stored as bf16 rows directly, unless the last wave of whole
+// tiles would leave SMs idle for longer than the exchange below costs. Then the
+// K blocks of all tiles, laid end to end, are cut into gridDim.x equal
 // contiguous ranges (stream-K), so every SM does the same work; a CTA stores the
 // fp32 partial of a tile it covers only in part into its own workspace slice
 // (plain coalesced stores), and the CTA that finishes a tile's last piece (an
-// atomic ticket, no waiting) adds the other pieces, stores the bf16 tile and
-// resets the ticket.
+// atomic ticket, no waiting) adds the pieces in CTA order, stores the bf16 tile
+// and resets the ticket.
 //
 // Warp roles (320 threads): warp 0 lane 0 issues the TMA copies into a 4-stage
 // ring (X8 and W8 tiles, 128 B x 128 rows each, 128-byte swizzle), warp 1
