@@ -129,7 +129,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // other warps form Y).
 __device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Waits for an MMA-completion phase; the verdict is uniform over the CTA.
+// Waits for an MMA-completion phase; the outcome is uniform over the CTA.
 __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity) {
   const int ok = __syncthreads_and(mbar_wait_bounded(bar, parity) ? 1 : 0);
   umma::fence_after_sync();
