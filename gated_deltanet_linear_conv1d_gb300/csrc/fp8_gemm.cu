@@ -428,6 +428,10 @@ constexpr int kWStgOff = kWBarOff + 256;
 constexpr int kWStgBytes = kPromoWarps * 32 * kWStgLd * 4;
 constexpr int kWSmemBytes = kWStgOff + kWStgBytes + 1024;
 static_assert(kWSmemBytes <= 227 * 1024, "wide kernel shared memory");
+// Launches that split K never store a whole tile: they take the ring (which also
+// holds their own band of partial sums) and the barriers only, and leave the rest
+// of the SM's storage to L1.
+constexpr int kWSplitSmemBytes = kWStgOff + 1024;
 constexpr int kWScaleAhead = 2;  // fewer registers than the narrow kernel: the sum takes 128
 constexpr uint32_t kWIdesc = umma::idesc(umma::kE4M3, false, false, kBM, kWN);
 constexpr uint32_t kPIdesc = umma::idesc(umma::kE4M3, false, false, 2 * kBM, kWN);
@@ -812,11 +816,12 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-// Clusters of `csize` CTAs of the wide kernel that fit on the GPU at once.
+// Clusters of `csize` CTAs of the wide kernel, launched with K split, that fit on
+// the GPU at once.
 int wide_resident_clusters(int csize) {
   const void* fn = reinterpret_cast<const void*>(fp8_gemm_wide_kernel<false>);
-  if (ensure_dynamic_smem(fn, kWSmemBytes) != cudaSuccess) return 0;
-  return resident_clusters(fn, kThreads, kWSmemBytes, csize);
+  if (ensure_dynamic_smem(fn, kWSmemBytes) != cudaSuccess) return 0;  // the largest launch of this kernel
+  return resident_clusters(fn, kThreads, kWSplitSmemBytes, csize);
 }
 
 // CTA pairs of the pair kernel that fit on the GPU at once.
@@ -954,7 +959,7 @@ cudaError_t launch_fp8_gemm(const Fp8Operands& o, void* workspace, size_t ws_byt
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kWSmemBytes;
+    cfg.dynamicSmemBytes = kWSplitSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
